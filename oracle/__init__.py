@@ -1,0 +1,36 @@
+"""CPU oracle for shared-prefix tree attention (TEST INFRASTRUCTURE ONLY).
+
+This package is the slow, plain, fp64 NumPy statement of what the GPU path
+computes.  It exists to check the CUDA library, never to stand in for it: only
+the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import it.  It shares no code with the CUDA path; both take
+their inputs from the separate ``workloads`` module.
+
+Sources (three web pages about one Megatron-LM feature):
+
+* "[ENHANCEMENT] Shared-prefix training with context parallelism for exact
+  agent trajectories" (issue #7386) -- "Describe the solution you'd like"
+  (DFS segments with parent/depth metadata; attention of each query run
+  against only its ancestor path; only sampled-edge sources projected, one
+  loss owner per sampled action) and "Describe alternatives you've
+  considered" (independent exact-call sequences are the correctness
+  reference).
+* "feat(hybrid): add opt-in shared-prefix attention and Mamba execution"
+  (#7914) -- introduction (prompt K/V reused, each suffix causally isolated,
+  backward accumulates branch contributions into the shared prefix).
+* "TreePackedSeqParams" draft (PR #7387) -- "Summary" (DFS segments, ancestor
+  relationships, causal attention over each query segment's ancestors,
+  edge-source selection before the vocabulary projection, rejection of
+  unsupported input).
+
+Modules: ``tree`` (validation, ancestry, brute-force visibility), ``plan``
+(per-query-tile ancestor KV ranges and the backward KV-block table, derived
+independently of the C++ planner), ``attention`` (leaf-unrolled forward and
+backward, plus the dense tree-mask route for tiny trees), ``gather``
+(sampled-edge selection).
+
+Parity status: every function here is pinned by ``tests/test_oracle.py``
+against brute force, library routines, finite differences or invariants; no
+function is "parity unpinned".
+"""
+from . import tree, plan, attention, gather  # noqa: F401

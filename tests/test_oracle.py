@@ -1,0 +1,354 @@
+"""Pins for the CPU oracle: brute force, library routines, finite differences,
+closed forms and invariants.  Nothing here touches the CUDA library."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+from oracle import gather as OG
+from oracle import plan as OP
+from oracle import tree as OT
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand(rng, T, hq, hkv, D, scale=1.0):
+    q = rng.standard_normal((T, hq, D)) * scale
+    k = rng.standard_normal((T, hkv, D)) * scale
+    v = rng.standard_normal((T, hkv, D)) * scale
+    do = rng.standard_normal((T, hq, D))
+    return q, k, v, do
+
+
+def _sdpa_causal(q, k, v, scale):
+    """torch's own causal attention in fp64 on [T, H, D] arrays (GQA expanded)."""
+    G = q.shape[1] // k.shape[1]
+    qt = torch.tensor(q).permute(1, 0, 2)[None]
+    kt = torch.tensor(k).repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+    vt = torch.tensor(v).repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, is_causal=True, scale=scale)
+    return o[0].permute(1, 0, 2).numpy()
+
+
+def _tree_args(t):
+    return t.seg_start, t.seg_len, t.parent
+
+
+# ---------------------------------------------------------------- tree checks
+
+def test_validate_accepts_generated_configs():
+    for name in ("tiny", "star", "agent", "long"):
+        t = W.get(name).tree
+        OT.validate(t.seg_start, t.seg_len, t.parent, t.depth, t.total_tokens)
+
+
+@pytest.mark.parametrize("mutate,msg", [
+    (lambda a: a["seg_len"].__setitem__(2, 0), "empty"),
+    (lambda a: a["seg_start"].__setitem__(3, 100), "start"),
+    (lambda a: a["parent"].__setitem__(1, 3), "parent"),
+    (lambda a: a["parent"].__setitem__(0, 0), "root"),
+    (lambda a: a["depth"].__setitem__(3, 1), "depth"),
+    (lambda a: (a["parent"].__setitem__(5, 1), a["depth"].__setitem__(5, 2)), "preorder"),
+])
+def test_validate_rejects(mutate, msg):
+    t = W.tiny().tree
+    a = {k: getattr(t, k).copy() for k in ("seg_start", "seg_len", "parent", "depth")}
+    mutate(a)
+    with pytest.raises(OT.InvalidTree):
+        OT.validate(a["seg_start"], a["seg_len"], a["parent"], a["depth"], t.total_tokens)
+
+
+def test_visibility_pairs_and_naive_tokens_match_hand_count():
+    gold = _read_golden()
+    t = W.tiny().tree
+    m = OT.visible_mask_bruteforce(*_tree_args(t))
+    assert int(m.sum()) == gold["pairs"]
+    naive = sum(len(OT.path_tokens(t.seg_start, t.seg_len, t.parent, l)) for l in OT.leaves(t.parent))
+    assert naive == gold["naive_tokens"]
+
+
+# ---------------------------------------------------------------- plan checks
+
+def _read_golden():
+    tiles, bwd, out = [], [], {}
+    with open(os.path.join(GOLDEN, "tiny_plan.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            if line.startswith("tile "):
+                head, rng = line[5:].split("|")
+                s, q0, q1 = map(int, head.split())
+                r = list(map(int, rng.split()))
+                tiles.append((s, q0, q1, list(zip(r[0::2], r[1::2]))))
+            elif line.startswith("bwd "):
+                bwd.append(tuple(map(int, line[4:].split())))
+            else:
+                k, v = line.split()
+                out[k] = int(v)
+    out["tiles"], out["bwd"] = tiles, bwd
+    return out
+
+
+def test_plan_matches_hand_derived_golden():
+    gold = _read_golden()
+    t = W.tiny().tree
+    tiles, ranges, bwd = OP.build(*_tree_args(t), tile_tokens=32, kv_block=32, order=0)
+    got = [(int(s), int(q0), int(q1), [tuple(map(int, ranges[r])) for r in range(rb, rb + rc)])
+           for s, q0, q1, rb, rc in tiles]
+    assert got == gold["tiles"]
+    assert [tuple(map(int, b)) for b in bwd] == gold["bwd"]
+    # r_begin is the running count of ranges in schedule order
+    assert list(tiles[:, 3]) == list(np.cumsum([0] + [len(x[3]) for x in gold["tiles"]])[:-1])
+
+
+@pytest.mark.parametrize("seed", range(200))
+def test_plan_masks_equal_bruteforce(seed):
+    rng = np.random.default_rng(1000 + seed)
+    t = W.random_small_tree(rng, max_segments=7, max_len=12)
+    T = t.total_tokens
+    brute = OT.visible_mask_bruteforce(*_tree_args(t))
+    tt = int(rng.integers(1, 9))
+    kb = int(rng.integers(1, 9))
+    for order in (0, 1):
+        tiles, ranges, bwd = OP.build(*_tree_args(t), tile_tokens=tt, kv_block=kb, order=order)
+        assert np.array_equal(OP.expand_forward_mask(T, tiles, ranges), brute)
+        assert np.array_equal(OP.expand_backward_mask(T, bwd), brute)
+        # every query token in exactly one tile, every key in exactly one block
+        cover = np.zeros(T, int)
+        for s, q0, q1, rb, rc in tiles:
+            cover[q0:q1] += 1
+        assert (cover == 1).all()
+        cover[:] = 0
+        for s, k0, k1, q0, q1 in bwd:
+            cover[k0:k1] += 1
+        assert (cover == 1).all()
+    # closed form: j visible to i  <=>  j <= i < end of seg(j)'s subtree
+    seg = OT.segment_of_token(t.seg_start, t.seg_len)
+    send = np.array([OP.subtree_end(*_tree_args(t), s) for s in range(t.num_segments)])
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    assert np.array_equal((j <= i) & (i < send[seg][None, :]), brute)
+
+
+def test_plan_order_keeps_siblings_adjacent():
+    t = W.grpo_star().tree
+    tiles, _, _ = OP.build(*_tree_args(t), tile_tokens=32, kv_block=128, order=0)
+    # after the prompt's tiles, tile k of all 8 completions run back to back
+    first = [int(s) for s in tiles[64:72, 0]]
+    assert first == list(range(1, 9))
+
+
+# ---------------------------------------------------------- attention: pins
+
+def test_single_segment_equals_library_causal_attention():
+    rng = np.random.default_rng(7)
+    q, k, v, do = _rand(rng, 97, 4, 2, 16)
+    seg_start, seg_len, parent = [0], [97], [-1]
+    O, LSE = A.tree_forward(q, k, v, seg_start, seg_len, parent, 0.25)
+    np.testing.assert_allclose(O, _sdpa_causal(q, k, v, 0.25), rtol=0, atol=1e-12)
+    # gradients against torch autograd through the same library routine
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    G = 2
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq.permute(1, 0, 2)[None], tk.repeat_interleave(G, 1).permute(1, 0, 2)[None],
+        tv.repeat_interleave(G, 1).permute(1, 0, 2)[None], is_causal=True, scale=0.25)
+    (o[0].permute(1, 0, 2) * torch.tensor(do)).sum().backward()
+    dQ, dK, dV = A.tree_backward(q, k, v, do, seg_start, seg_len, parent, 0.25)
+    for ours, ref in ((dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+        np.testing.assert_allclose(ours, ref.numpy(), rtol=0, atol=1e-11)
+
+
+def test_star_with_one_child_equals_causal_on_concatenation():
+    rng = np.random.default_rng(8)
+    q, k, v, _ = _rand(rng, 50, 2, 2, 8)
+    O, _ = A.tree_forward(q, k, v, [0, 30], [30, 20], [-1, 0], 0.5)
+    np.testing.assert_allclose(O, _sdpa_causal(q, k, v, 0.5), rtol=0, atol=1e-12)
+
+
+def test_lse_is_log_sum_exp_over_visible_keys():
+    t = W.tiny().tree
+    rng = np.random.default_rng(9)
+    q, k, v, _ = _rand(rng, t.total_tokens, 2, 1, 8)
+    _, LSE = A.tree_forward(q, k, v, *_tree_args(t), 0.3)
+    m = OT.visible_mask_bruteforce(*_tree_args(t))
+    for h in range(2):
+        for i in range(0, t.total_tokens, 7):
+            js = np.nonzero(m[i])[0]
+            s = [0.3 * float(np.dot(q[i, h], k[j, 0])) for j in js]
+            assert abs(LSE[h, i] - np.log(np.sum(np.exp(s)))) < 1e-12
+
+
+@pytest.mark.parametrize("seed", range(50))
+def test_unrolled_equals_dense_tree_mask(seed):
+    rng = np.random.default_rng(seed)
+    t = W.random_small_tree(rng, max_segments=7, max_len=20)
+    hkv = int(rng.integers(1, 3))
+    hq = hkv * int(rng.choice([1, 2]))
+    q, k, v, do = _rand(rng, t.total_tokens, hq, hkv, 8)
+    mask = OT.visible_mask_bruteforce(*_tree_args(t))
+    O1, L1 = A.tree_forward(q, k, v, *_tree_args(t), 0.4)
+    O2, L2, _ = A.dense_forward(q, k, v, mask, 0.4)
+    np.testing.assert_allclose(O1, O2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L1, L2, rtol=0, atol=1e-12)
+    g1 = A.tree_backward(q, k, v, do, *_tree_args(t), 0.4)
+    g2 = A.dense_backward(q, k, v, do, mask, 0.4)
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-11)
+
+
+def test_dense_route_matches_library_masked_attention_and_autograd():
+    t = W.tiny().tree
+    rng = np.random.default_rng(11)
+    q, k, v, do = _rand(rng, t.total_tokens, 2, 2, 8)
+    mask = OT.visible_mask_bruteforce(*_tree_args(t))
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        tq.permute(1, 0, 2)[None], tk.permute(1, 0, 2)[None], tv.permute(1, 0, 2)[None],
+        attn_mask=torch.tensor(mask), scale=0.35)
+    (o[0].permute(1, 0, 2) * torch.tensor(do)).sum().backward()
+    O, _, _ = A.dense_forward(q, k, v, mask, 0.35)
+    np.testing.assert_allclose(O, o[0].permute(1, 0, 2).detach().numpy(), rtol=0, atol=1e-12)
+    dQ, dK, dV = A.dense_backward(q, k, v, do, mask, 0.35)
+    for ours, ref in ((dQ, tq.grad), (dK, tk.grad), (dV, tv.grad)):
+        np.testing.assert_allclose(ours, ref.numpy(), rtol=0, atol=1e-11)
+
+
+def test_gradients_match_finite_differences():
+    t = W.tiny().tree
+    rng = np.random.default_rng(12)
+    q, k, v, do = _rand(rng, t.total_tokens, 2, 1, 8, 0.7)
+    args = _tree_args(t)
+    scale = 0.35
+
+    def loss(q_, k_, v_):
+        O, _ = A.tree_forward(q_, k_, v_, *args, scale)
+        return float((O * do).sum())
+
+    dQ, dK, dV = A.tree_backward(q, k, v, do, *args, scale)
+    h = 1e-6
+    for trial in range(8):
+        u = [rng.standard_normal(x.shape) for x in (q, k, v)]
+        fp = loss(q + h * u[0], k + h * u[1], v + h * u[2])
+        fm = loss(q - h * u[0], k - h * u[1], v - h * u[2])
+        fd = (fp - fm) / (2 * h)
+        an = float((dQ * u[0]).sum() + (dK * u[1]).sum() + (dV * u[2]).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an))
+    # single coordinates: each (tensor, entry) in isolation
+    for trial in range(40):
+        which = trial % 3
+        x = [q, k, v][which]
+        pos = tuple(int(rng.integers(0, n)) for n in x.shape)
+        e = np.zeros_like(x)
+        e[pos] = 1.0
+        xs = [q, k, v]
+        p = [a + h * e if i == which else a for i, a in enumerate(xs)]
+        m = [a - h * e if i == which else a for i, a in enumerate(xs)]
+        fd = (loss(*p) - loss(*m)) / (2 * h)
+        an = [dQ, dK, dV][which][pos]
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an))
+
+
+def test_loss_owner_choice_does_not_change_gradients():
+    t = W.tiny().tree
+    rng = np.random.default_rng(13)
+    q, k, v, do = _rand(rng, t.total_tokens, 2, 2, 8)
+    g1 = A.tree_backward(q, k, v, do, *_tree_args(t), 0.4, owner="first")
+    g2 = A.tree_backward(q, k, v, do, *_tree_args(t), 0.4, owner="last")
+    for a, b in zip(g1, g2):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_gradient_sums():
+    """sum_j dV_j = sum_i dO_i (rows of P sum to 1); sum_j dK_j = 0 (rows of dS sum to 0)."""
+    t = W.tiny().tree
+    rng = np.random.default_rng(14)
+    q, k, v, do = _rand(rng, t.total_tokens, 4, 2, 8)
+    dQ, dK, dV = A.tree_backward(q, k, v, do, *_tree_args(t), 0.4)
+    for g in range(2):
+        np.testing.assert_allclose(dV[:, g].sum(0), do[:, 2 * g:2 * g + 2].sum((0, 1)), atol=1e-11)
+        np.testing.assert_allclose(dK[:, g].sum(0), 0.0, atol=1e-11)
+
+
+def _permute_siblings(t, rng):
+    """Re-lay the tree with every node's children in a random order.
+
+    Returns the new tree and new_index_of_old_token."""
+    ch = OT.children(t.parent)
+    roots = [s for s in range(t.num_segments) if t.parent[s] == -1]
+    order, pars = [], []
+    newid = {}
+
+    def visit(s, p):
+        newid[s] = len(order)
+        order.append(s)
+        pars.append(p)
+        kids = list(ch[s])
+        rng.shuffle(kids)
+        for c in kids:
+            visit(c, newid[s])
+
+    for r in roots:
+        visit(r, -1)
+    nt = W.tree_from_preorder([int(t.seg_len[s]) for s in order], pars)
+    perm = np.empty(t.total_tokens, dtype=np.int64)
+    for s in order:
+        a = int(t.seg_start[s])
+        b = int(nt.seg_start[newid[s]])
+        perm[a:a + int(t.seg_len[s])] = np.arange(b, b + int(t.seg_len[s]))
+    return nt, perm
+
+
+def test_sibling_permutation_leaves_results_unchanged():
+    t = W.tiny().tree
+    rng = np.random.default_rng(15)
+    q, k, v, do = _rand(rng, t.total_tokens, 2, 1, 8)
+    O, L = A.tree_forward(q, k, v, *_tree_args(t), 0.4)
+    g = A.tree_backward(q, k, v, do, *_tree_args(t), 0.4)
+    for trial in range(4):
+        nt, perm = _permute_siblings(t, rng)
+        inv = np.argsort(perm)
+        q2, k2, v2, do2 = (x[inv] for x in (q, k, v, do))
+        O2, L2 = A.tree_forward(q2, k2, v2, *_tree_args(nt), 0.4)
+        np.testing.assert_allclose(O2[perm], O, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(L2[:, perm], L, rtol=0, atol=1e-12)
+        g2 = A.tree_backward(q2, k2, v2, do2, *_tree_args(nt), 0.4)
+        for a, b in zip(g2, g):
+            np.testing.assert_allclose(a[perm], b, rtol=0, atol=1e-12)
+
+
+def test_sibling_isolation():
+    """Changing one branch's K/V changes nothing outside that branch's subtree."""
+    t = W.tiny().tree
+    rng = np.random.default_rng(16)
+    q, k, v, _ = _rand(rng, t.total_tokens, 2, 1, 8)
+    O, L = A.tree_forward(q, k, v, *_tree_args(t), 0.4)
+    k2, v2 = k.copy(), v.copy()
+    k2[96:169] += 1.0  # seg2 and its subtree (seg3, seg4)
+    v2[96:169] -= 2.0
+    O2, L2 = A.tree_forward(q, k2, v2, *_tree_args(t), 0.4)
+    outside = np.r_[0:96, 169:186]
+    assert np.array_equal(O2[outside], O[outside])
+    assert np.array_equal(L2[:, outside], L[:, outside])
+    assert not np.allclose(O2[96:169], O[96:169])
+
+
+def test_bf16_inputs_are_upcast_exactly():
+    w = W.tiny()
+    x = W.draw_tensors(w, "bf16")
+    q = x["q"].float().numpy()
+    assert np.array_equal(q.astype(np.float64), x["q"].double().numpy())
+
+
+def test_edge_gather_oracle():
+    h = np.arange(12.0).reshape(6, 2)
+    out = OG.edge_gather(h, [5, 0, 5])
+    assert out.tolist() == [[10.0, 11.0], [0.0, 1.0], [10.0, 11.0]]
+    assert OG.edge_gather(h, []).shape == (0, 2)
+    with pytest.raises(IndexError):
+        OG.edge_gather(h, [6])
+    with pytest.raises(IndexError):
+        OG.edge_gather(h, [-1])
