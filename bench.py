@@ -1,0 +1,470 @@
+"""Benchmark: shared-prefix tree attention forward + backward on one GB300.
+
+One step = the whole hot path over one batch: tree attention forward,
+backward (which includes its preprocess and dQ conversion kernels) and the
+sampled-edge gather, on the seeded synthetic agent-call tree (65,536 tokens,
+32 query heads, 8 KV heads, head_dim 128, bf16) unless ``--config`` names
+another workload.  The plan is built once per tree; the end-to-end figure
+rebuilds and uploads it every step.
+
+Prints one JSON line.  ``value`` is useful (ancestor-masked) attention
+TFLOP/s with inputs resident in HBM: 4*D*Hq*pairs forward plus 10*D*Hq*pairs
+backward per step, where pairs counts only visible (query, key) pairs.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "tree-attn fwd+bwd useful TFLOP/s and tokens/s at 1 GB300; % of BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# kernels the library launches per call (fwd; bwd = preprocess, main, dQ; gather)
+LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 3, "gather": 1}
+
+
+# ------------------------------------------------------------------ helpers
+
+def useful_pairs(tree) -> int:
+    """Visible (query, key) pairs: sum over segments of len*len(ancestors) + len*(len+1)/2."""
+    anc = np.zeros(tree.num_segments, dtype=np.int64)
+    total = 0
+    for s in range(tree.num_segments):
+        p = int(tree.parent[s])
+        if p >= 0:
+            anc[s] = anc[p] + int(tree.seg_len[p])
+        n = int(tree.seg_len[s])
+        total += n * int(anc[s]) + n * (n + 1) // 2
+    return total
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _peak_value(peaks, *keys):
+    for k in keys:
+        if k in peaks and isinstance(peaks[k], (int, float)):
+            return float(peaks[k])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            import tempfile
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------- oracle (CPU) leg
+
+def _subtree_of_leaves(tree, leaves):
+    """Re-pack the union of some root-to-leaf paths as its own preorder tree.
+
+    Returns (tree, token_index) where token_index maps new tokens to old."""
+    from oracle import tree as OT
+    keep = set()
+    for l in leaves:
+        keep.update(OT.ancestors(tree.parent, l))
+        keep.add(l)
+    order = sorted(keep)  # preorder is preserved by index order
+    newid = {s: i for i, s in enumerate(order)}
+    lens = [int(tree.seg_len[s]) for s in order]
+    pars = [newid[int(tree.parent[s])] if int(tree.parent[s]) >= 0 else -1 for s in order]
+    tok = np.concatenate([np.arange(int(tree.seg_start[s]), int(tree.seg_start[s]) + int(tree.seg_len[s]))
+                          for s in order])
+    return W.tree_from_preorder(lens, pars), tok
+
+
+def oracle_sample_plan(w, flop_budget: float):
+    """Root-to-leaf paths of the workload, shortest first, while their
+    unrolled fp64 cost (KV group 0) stays within ``flop_budget``; at least one."""
+    from oracle import tree as OT
+    t = w.tree
+    G = w.hq // w.hkv
+    leaves = OT.leaves(t.parent)
+    plen = {l: len(OT.path_tokens(t.seg_start, t.seg_len, t.parent, l)) for l in leaves}
+    chosen, cost = [], 0.0
+    for l in sorted(leaves, key=lambda l: (plen[l], l)):
+        c = 14.0 * w.head_dim * G * plen[l] * plen[l] / 2
+        if chosen and cost + c > flop_budget:
+            break
+        chosen.append(l)
+        cost += c
+    return sorted(chosen)
+
+
+def oracle_child(spec: dict):
+    """Runs in a fresh interpreter: times the oracle on one sample."""
+    from oracle import attention as A
+    w = W.get(spec["config"])
+    sub, tok = _subtree_of_leaves(w.tree, spec["leaves"])
+    x = W.draw_tensors(w, "bf16")
+    G = w.hq // w.hkv
+    q = x["q"][tok][:, :G].float().numpy()
+    k = x["k"][tok][:, :1].float().numpy()
+    v = x["v"][tok][:, :1].float().numpy()
+    do = x["do"][tok][:, :G].float().numpy()
+    args = (sub.seg_start, sub.seg_len, sub.parent, w.softmax_scale)
+    times = []
+    for _ in range(spec.get("reps", 1)):
+        t0 = time.perf_counter()
+        A.tree_forward(q, k, v, *args)
+        A.tree_backward(q, k, v, do, *args)
+        times.append(time.perf_counter() - t0)
+    pairs = useful_pairs(sub)
+    flops = 14.0 * w.head_dim * G * pairs
+    print(json.dumps({"times": times, "useful_flops": flops, "tokens": int(sub.total_tokens),
+                      "paths": len(spec["leaves"])}))
+
+
+def run_oracle_sample(w, flop_budget: float, reps: int = 1):
+    leaves = oracle_sample_plan(w, flop_budget)
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    spec = {"config": w.name, "leaves": [int(l) for l in leaves], "reps": reps}
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--_oracle-child", json.dumps(spec)],
+                       capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    out["cores"] = cores
+    out["sample"] = (f"KV head 0 ({w.hq // w.hkv} query heads) over the {len(leaves)} shortest root-to-leaf "
+                     f"paths ({out['tokens']} physical tokens of {w.T}), fwd+bwd, fp64 leaf-unrolled "
+                     f"NumPy, {cores} BLAS threads")
+    return out
+
+
+# --------------------------------------------------------------- GPU leg
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_gpu(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    import shared_prefix_causal_gb300 as spc
+
+    w = W.get(args.config)
+    G = w.hq // w.hkv
+    T, D = w.T, w.head_dim
+    x = W.draw_tensors(w, "bf16", with_hidden=w.hidden_dim is not None)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    hidden = x["hidden"].to(dev) if "hidden" in x else None
+    idx = torch.from_numpy(w.edge_idx).to(dev) if w.edge_idx is not None else None
+    scale = w.softmax_scale
+
+    t0 = time.perf_counter()
+    plan = spc.tree_plan(w.tree, 128 // G, 128, 0, upload=False)
+    plan_ms = (time.perf_counter() - t0) * 1e3
+    spc.sp_plan_upload(plan)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_buf = spc.bwd_workspace(q)
+    gathered = torch.empty((idx.shape[0], hidden.shape[1]), dtype=hidden.dtype, device=dev) \
+        if hidden is not None else None
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        spc.sp_tree_attn_fwd(plan, q, k, v, o, lse, scale, status)
+        if evs:
+            evs[1].record(stream)
+        spc.sp_tree_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status)
+        if evs:
+            evs[2].record(stream)
+        if hidden is not None:
+            spc.sp_edge_gather(hidden, idx, gathered, status)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(dev.index)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    gat_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} in the timed region")
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+
+    pairs = useful_pairs(w.tree)
+    f_fwd = 4.0 * D * w.hq * pairs
+    f_bwd = 10.0 * D * w.hq * pairs
+    ms_step = total_ms / args.steps
+    value = ws * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    p_burst = _peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
+    p_sust = _peak_value(peaks, "bf16_tflops_sustained") or p_burst
+    med_fwd, med_bwd = statistics.median(fwd_ms), statistics.median(bwd_ms)
+    fwd_tflops = f_fwd / (med_fwd * 1e-3) / 1e12
+    bwd_tflops = f_bwd / (med_bwd * 1e-3) / 1e12
+    mean_bwd = statistics.mean(bwd_ms)
+    mean_fwd = statistics.mean(fwd_ms)
+    e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 else None
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; inputs drawn by workloads.py, no dataset)",
+        "config": {"workload": w.description, "tokens": T, "segments": w.tree.num_segments,
+                   "q_heads": w.hq, "kv_heads": w.hkv, "head_dim": D, "useful_pairs_per_head": pairs,
+                   "tile_tokens": 128 // G, "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
+                   "l2": "inputs larger than L2 (Q and dO %d MiB each); no flush" % (q.numel() * 2 >> 20)},
+        "tokens_per_s": round(ws * T / (ms_step * 1e-3), 1),
+        "fwd": {"ms": round(med_fwd, 4), "useful_tflops": round(fwd_tflops, 2),
+                "frac_of_peak": round(fwd_tflops / p_burst, 4) if p_burst else None},
+        "bwd": {"ms": round(med_bwd, 4), "useful_tflops": round(bwd_tflops, 2),
+                "frac_of_peak": round(bwd_tflops / p_burst, 4) if p_burst else None},
+        "edge_gather": {"ms": round(statistics.median(gat_ms), 4),
+                        "gbs": round(2 * gathered.numel() * 2 / (statistics.median(gat_ms) * 1e-3) / 1e9, 1)
+                        if gathered is not None and statistics.median(gat_ms) > 0 else None},
+        "frac_of_bf16_peak": round(value / ws / p_burst, 4) if p_burst else None,
+        "plan_ms": round(plan_ms, 3),
+        "roofline": {
+            "kernel": "tree_attn_bwd call (main kernel plus two small HBM-bound kernels)",
+            "bound": "tensor", "achieved": round(f_bwd / (mean_bwd * 1e-3) / 1e12, 2),
+            "peak": p_sust, "unit": "TFLOP/s",
+            "frac": round(f_bwd / (mean_bwd * 1e-3) / 1e12 / p_sust, 4) if p_sust else None,
+            "traffic": None, "peak_source": f"bf16 sustained, {peak_src}"},
+        "roofline_fwd": {
+            "kernel": "tree_attn_fwd", "bound": "tensor",
+            "achieved": round(f_fwd / (mean_fwd * 1e-3) / 1e12, 2), "peak": p_burst, "unit": "TFLOP/s",
+            "frac": round(f_fwd / (mean_fwd * 1e-3) / 1e12 / p_burst, 4) if p_burst else None,
+            "traffic": None, "peak_source": f"bf16 burst, {peak_src}"},
+        "gpu_launches": args.steps * sum(LAUNCHES_PER_STEP.values() if hidden is not None
+                                         else [LAUNCHES_PER_STEP["fwd"], LAUNCHES_PER_STEP["bwd"]]),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        cb = run_oracle_sample(w, args.cpu_flops)
+        line["cpu_baseline"] = {"value": round(cb["useful_flops"] / cb["times"][0] / 1e12, 6), "unit": UNIT,
+                                "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"],
+                                "seconds": round(cb["times"][0], 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(args, spc, w, x, dev, flops_per_step):
+    """Same metric through the public API from pinned host buffers: each step
+    plans and uploads the tree, copies the inputs in, runs forward, backward
+    and the gather, and copies dQ, dK, dV and the gathered rows out."""
+    import torch
+    G = w.hq // w.hkv
+    host = {n: t.pin_memory() for n, t in x.items()}
+    idx_h = torch.from_numpy(w.edge_idx).pin_memory() if w.edge_idx is not None else None
+    dvc = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    idx_d = torch.empty_like(idx_h, device=dev) if idx_h is not None else None
+    outs_h = {n: torch.empty_like(host[src]).pin_memory() for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
+    g_h = torch.empty((idx_h.shape[0], host["hidden"].shape[1]), dtype=torch.bfloat16).pin_memory() \
+        if idx_h is not None and "hidden" in host else None
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        (idx_h.numel() * 4 if idx_h is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values()) + \
+        (g_h.numel() * 2 if g_h is not None else 0)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_buf = spc.bwd_workspace(dvc["q"])
+
+    def step():
+        plan = spc.tree_plan(w.tree, 128 // G, 128, 0)
+        for n in host:
+            dvc[n].copy_(host[n], non_blocking=True)
+        if idx_h is not None:
+            idx_d.copy_(idx_h, non_blocking=True)
+        q, k, v, do = dvc["q"], dvc["k"], dvc["v"], dvc["do"]
+        o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale, status)
+        dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, workspace=ws_buf,
+                                       d_status=status)
+        outs_h["dq"].copy_(dq, non_blocking=True)
+        outs_h["dk"].copy_(dk, non_blocking=True)
+        outs_h["dv"].copy_(dv, non_blocking=True)
+        if g_h is not None:
+            g_h.copy_(spc.edge_gather(dvc["hidden"], idx_d, status), non_blocking=True)
+        torch.cuda.synchronize(dev)
+        plan.close()
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    n = max(1, min(args.steps, 5))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    el = (time.perf_counter() - t0) / n
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} in the end-to-end run")
+    return {"value": round(flops_per_step / el / 1e12, 3), "unit": UNIT, "ms_per_step": round(el * 1e3, 3),
+            "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "includes": "tree_plan + plan upload + H2D of q,k,v,dO,hidden,idx + fwd + bwd + edge_gather + "
+                        "D2H of dQ,dK,dV and gathered rows"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = W.get(args.config)
+    r = run_oracle_sample(w, args.ref_flops, reps=args.warmup + args.steps)
+    times = r["times"][args.warmup:]
+    total = sum(times)
+    value = r["useful_flops"] * len(times) / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; inputs drawn by workloads.py, no dataset)",
+        "config": {"workload": w.description, "sample_tokens_per_step": r["tokens"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="agent", choices=list(W.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-flops", type=float, default=6e11, help="fp64 flop budget of the CPU-baseline sample")
+    ap.add_argument("--ref-flops", type=float, default=1.2e11, help="fp64 flop budget per reference step")
+    ap.add_argument("--_oracle-child", dest="oracle_child", default=None, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(json.loads(args.oracle_child))
+        return
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

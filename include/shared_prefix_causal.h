@@ -1,0 +1,188 @@
+/*
+ * shared_prefix_causal.h -- C ABI of the shared-prefix tree attention library.
+ *
+ * Several model calls whose token prefixes match exactly are packed once as a
+ * tree of token segments, laid out in DFS preorder with each segment's start,
+ * length, parent and depth ("[ENHANCEMENT] Shared-prefix training with context
+ * parallelism for exact agent trajectories", issue #7386, "Describe the
+ * solution you'd like", first bullet; "TreePackedSeqParams" PR #7387,
+ * "Summary", first bullet).  A query token attends causally inside its own
+ * segment and fully to every ancestor segment, and to nothing else (issue
+ * #7386, third bullet; PR #7387, second bullet).  The result equals packing
+ * every root-to-leaf call on its own (issue #7386, "Describe alternatives
+ * you've considered", item 1) while each shared prefix's K/V is stored once.
+ *
+ * General conventions
+ *  - Every call returns an int status (sp_status); nothing throws across the
+ *    ABI.  A non-zero host return means nothing was launched, except
+ *    SP_ERR_CUDA, which reports a failed launch.
+ *  - Device pointers are CUDA global-memory pointers that the caller owns and
+ *    keeps alive until the work on `stream` has finished; every tensor is
+ *    dense (contiguous) in the layout given below and 16-byte aligned
+ *    (SP_ERR_ALIGNMENT otherwise).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  All device work is asynchronous on that stream.
+ *  - `d_status` (nullable) is a device int32 into which kernels OR the
+ *    SP_DEV_* bits of errors they detect while running; the caller zeroes it
+ *    before the call and reads it after synchronising.
+ *  - Head layout (grouped-query attention): Hq query heads, Hkv key/value
+ *    heads, G = Hq / Hkv; query head h reads key/value head h / G.
+ *  - The ABI takes no mask, window, bias or soft-cap: unsupported attention
+ *    modifiers cannot be requested (issue #7386, sixth bullet; PR #7387,
+ *    fifth bullet: reject unsupported modifiers instead of ignoring them).
+ */
+#ifndef SHARED_PREFIX_CAUSAL_H
+#define SHARED_PREFIX_CAUSAL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SP_API __attribute__((visibility("default")))
+#else
+#define SP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SP_OK = 0,
+  SP_ERR_INVALID_TREE = -1, /* tree metadata is malformed or not in DFS preorder */
+  SP_ERR_INVALID_ARG = -2,  /* null pointer, negative size, size mismatch */
+  SP_ERR_UNSUPPORTED = -3,  /* dtype / head_dim / GQA ratio / plan tiling not supported */
+  SP_ERR_ALIGNMENT = -4,    /* a tensor pointer is not 16-byte aligned */
+  SP_ERR_CUDA = -5,         /* a CUDA runtime or driver call failed */
+  SP_ERR_TIMEOUT = -6,      /* (device) a bounded wait gave up */
+  SP_ERR_INDEX_RANGE = -7,  /* (device) an edge index outside [0, T) */
+  SP_ERR_WORKSPACE = -8,    /* workspace missing or smaller than required */
+  SP_ERR_NOT_UPLOADED = -9  /* the plan has no device copy (call sp_plan_upload) */
+} sp_status;
+
+/* Bits a kernel ORs into *d_status. */
+#define SP_DEV_INDEX_RANGE 1 /* edge_gather met an index outside [0, T); that row is zero-filled */
+#define SP_DEV_TIMEOUT 2     /* a pipeline wait in an attention kernel exceeded its spin limit */
+#define SP_DEV_BAD_PLAN 4    /* a plan entry points outside [0, T); the work item was skipped */
+
+typedef enum { SP_BF16 = 0, SP_F32 = 1 } sp_dtype;
+
+/* Tree metadata (host pointers, caller-owned, read only during sp_tree_plan).
+ * Segment s owns tokens [seg_start[s], seg_start[s] + seg_len[s]); segments
+ * are in DFS preorder; parent[s] < s, or -1 for a root (several roots make a
+ * forest, e.g. packed GRPO stars, #7914 introduction); depth[s] = 0 at a
+ * root, else depth[parent[s]] + 1.  Segments must tile [0, total_tokens)
+ * densely and be non-empty.  num_segments == 0 with total_tokens == 0 is the
+ * empty tree (a plan with no work). */
+typedef struct {
+  int32_t num_segments;
+  int32_t total_tokens;
+  const int32_t *seg_start;
+  const int32_t *seg_len;
+  const int32_t *parent;
+  const int32_t *depth;
+} sp_tree_desc;
+
+/* Opaque plan; library-owned (host and device copies) until sp_plan_destroy. */
+typedef struct sp_plan sp_plan;
+
+/* Read-only view of a plan's host tables (valid until sp_plan_destroy).
+ *   tiles  [n_tiles][5]  = {seg, q_start, q_end, r_begin, r_count}
+ *   ranges [n_ranges][2] = {kv_start, kv_end}; tile t reads ranges
+ *                          [r_begin, r_begin + r_count); the last one is causal
+ *                          (key j visible to query i iff j <= i), the others
+ *                          fully visible
+ *   bwd    [n_bwd][5]    = {seg, kv_start, kv_end, q_begin, q_end}: the keys
+ *                          [kv_start, kv_end) are seen exactly by the queries
+ *                          [q_begin, q_end) with j <= i */
+typedef struct {
+  int32_t tile_tokens, kv_block, order;
+  int32_t total_tokens, num_segments;
+  int32_t n_tiles, n_ranges, n_bwd, max_ranges_per_tile;
+  const int32_t *tiles;
+  const int32_t *ranges;
+  const int32_t *bwd;
+} sp_plan_info;
+
+/* tree_plan -- validate the tree and build the per-query-tile ancestor
+ * KV-range lists (issue #7386, third bullet: attention "for each query run
+ * against only its ancestor path"; PR #7387, "Summary": "causal attention over
+ * each query segment's ancestors").
+ *   tile_tokens  query tokens per tile (> 0); a tile never crosses a segment
+ *                end.  The bf16 kernels need tile_tokens * G == 128; the fp32
+ *                kernels need tile_tokens * G <= 128.
+ *   kv_block     keys per backward block (> 0); bf16 needs 128, fp32 <= 128.
+ *   order        0: tiles sorted so that tile k of all siblings run back to back
+ *                (shared ancestor K/V stays in L2); 1: longest KV walk first.
+ *   *out         receives the new plan (NULL on error).
+ * Errors: SP_ERR_INVALID_ARG (null pointers, bad sizes), SP_ERR_INVALID_TREE
+ * (checks listed in sp_tree_desc; issue #7914: unsupported layouts "fail
+ * before execution"). */
+SP_API int sp_tree_plan(const sp_tree_desc *tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
+                 sp_plan **out);
+
+/* Fills *info with the plan's host tables.  Errors: SP_ERR_INVALID_ARG. */
+SP_API int sp_plan_view(const sp_plan *plan, sp_plan_info *info);
+
+/* Copies the plan tables to device memory owned by the plan (a cudaMalloc on
+ * the current device and an async copy on `stream`).  Must precede the first
+ * attention call with this plan; repeat calls are no-ops.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA. */
+SP_API int sp_plan_upload(sp_plan *plan, void *stream);
+
+/* Frees the plan (host and device copies).  NULL is ignored.  The caller
+ * must make sure no queued kernel still reads the plan. */
+SP_API void sp_plan_destroy(sp_plan *plan);
+
+/* tree_attn_fwd -- O and LSE of shared-prefix tree attention.
+ *   q   [T][Hq][D], k and v [T][Hkv][D], o [T][Hq][D]: dtype (bf16 or fp32)
+ *   lse [Hq][T] fp32: natural-log sum of exp(softmax_scale * q.k) over the
+ *       visible keys (the softmax normaliser, kept for the backward pass)
+ *   D in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8}; T == plan total_tokens.
+ * bf16 runs on the tensor cores (fp32 accumulation and softmax, P rounded to
+ * bf16 for the P*V product); fp32 runs a full-fp32 SIMT kernel.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_ALIGNMENT,
+ * SP_ERR_NOT_UPLOADED, SP_ERR_CUDA; device: SP_DEV_TIMEOUT, SP_DEV_BAD_PLAN. */
+SP_API int sp_tree_attn_fwd(const sp_plan *plan, int32_t dtype, const void *q, const void *k,
+                     const void *v, void *o, float *lse, int32_t T, int32_t Hq, int32_t Hkv,
+                     int32_t D, float softmax_scale, int32_t *d_status, void *stream);
+
+/* Bytes of device workspace sp_tree_attn_bwd needs for these sizes. */
+SP_API size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t Hq, int32_t D);
+
+/* tree_attn_bwd -- dQ, dK, dV of L = sum_i <O_i, dO_i> through the tree
+ * attention (FlashAttention-style: S and P are recomputed from q, k and lse).
+ * Every child branch's contribution to a shared prefix's dK/dV is summed into
+ * that prefix ("Backward accumulates branch contributions into the shared
+ * prefix", #7914 introduction).
+ *   q, k, v, o, lse, d_o: as in / out of tree_attn_fwd (d_o like o)
+ *   dq [T][Hq][D], dk and dv [T][Hkv][D]: outputs in dtype, fully overwritten
+ *   workspace: device scratch of at least
+ *       sp_tree_attn_bwd_workspace_bytes(dtype, T, Hq, D) bytes, caller-owned;
+ *       its contents on entry do not matter.
+ * Errors: as sp_tree_attn_fwd, plus SP_ERR_WORKSPACE. */
+SP_API int sp_tree_attn_bwd(const sp_plan *plan, int32_t dtype, const void *q, const void *k,
+                     const void *v, const void *o, const float *lse, const void *d_o, void *dq,
+                     void *dk, void *dv, void *workspace, size_t workspace_bytes, int32_t T,
+                     int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale, int32_t *d_status,
+                     void *stream);
+
+/* edge_gather -- out[e][:] = hidden[idx[e]][:] for e < E: the sampled-edge
+ * source rows that go on to the vocabulary projection (issue #7386, fifth
+ * bullet; PR #7387, "Summary", fourth bullet).  hidden [T][hidden_dim] and
+ * out [E][hidden_dim] in dtype; idx [E] int32 on the device.  Duplicate
+ * indices are legal (one row per sampled action).  hidden_dim * element size
+ * must be a multiple of 16 bytes.  An index outside [0, T) zero-fills its
+ * row and sets SP_DEV_INDEX_RANGE.  E == 0 is a no-op.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_ALIGNMENT, SP_ERR_CUDA. */
+SP_API int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_dim,
+                   const int32_t *idx, int32_t E, void *out, int32_t *d_status, void *stream);
+
+/* Static English text for a status code (never NULL). */
+SP_API const char *sp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SHARED_PREFIX_CAUSAL_H */

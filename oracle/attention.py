@@ -241,3 +241,33 @@ def dense_backward(q, k, v, do, mask, scale):
         dQ[:, h] = scale * (dS @ k[:, g])
         dK[:, g] += scale * (dS.T @ q[:, h])
     return dQ, dK, dV
+
+
+def subtree_key_grads(q, k, v, do, seg_start, seg_len, parent, scale, seg, group):
+    """dK, dV [len(seg), D] of segment ``seg``'s keys for KV head ``group``.
+
+    Only queries in seg's subtree can see seg's keys, so this is
+    ``tree_backward`` restricted to the root-to-leaf paths through ``seg``:
+    each physical token of the subtree is owned by the first such path (DFS
+    order) that contains it.  Cost grows with the subtree, not the tree.
+    """
+    sub = set(_tree.descendants(parent, seg))
+    a0, a1 = int(seg_start[seg]), int(seg_start[seg]) + int(seg_len[seg])
+    D = k.shape[2]
+    dK = np.zeros((a1 - a0, D))
+    dV = np.zeros((a1 - a0, D))
+    seen = set()
+    for leaf in _tree.leaves(parent):
+        if leaf not in sub:
+            continue
+        idx = _tree.path_tokens(seg_start, seg_len, parent, leaf)
+        inside = (idx >= a0)  # tokens of seg and below on this path
+        own = np.array([p for p in np.nonzero(inside)[0] if int(idx[p]) not in seen], dtype=np.int64)
+        seen.update(int(t) for t in idx[inside])
+        if len(own) == 0:
+            continue
+        r = path_attention(q, k, v, scale, idx, group, rows=own, do=do)
+        pos = np.nonzero((idx >= a0) & (idx < a1))[0]
+        dK += r["dK"][pos]
+        dV += r["dV"][pos]
+    return dK, dV

@@ -1,0 +1,256 @@
+"""Python binding of the shared-prefix tree attention C ABI (``libspc.so``).
+
+Argument marshalling only: every function here checks Python-side types,
+pulls raw pointers, sizes and the current CUDA stream out of torch tensors and
+calls the C entry point of the same name (declared in
+``include/shared_prefix_causal.h``).  All arithmetic runs in the library's
+CUDA kernels.  There is no fallback: if ``libspc.so`` is missing, importing
+this package raises.  Build it with ``python shared_prefix_causal_gb300/build.py``.
+
+Layouts: q, o, dO, dq ``[T, Hq, D]``; k, v, dk, dv ``[T, Hkv, D]``; lse
+``[Hq, T]`` fp32; hidden ``[T, hidden_dim]``; edge indices int32 ``[E]``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libspc.so")
+
+SP_OK = 0
+SP_BF16 = 0
+SP_F32 = 1
+SP_DEV_INDEX_RANGE = 1
+SP_DEV_TIMEOUT = 2
+SP_DEV_BAD_PLAN = 4
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run `python shared_prefix_causal_gb300/build.py` "
+                      "(the CUDA library is required: there is no CPU path)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+class _TreeDesc(ctypes.Structure):
+    _fields_ = [("num_segments", _i32), ("total_tokens", _i32), ("seg_start", _i32p),
+                ("seg_len", _i32p), ("parent", _i32p), ("depth", _i32p)]
+
+
+class _PlanInfo(ctypes.Structure):
+    _fields_ = [("tile_tokens", _i32), ("kv_block", _i32), ("order", _i32), ("total_tokens", _i32),
+                ("num_segments", _i32), ("n_tiles", _i32), ("n_ranges", _i32), ("n_bwd", _i32),
+                ("max_ranges_per_tile", _i32), ("tiles", _i32p), ("ranges", _i32p), ("bwd", _i32p)]
+
+
+def _sig(name, res, args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = args
+    return f
+
+
+_c_tree_plan = _sig("sp_tree_plan", ctypes.c_int, [ctypes.POINTER(_TreeDesc), _i32, _i32, _i32, ctypes.POINTER(_vp)])
+_c_plan_view = _sig("sp_plan_view", ctypes.c_int, [_vp, ctypes.POINTER(_PlanInfo)])
+_c_plan_upload = _sig("sp_plan_upload", ctypes.c_int, [_vp, _vp])
+_c_plan_destroy = _sig("sp_plan_destroy", None, [_vp])
+_c_fwd = _sig("sp_tree_attn_fwd", ctypes.c_int,
+              [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_ws = _sig("sp_tree_attn_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32, _i32, _i32])
+_c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
+              [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+               _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_gather = _sig("sp_edge_gather", ctypes.c_int, [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp])
+_c_status = _sig("sp_status_string", ctypes.c_char_p, [ctypes.c_int])
+
+EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
+            "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_edge_gather", "sp_status_string")
+
+
+class SPError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {sp_status_string(code)} (status {code})")
+        self.code = code
+
+
+def sp_status_string(code: int) -> str:
+    return _c_status(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != SP_OK:
+        raise SPError(code, where)
+
+
+class Plan:
+    """Owner of an ``sp_plan`` handle (freed with ``sp_plan_destroy``)."""
+
+    def __init__(self, handle: int):
+        self._h = _vp(handle)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if self._h:
+            _c_plan_destroy(self._h)
+            self._h = _vp()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def info(self) -> dict:
+        return sp_plan_view(self)
+
+
+def sp_tree_plan(seg_start, seg_len, parent, depth, tile_tokens: int, kv_block: int, order: int = 0) -> Plan:
+    arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.int32)) for a in (seg_start, seg_len, parent, depth)]
+    n = int(arrs[0].shape[0])
+    total = int(arrs[1].astype(np.int64).sum()) if n else 0
+    ptr = [a.ctypes.data_as(_i32p) for a in arrs]
+    desc = _TreeDesc(n, total, *ptr)
+    out = _vp()
+    _check(_c_tree_plan(ctypes.byref(desc), tile_tokens, kv_block, order, ctypes.byref(out)), "sp_tree_plan")
+    return Plan(out.value)
+
+
+def sp_plan_view(plan: Plan) -> dict:
+    info = _PlanInfo()
+    _check(_c_plan_view(plan.handle, ctypes.byref(info)), "sp_plan_view")
+
+    def arr(p, n, w):
+        if n == 0:
+            return np.zeros((0, w), dtype=np.int32)
+        return np.ctypeslib.as_array(p, shape=(n * w,)).reshape(n, w).copy()
+
+    return {
+        "tile_tokens": info.tile_tokens, "kv_block": info.kv_block, "order": info.order,
+        "total_tokens": info.total_tokens, "num_segments": info.num_segments,
+        "max_ranges_per_tile": info.max_ranges_per_tile,
+        "tiles": arr(info.tiles, info.n_tiles, 5), "ranges": arr(info.ranges, info.n_ranges, 2),
+        "bwd": arr(info.bwd, info.n_bwd, 5),
+    }
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        return _vp(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return _vp(stream)
+    return _vp(stream.cuda_stream)
+
+
+def sp_plan_upload(plan: Plan, stream=None):
+    _check(_c_plan_upload(plan.handle, _stream(stream)), "sp_plan_upload")
+
+
+def _ptr(t):
+    return _vp(t.data_ptr()) if t is not None else _vp()
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return SP_BF16
+    if t.dtype == torch.float32:
+        return SP_F32
+    return -1
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def sp_tree_attn_fwd(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status=None, stream=None):
+    _need_cuda(q, k, v, o, lse, d_status)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) or tuple(o.shape) != (T, Hq, D) \
+            or tuple(lse.shape) != (Hq, T) or o.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("shape or dtype mismatch")
+    _check(_c_fwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, D,
+                  float(softmax_scale), _ptr(d_status), _stream(stream)), "sp_tree_attn_fwd")
+
+
+def sp_tree_attn_bwd_workspace_bytes(dtype: int, T: int, Hq: int, D: int) -> int:
+    return int(_c_ws(dtype, T, Hq, D))
+
+
+def sp_tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale: float,
+                     d_status=None, stream=None):
+    _need_cuda(q, k, v, o, lse, d_o, dq, dk, dv, workspace, d_status)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    for t, shp in ((k, (T, Hkv, D)), (v, (T, Hkv, D)), (o, (T, Hq, D)), (d_o, (T, Hq, D)), (dq, (T, Hq, D)),
+                   (dk, (T, Hkv, D)), (dv, (T, Hkv, D))):
+        if tuple(t.shape) != shp or t.dtype != q.dtype:
+            raise ValueError("shape or dtype mismatch")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_c_bwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D, float(softmax_scale),
+                  _ptr(d_status), _stream(stream)), "sp_tree_attn_bwd")
+
+
+def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
+    _need_cuda(hidden, idx, out, d_status)
+    import torch
+    if idx.dtype != torch.int32:
+        raise ValueError("edge indices must be int32")
+    T, Hd = hidden.shape
+    E = idx.shape[0]
+    if tuple(out.shape) != (E, Hd) or out.dtype != hidden.dtype:
+        raise ValueError("shape or dtype mismatch")
+    _check(_c_gather(_dtype_code(hidden), _ptr(hidden), T, Hd, _ptr(idx), E, _ptr(out), _ptr(d_status),
+                     _stream(stream)), "sp_edge_gather")
+
+
+# ------------------------------------------------------------ conveniences
+# Thin allocating wrappers over the entry points above (torch.empty only).
+
+def tree_plan(tree, tile_tokens: int, kv_block: int = 128, order: int = 0, upload: bool = True) -> Plan:
+    """Plan from any object with seg_start/seg_len/parent/depth arrays."""
+    p = sp_tree_plan(tree.seg_start, tree.seg_len, tree.parent, tree.depth, tile_tokens, kv_block, order)
+    if upload:
+        sp_plan_upload(p)
+    return p
+
+
+def tree_attn_fwd(plan: Plan, q, k, v, softmax_scale: float, d_status=None):
+    import torch
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    sp_tree_attn_fwd(plan, q, k, v, o, lse, softmax_scale, d_status)
+    return o, lse
+
+
+def bwd_workspace(q) -> "torch.Tensor":
+    import torch
+    n = sp_tree_attn_bwd_workspace_bytes(_dtype_code(q), q.shape[0], q.shape[1], q.shape[2])
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
+
+
+def tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, softmax_scale: float, workspace=None, d_status=None):
+    import torch
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = bwd_workspace(q) if workspace is None else workspace
+    sp_tree_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, ws, softmax_scale, d_status)
+    return dq, dk, dv
+
+
+def edge_gather(hidden, idx, d_status=None):
+    import torch
+    out = torch.empty((idx.shape[0], hidden.shape[1]), dtype=hidden.dtype, device=hidden.device)
+    sp_edge_gather(hidden, idx, out, d_status)
+    return out

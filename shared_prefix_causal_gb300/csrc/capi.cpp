@@ -1,0 +1,184 @@
+// The C ABI: argument checks, plan ownership and kernel dispatch.  Every
+// entry point returns an sp_status and never throws.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <new>
+
+#include "internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_heads(int32_t dtype, int32_t T, int32_t Hq, int32_t Hkv, int32_t D) {
+  if (T < 0 || Hq <= 0 || Hkv <= 0) return SP_ERR_INVALID_ARG;
+  if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return SP_ERR_UNSUPPORTED;
+  if (Hq % Hkv) return SP_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return SP_ERR_UNSUPPORTED;
+  return SP_OK;
+}
+
+// Tiling each kernel family accepts (see the header's sp_tree_plan notes).
+int check_tiling(const sp_plan &p, int32_t dtype, int32_t G) {
+  if (p.tile_tokens * G > 128 || p.kv_block > 128) return SP_ERR_UNSUPPORTED;
+  (void)dtype;
+  return SP_OK;
+}
+
+spc::PlanDev plan_dev(const sp_plan &p) {
+  return {p.d_tiles, p.d_ranges, p.d_bwd, p.n_tiles(), p.n_bwd(), p.tile_tokens, p.kv_block};
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+int sp_tree_plan(const sp_tree_desc *tree, int32_t tile_tokens, int32_t kv_block, int32_t order, sp_plan **out) {
+  if (!out) return SP_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!tree) return SP_ERR_INVALID_ARG;
+  sp_plan *p = new (std::nothrow) sp_plan();
+  if (!p) return SP_ERR_INVALID_ARG;
+  int rc;
+  try {
+    rc = spc::build_plan(*tree, tile_tokens, kv_block, order, *p);
+  } catch (...) {
+    rc = SP_ERR_INVALID_ARG;
+  }
+  if (rc != SP_OK) {
+    delete p;
+    return rc;
+  }
+  *out = p;
+  return SP_OK;
+}
+
+int sp_plan_view(const sp_plan *p, sp_plan_info *info) {
+  if (!p || !info) return SP_ERR_INVALID_ARG;
+  info->tile_tokens = p->tile_tokens;
+  info->kv_block = p->kv_block;
+  info->order = p->order;
+  info->total_tokens = p->total_tokens;
+  info->num_segments = p->num_segments;
+  info->n_tiles = p->n_tiles();
+  info->n_ranges = p->n_ranges();
+  info->n_bwd = p->n_bwd();
+  info->max_ranges_per_tile = p->max_ranges_per_tile;
+  info->tiles = p->tiles.data();
+  info->ranges = p->ranges.data();
+  info->bwd = p->bwd.data();
+  return SP_OK;
+}
+
+int sp_plan_upload(sp_plan *p, void *stream) {
+  if (!p) return SP_ERR_INVALID_ARG;
+  if (p->d_tiles) return SP_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bt = p->tiles.size() * 4, br = p->ranges.size() * 4, bb = p->bwd.size() * 4;
+  const size_t total = align_up(bt) + align_up(br) + align_up(bb) + 256;
+  char *base = nullptr;
+  if (cudaMalloc(&base, total) != cudaSuccess) return SP_ERR_CUDA;
+  int32_t *dt = reinterpret_cast<int32_t *>(base);
+  int32_t *dr = reinterpret_cast<int32_t *>(base + align_up(bt));
+  int32_t *db = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br));
+  if ((bt && cudaMemcpyAsync(dt, p->tiles.data(), bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (br && cudaMemcpyAsync(dr, p->ranges.data(), br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (bb && cudaMemcpyAsync(db, p->bwd.data(), bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaFree(base);
+    return SP_ERR_CUDA;
+  }
+  p->d_tiles = dt;
+  p->d_ranges = dr;
+  p->d_bwd = db;
+  cudaGetDevice(&p->device);
+  return SP_OK;
+}
+
+void sp_plan_destroy(sp_plan *p) {
+  if (!p) return;
+  if (p->d_tiles) cudaFree(p->d_tiles);
+  delete p;
+}
+
+int sp_tree_attn_fwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, void *o,
+                     float *lse, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
+                     int32_t *d_status, void *stream) {
+  if (!p) return SP_ERR_INVALID_ARG;
+  if (int rc = check_heads(dtype, T, Hq, Hkv, D)) return rc;
+  if (T != p->total_tokens) return SP_ERR_INVALID_ARG;
+  if (T == 0) return SP_OK;
+  if (!q || !k || !v || !o || !lse) return SP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return SP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f)) return SP_ERR_INVALID_ARG;
+  if (!p->d_tiles) return SP_ERR_NOT_UPLOADED;
+  const int G = Hq / Hkv;
+  if (int rc = check_tiling(*p, dtype, G)) return rc;
+  const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
+  return spc::simt_fwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_status, stream);
+}
+
+size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t Hq, int32_t D) {
+  (void)dtype;
+  (void)D;
+  if (T <= 0 || Hq <= 0) return 0;
+  return align_up(size_t(T) * size_t(Hq) * sizeof(float));  // Delta [Hq][T]
+}
+
+int sp_tree_attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace,
+                     size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
+                     int32_t *d_status, void *stream) {
+  if (!p) return SP_ERR_INVALID_ARG;
+  if (int rc = check_heads(dtype, T, Hq, Hkv, D)) return rc;
+  if (T != p->total_tokens) return SP_ERR_INVALID_ARG;
+  if (T == 0) return SP_OK;
+  if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv) return SP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(d_o) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return SP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f)) return SP_ERR_INVALID_ARG;
+  const size_t need = sp_tree_attn_bwd_workspace_bytes(dtype, T, Hq, D);
+  if (!workspace || workspace_bytes < need) return SP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SP_ERR_ALIGNMENT;
+  if (!p->d_tiles) return SP_ERR_NOT_UPLOADED;
+  const int G = Hq / Hkv;
+  if (int rc = check_tiling(*p, dtype, G)) return rc;
+  const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
+  return spc::simt_bwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_o, dq, dk, dv, static_cast<float *>(workspace),
+                       d_status, stream);
+}
+
+int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_dim, const int32_t *idx, int32_t E,
+                   void *out, int32_t *d_status, void *stream) {
+  if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_UNSUPPORTED;
+  if (T < 0 || E < 0 || hidden_dim <= 0) return SP_ERR_INVALID_ARG;
+  if (E == 0) return SP_OK;
+  if (!hidden || !idx || !out) return SP_ERR_INVALID_ARG;
+  if (!aligned16(hidden) || !aligned16(out)) return SP_ERR_ALIGNMENT;
+  return spc::edge_gather(dtype == SP_BF16 ? 2 : 4, hidden, T, hidden_dim, idx, E, out, d_status, stream);
+}
+
+const char *sp_status_string(int status) {
+  switch (status) {
+    case SP_OK: return "ok";
+    case SP_ERR_INVALID_TREE: return "invalid tree: metadata malformed or not in DFS preorder";
+    case SP_ERR_INVALID_ARG: return "invalid argument";
+    case SP_ERR_UNSUPPORTED: return "unsupported dtype, head_dim, GQA ratio or plan tiling";
+    case SP_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+    case SP_ERR_CUDA: return "CUDA call failed";
+    case SP_ERR_TIMEOUT: return "device wait timed out";
+    case SP_ERR_INDEX_RANGE: return "edge index out of range";
+    case SP_ERR_WORKSPACE: return "workspace missing or too small";
+    case SP_ERR_NOT_UPLOADED: return "plan not uploaded to the device";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "../../include/shared_prefix_causal.h"
+
+struct sp_plan {
+  int32_t tile_tokens = 0, kv_block = 0, order = 0;
+  int32_t total_tokens = 0, num_segments = 0;
+  int32_t max_ranges_per_tile = 0;
+  std::vector<int32_t> tiles;   // [n][5]
+  std::vector<int32_t> ranges;  // [m][2]
+  std::vector<int32_t> bwd;     // [k][5]
+  // device copies (owned), valid after sp_plan_upload
+  int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr;
+  int device = -1;
+  int32_t n_tiles() const { return int32_t(tiles.size() / 5); }
+  int32_t n_ranges() const { return int32_t(ranges.size() / 2); }
+  int32_t n_bwd() const { return int32_t(bwd.size() / 5); }
+};
+
+namespace spc {
+
+// Plan builder (plan.cpp).  Returns SP_OK or SP_ERR_INVALID_TREE/ARG.
+int build_plan(const sp_tree_desc &tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
+               sp_plan &plan);
+
+// Device-side view of a plan passed to kernels by value.
+struct PlanDev {
+  const int32_t *tiles;
+  const int32_t *ranges;
+  const int32_t *bwd;
+  int32_t n_tiles, n_bwd, tile_tokens, kv_block;
+};
+
+struct AttnShape {
+  int32_t T, Hq, Hkv, D, G;
+  float scale;
+};
+
+// SIMT kernels (attn_simt.cu): any tiling, fp32 arithmetic, input in fp32 or bf16.
+int simt_fwd(const PlanDev &p, const AttnShape &s, int32_t dtype, const void *q, const void *k,
+             const void *v, void *o, float *lse, int32_t *d_status, void *stream);
+int simt_bwd(const PlanDev &p, const AttnShape &s, int32_t dtype, const void *q, const void *k,
+             const void *v, const void *o, const float *lse, const void *d_o, void *dq, void *dk,
+             void *dv, float *delta, int32_t *d_status, void *stream);
+
+// edge_gather (edge_gather.cu).
+int edge_gather(int32_t elem_bytes, const void *hidden, int32_t T, int32_t hidden_dim,
+                const int32_t *idx, int32_t E, void *out, int32_t *d_status, void *stream);
+
+}  // namespace spc

@@ -1,0 +1,162 @@
+// Host planner: tree validation and the per-query-tile ancestor KV-range
+// lists ("[ENHANCEMENT] Shared-prefix training with context parallelism for
+// exact agent trajectories", issue #7386, "Describe the solution you'd like":
+// attention for each query run against only its ancestor path; PR #7387
+// "TreePackedSeqParams", "Summary": causal attention over each query
+// segment's ancestors).
+//
+// One preorder pass with an explicit root-path stack validates the tree and
+// builds, per segment, the merged token intervals of its root path; a reverse
+// pass gives each segment's subtree end.  Tiles and backward blocks are then
+// emitted and sorted.  The canonical output (tile order, range merging,
+// backward order) is documented in the public header.
+#include <algorithm>
+#include <numeric>
+#include <utility>
+#include <vector>
+
+#include "internal.h"
+
+namespace spc {
+namespace {
+
+using Interval = std::pair<int32_t, int32_t>;
+
+void push_merged(std::vector<Interval> &v, Interval x) {
+  if (!v.empty() && v.back().second == x.first)
+    v.back().second = x.second;
+  else
+    v.push_back(x);
+}
+
+int validate(const sp_tree_desc &t) {
+  const int n = t.num_segments;
+  int64_t pos = 0;
+  for (int s = 0; s < n; ++s) {
+    if (t.seg_len[s] < 1 || t.seg_start[s] != pos) return SP_ERR_INVALID_TREE;
+    pos += t.seg_len[s];
+  }
+  if (pos != t.total_tokens) return SP_ERR_INVALID_TREE;
+  std::vector<int32_t> stack;  // root path of the last placed segment
+  for (int s = 0; s < n; ++s) {
+    const int32_t p = t.parent[s];
+    if (p < -1 || p >= s) return SP_ERR_INVALID_TREE;
+    if (t.depth[s] != (p < 0 ? 0 : t.depth[p] + 1)) return SP_ERR_INVALID_TREE;
+    if (p < 0) {
+      stack.clear();
+    } else {
+      while (!stack.empty() && stack.back() != p) stack.pop_back();
+      if (stack.empty()) return SP_ERR_INVALID_TREE;  // parent's subtree already closed
+    }
+    stack.push_back(s);
+  }
+  return SP_OK;
+}
+
+}  // namespace
+
+int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int32_t order,
+               sp_plan &plan) {
+  if (tile_tokens <= 0 || kv_block <= 0 || (order != 0 && order != 1)) return SP_ERR_INVALID_ARG;
+  if (t.num_segments < 0 || t.total_tokens < 0) return SP_ERR_INVALID_ARG;
+  if (t.num_segments > 0 &&
+      (!t.seg_start || !t.seg_len || !t.parent || !t.depth))
+    return SP_ERR_INVALID_ARG;
+  if ((t.num_segments == 0) != (t.total_tokens == 0)) return SP_ERR_INVALID_TREE;
+  if (int rc = validate(t)) return rc;
+
+  const int n = t.num_segments;
+  plan.tile_tokens = tile_tokens;
+  plan.kv_block = kv_block;
+  plan.order = order;
+  plan.total_tokens = t.total_tokens;
+  plan.num_segments = n;
+
+  // Root-path intervals per segment (inclusive of the segment itself), built
+  // from the parent's list; root id per segment; subtree ends.
+  std::vector<std::vector<Interval>> path(n);
+  std::vector<int32_t> root(n), send(n);
+  for (int s = 0; s < n; ++s) {
+    const int32_t p = t.parent[s];
+    if (p >= 0) path[s] = path[p];
+    root[s] = p < 0 ? s : root[p];
+    push_merged(path[s], {t.seg_start[s], t.seg_start[s] + t.seg_len[s]});
+    send[s] = t.seg_start[s] + t.seg_len[s];
+  }
+  for (int s = n - 1; s >= 0; --s)
+    if (t.parent[s] >= 0) send[t.parent[s]] = std::max(send[t.parent[s]], send[s]);
+
+  struct Tile {
+    int32_t seg, k, q0, q1;
+    int64_t kv_total;
+    std::vector<Interval> r;
+  };
+  std::vector<Tile> tiles;
+  for (int s = 0; s < n; ++s) {
+    const int32_t a0 = t.seg_start[s], a1 = a0 + t.seg_len[s];
+    const int32_t p = t.parent[s];
+    int32_t k = 0;
+    for (int32_t q0 = a0; q0 < a1; q0 += tile_tokens, ++k) {
+      Tile x;
+      x.seg = s;
+      x.k = k;
+      x.q0 = q0;
+      x.q1 = std::min(a1, q0 + tile_tokens);
+      if (p >= 0) x.r = path[p];
+      push_merged(x.r, {a0, x.q1});
+      x.kv_total = 0;
+      for (auto &iv : x.r) x.kv_total += iv.second - iv.first;
+      tiles.push_back(std::move(x));
+    }
+  }
+  std::vector<int32_t> perm(tiles.size());
+  std::iota(perm.begin(), perm.end(), 0);
+  if (order == 0) {
+    std::sort(perm.begin(), perm.end(), [&](int32_t a, int32_t b) {
+      const Tile &x = tiles[a], &y = tiles[b];
+      const int32_t px = t.parent[x.seg], py = t.parent[y.seg];
+      if (root[x.seg] != root[y.seg]) return root[x.seg] < root[y.seg];
+      if (px != py) return px < py;
+      if (x.k != y.k) return x.k < y.k;
+      return x.seg < y.seg;
+    });
+  } else {
+    std::sort(perm.begin(), perm.end(), [&](int32_t a, int32_t b) {
+      const Tile &x = tiles[a], &y = tiles[b];
+      if (x.kv_total != y.kv_total) return x.kv_total > y.kv_total;
+      if (x.seg != y.seg) return x.seg < y.seg;
+      return x.k < y.k;
+    });
+  }
+  plan.tiles.clear();
+  plan.ranges.clear();
+  plan.max_ranges_per_tile = 0;
+  for (int32_t i : perm) {
+    const Tile &x = tiles[i];
+    const int32_t rb = int32_t(plan.ranges.size() / 2);
+    const int32_t rc = int32_t(x.r.size());
+    plan.tiles.insert(plan.tiles.end(), {x.seg, x.q0, x.q1, rb, rc});
+    for (auto &iv : x.r) plan.ranges.insert(plan.ranges.end(), {iv.first, iv.second});
+    plan.max_ranges_per_tile = std::max(plan.max_ranges_per_tile, rc);
+  }
+
+  struct Blk {
+    int32_t seg, k0, k1, q0, q1;
+  };
+  std::vector<Blk> blocks;
+  for (int s = 0; s < n; ++s) {
+    const int32_t a0 = t.seg_start[s], a1 = a0 + t.seg_len[s];
+    for (int32_t k0 = a0; k0 < a1; k0 += kv_block)
+      blocks.push_back({s, k0, std::min(a1, k0 + kv_block), k0, send[s]});
+  }
+  std::sort(blocks.begin(), blocks.end(), [](const Blk &x, const Blk &y) {
+    const int32_t cx = x.q1 - x.q0, cy = y.q1 - y.q0;
+    if (cx != cy) return cx > cy;
+    return x.k0 < y.k0;
+  });
+  plan.bwd.clear();
+  for (auto &b : blocks) plan.bwd.insert(plan.bwd.end(), {b.seg, b.k0, b.k1, b.q0, b.q1});
+  return SP_OK;
+}
+
+}  // namespace spc

@@ -1,0 +1,140 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, builds plans bit-identical to the oracle's independent planner, and
+rejects malformed input before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import plan as OP
+
+spc = pytest.importorskip("shared_prefix_causal_gb300")
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "shared_prefix_causal.h")
+
+
+def test_library_exports_every_declared_symbol():
+    decl = re.findall(r"SP_API\s+[\w\s\*]*?\b(sp_\w+)\s*\(", open(HEADER).read())
+    assert len(decl) >= 9
+    lib = ctypes.CDLL(spc.LIB_PATH)
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert set(decl) == set(spc.EXPORTED)
+
+
+def _plan_tables(tree, tt, kb, order):
+    p = spc.sp_tree_plan(tree.seg_start, tree.seg_len, tree.parent, tree.depth, tt, kb, order)
+    return spc.sp_plan_view(p)
+
+
+@pytest.mark.parametrize("name", ["tiny", "star", "forest", "agent", "long"])
+@pytest.mark.parametrize("order", [0, 1])
+def test_plan_bit_exact_on_configs(name, order):
+    w = W.get(name)
+    G = w.hq // w.hkv
+    t = w.tree
+    for tt in {128 // G, 16}:
+        got = _plan_tables(t, tt, 128, order)
+        want = OP.build(t.seg_start, t.seg_len, t.parent, tt, 128, order)
+        for a, b in zip((got["tiles"], got["ranges"], got["bwd"]), want):
+            assert a.dtype == np.int32
+            assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("seed", range(100))
+def test_plan_bit_exact_random(seed):
+    rng = np.random.default_rng(seed)
+    t = W.random_small_tree(rng, max_segments=12, max_len=40)
+    tt, kb, order = int(rng.integers(1, 40)), int(rng.integers(1, 40)), int(rng.integers(0, 2))
+    got = _plan_tables(t, tt, kb, order)
+    want = OP.build(t.seg_start, t.seg_len, t.parent, tt, kb, order)
+    for a, b in zip((got["tiles"], got["ranges"], got["bwd"]), want):
+        assert np.array_equal(a, b)
+    assert got["max_ranges_per_tile"] == int(want[0][:, 4].max())
+
+
+def test_plan_matches_tiny_golden_file():
+    from tests.test_oracle import _read_golden
+    gold = _read_golden()
+    t = W.tiny().tree
+    got = _plan_tables(t, 32, 32, 0)
+    tiles = [(int(s), int(a), int(b), [tuple(map(int, got["ranges"][r])) for r in range(rb, rb + rc)])
+             for s, a, b, rb, rc in got["tiles"]]
+    assert tiles == gold["tiles"]
+    assert [tuple(map(int, b)) for b in got["bwd"]] == gold["bwd"]
+
+
+def _desc(t):
+    return [np.asarray(getattr(t, k)).copy() for k in ("seg_start", "seg_len", "parent", "depth")]
+
+
+@pytest.mark.parametrize("mutate", [
+    lambda a: a[1].__setitem__(2, 0),                       # empty segment
+    lambda a: a[0].__setitem__(3, 100),                     # gap in packing
+    lambda a: a[2].__setitem__(1, 3),                       # parent after child
+    lambda a: a[2].__setitem__(0, 0),                       # first segment not a root
+    lambda a: a[3].__setitem__(3, 1),                       # wrong depth
+    lambda a: (a[2].__setitem__(5, 1), a[3].__setitem__(5, 2)),  # not preorder
+    lambda a: a[2].__setitem__(4, -2),                      # parent below -1
+])
+def test_plan_rejects_invalid_tree(mutate):
+    a = _desc(W.tiny().tree)
+    mutate(a)
+    with pytest.raises(spc.SPError) as e:
+        spc.sp_tree_plan(*a, 32, 128, 0)
+    assert e.value.code == -1
+
+
+def test_plan_rejects_bad_arguments():
+    a = _desc(W.tiny().tree)
+    for tt, kb, order in ((0, 128, 0), (32, 0, 0), (32, 128, 2)):
+        with pytest.raises(spc.SPError) as e:
+            spc.sp_tree_plan(*a, tt, kb, order)
+        assert e.value.code == -2
+
+
+def test_empty_tree_gives_empty_plan():
+    e = np.zeros(0, dtype=np.int32)
+    info = spc.sp_plan_view(spc.sp_tree_plan(e, e, e, e, 32, 128, 0))
+    assert info["tiles"].shape == (0, 5) and info["bwd"].shape == (0, 5)
+
+
+def test_status_strings_and_workspace_size():
+    assert spc.sp_status_string(0) == "ok"
+    assert "preorder" in spc.sp_status_string(-1)
+    assert spc.sp_status_string(12345) == "unknown status"
+    assert spc.sp_tree_attn_bwd_workspace_bytes(spc.SP_F32, 0, 4, 64) == 0
+    n = spc.sp_tree_attn_bwd_workspace_bytes(spc.SP_BF16, 1000, 8, 128)
+    assert n >= 1000 * 8 * 4 and n % 256 == 0
+
+
+def test_attention_argument_checks_fail_before_device_work():
+    """Bad arguments come back as status codes; no pointer is dereferenced."""
+    t = W.tiny().tree
+    p = spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 64, 128, 0)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the checks fail first
+    f = spc._c_fwd
+    args = lambda dtype, T, Hq, Hkv, D, ptr=fake: (p.handle, dtype, ptr, ptr, ptr, ptr, ptr, T, Hq, Hkv, D,  # noqa
+                                                   0.125, None, None)
+    assert f(*args(0, 186, 2, 2, 96)) == -3          # head_dim
+    assert f(*args(0, 186, 6, 4, 64)) == -3          # Hq % Hkv
+    assert f(*args(0, 186, 32, 2, 64)) == -3         # G = 16
+    assert f(*args(7, 186, 2, 2, 64)) == -3          # dtype
+    assert f(*args(0, 185, 2, 2, 64)) == -2          # T mismatch
+    assert f(*args(0, 186, 2, 2, 64, ctypes.c_void_p((1 << 20) + 8))) == -4  # alignment
+    assert f(*args(0, 186, 2, 2, 64)) == -9          # plan not uploaded
+    assert f(None, 0, fake, fake, fake, fake, fake, 186, 2, 2, 64, 0.125, None, None) == -2
+    b = spc._c_bwd
+    assert b(p.handle, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, None, 0, 186, 2, 2, 64, 0.125,
+             None, None) == -8
+    assert b(p.handle, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 186, 2, 2, 64,
+             0.125, None, None) == -9
+    g = spc._c_gather
+    assert g(0, fake, 186, 256, fake, 0, fake, None, None) == 0       # E == 0: no-op
+    assert g(0, fake, 186, 3, fake, 4, fake, None, None) == -3        # row not a multiple of 16 bytes
+    assert g(0, fake, 186, 256, fake, -1, fake, None, None) == -2
+    assert g(0, ctypes.c_void_p((1 << 20) + 2), 186, 256, fake, 4, fake, None, None) == -4

@@ -1,0 +1,280 @@
+"""GPU parity: the CUDA library (called through the C ABI) against the fp64
+CPU oracle, on the seeded workloads.
+
+Tolerances (applied to the whole compared tensor, in fp64):
+  bf16 forward O: relative L2 <= 1e-2 and max-abs <= 2e-2;
+  fp32 forward O: relative L2 <= 1e-5;
+  dQ/dK/dV: relative L2 <= 2.5e-2 (bf16) and <= 1e-5 (fp32);
+  LSE: max-abs <= 5e-3 (bf16), <= 1e-5 (fp32).  LSE is the log of an fp32
+  sum over up to 131,072 keys; fp32 rounding of such a sum stays well below
+  1e-3 in practice, and the bf16 bound leaves room for the bf16 rounding of
+  P on the tensor-core path, which does not enter LSE.
+Plans and edge_gather: bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+from oracle import tree as OT
+
+pytestmark = pytest.mark.gpu
+
+spc = pytest.importorskip("shared_prefix_causal_gb300")
+
+TOL = {"bf16": dict(o_rel=1e-2, o_abs=2e-2, g_rel=2.5e-2, lse=5e-3),
+       "f32": dict(o_rel=1e-5, o_abs=None, g_rel=1e-5, lse=1e-5)}
+
+
+def rel_l2(x, ref):
+    """||x - ref|| / ||ref||; where the exact result is all zeros (e.g. dQ of a
+    forest of one-token roots: every softmax row has one entry, so dS = 0) the
+    root-mean-square of x is returned instead, against the same bound."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    nref = np.linalg.norm(ref)
+    if nref == 0.0:
+        return float(np.sqrt(np.mean(x * x))) if x.size else 0.0
+    return float(np.linalg.norm(x - ref) / nref)
+
+
+def run_gpu(w, dtype="bf16", tile_tokens=None, order=0, x=None, kv_block=128):
+    x = W.draw_tensors(w, dtype) if x is None else x
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    G = w.hq // w.hkv
+    plan = spc.tree_plan(w.tree, tile_tokens or 128 // G, kv_block, order)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale, st)
+    dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, d_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    out = {n: t.float().cpu().numpy() for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    return x, out
+
+
+def np32(x):
+    return {n: t.float().numpy() for n, t in x.items()}
+
+
+def check_full(w, x, out, dtype, groups=None):
+    tol = TOL[dtype]
+    t = w.tree
+    xs = np32(x)
+    args = (t.seg_start, t.seg_len, t.parent, w.softmax_scale)
+    O, L = A.tree_forward(xs["q"], xs["k"], xs["v"], t.seg_start, t.seg_len, t.parent, w.softmax_scale, groups)
+    dQ, dK, dV = A.tree_backward(xs["q"], xs["k"], xs["v"], xs["do"], *args, groups=groups)
+    G = w.hq // w.hkv
+    gs = list(range(w.hkv)) if groups is None else list(groups)
+    hs = [g * G + j for g in gs for j in range(G)]
+    res = {
+        "o": rel_l2(out["o"][:, hs], O[:, hs]),
+        "o_abs": float(np.abs(out["o"][:, hs] - O[:, hs]).max()),
+        "lse": float(np.abs(out["lse"][hs] - L[hs]).max()),
+        "dq": rel_l2(out["dq"][:, hs], dQ[:, hs]),
+        "dk": rel_l2(out["dk"][:, gs], dK[:, gs]),
+        "dv": rel_l2(out["dv"][:, gs], dV[:, gs]),
+    }
+    print(w.name, dtype, res)
+    assert res["o"] <= tol["o_rel"]
+    if tol["o_abs"] is not None:
+        assert res["o_abs"] <= tol["o_abs"]
+    assert res["lse"] <= tol["lse"]
+    for n in ("dq", "dk", "dv"):
+        assert res[n] <= tol["g_rel"], n
+    return res
+
+
+def check_sampled(w, x, out, groups, n_leaves=2, extra_rows=256, seed=0):
+    """Full-size check on sampled outputs the oracle computes path by path:
+    O, LSE and dQ on rows of a few root-to-leaf paths, dK/dV of the leaf
+    segments' keys and of the parent segment's keys (which sum several
+    branches)."""
+    tol = TOL["bf16"]
+    t = w.tree
+    rng = np.random.default_rng(seed)
+    G = w.hq // w.hkv
+    leaves = OT.leaves(t.parent)
+    plen = {l: len(OT.path_tokens(t.seg_start, t.seg_len, t.parent, l)) for l in leaves}
+    by_len = sorted(leaves, key=lambda l: plen[l])
+    chosen = [by_len[0], by_len[len(by_len) // 4]][:n_leaves]
+    q, k, v, do = (x[n].float().numpy() for n in ("q", "k", "v", "do"))
+    got = {n: [] for n in ("o", "lse", "dq", "dk", "dv")}
+    ref = {n: [] for n in got}
+    for leaf in chosen:
+        idx = OT.path_tokens(t.seg_start, t.seg_len, t.parent, leaf)
+        a0 = int(t.seg_start[leaf])
+        leafpos = np.nonzero(idx >= a0)[0]
+        others = np.setdiff1d(np.arange(len(idx)), leafpos)
+        pick = rng.choice(others, size=min(extra_rows, len(others)), replace=False) if len(others) else others
+        rows = np.sort(np.concatenate([leafpos, pick]))
+        is_leaf_row = idx[rows] >= a0
+        for g in groups:
+            hs = slice(g * G, (g + 1) * G)
+            r = A.path_attention(q, k, v, w.softmax_scale, idx, g, rows=rows, do=do)
+            got["o"].append(out["o"][idx[rows], hs])
+            ref["o"].append(r["O"])
+            got["lse"].append(out["lse"][hs][:, idx[rows]])
+            ref["lse"].append(r["LSE"])
+            got["dq"].append(out["dq"][idx[rows], hs])
+            ref["dq"].append(r["dQ"])
+            lp = rows[is_leaf_row]
+            got["dk"].append(out["dk"][idx[lp], g])
+            ref["dk"].append(r["dK"][lp])
+            got["dv"].append(out["dv"][idx[lp], g])
+            ref["dv"].append(r["dV"][lp])
+        par = int(t.parent[leaf])
+        if par >= 0:
+            p0, p1 = int(t.seg_start[par]), int(t.seg_start[par] + t.seg_len[par])
+            for g in groups:
+                sk, sv = A.subtree_key_grads(q, k, v, do, t.seg_start, t.seg_len, t.parent, w.softmax_scale, par, g)
+                got["dk"].append(out["dk"][p0:p1, g])
+                ref["dk"].append(sk)
+                got["dv"].append(out["dv"][p0:p1, g])
+                ref["dv"].append(sv)
+    cat = lambda L: np.concatenate([np.ravel(a) for a in L])  # noqa: E731
+    res = {n: rel_l2(cat(got[n]), cat(ref[n])) for n in ("o", "dq", "dk", "dv")}
+    res["o_abs"] = float(np.abs(cat(got["o"]) - cat(ref["o"])).max())
+    res["lse"] = float(np.abs(cat(got["lse"]) - cat(ref["lse"])).max())
+    print(w.name, "sampled", res)
+    assert res["o"] <= tol["o_rel"] and res["o_abs"] <= tol["o_abs"]
+    assert res["lse"] <= tol["lse"]
+    for n in ("dq", "dk", "dv"):
+        assert res[n] <= tol["g_rel"], n
+    return res
+
+
+def check_sums(w, x, out):
+    """Properties at any size: sum_j dV_j = sum_i sum_(h in group) dO_ih (rows
+    of P sum to 1) and sum_j dK_j = 0 (rows of dS sum to 0), per KV head."""
+    G = w.hq // w.hkv
+    do = x["do"].double()
+    T = w.T
+    for g in range(w.hkv):
+        dv = torch.from_numpy(out["dv"][:, g]).double()
+        dk = torch.from_numpy(out["dk"][:, g]).double()
+        want = do[:, g * G:(g + 1) * G].sum((0, 1))
+        # bf16 rounding of each row (2^-8 relative) adds up like a random walk
+        bound_v = 8 * np.sqrt(T) * float(dv.pow(2).mean().sqrt()) * 2.0 ** -8
+        bound_k = 8 * np.sqrt(T) * float(dk.pow(2).mean().sqrt()) * 2.0 ** -8
+        assert float((dv.sum(0) - want).abs().max()) <= bound_v
+        assert float(dk.sum(0).abs().max()) <= bound_k
+
+
+# ------------------------------------------------------------------ tests
+
+def test_tiny_f32_matches_oracle():
+    w = W.tiny()
+    for tt in (1, 7, 32, 64):
+        x, out = run_gpu(w, "f32", tile_tokens=tt, kv_block=64)
+        check_full(w, x, out, "f32")
+
+
+def test_tiny_bf16_matches_oracle():
+    w = W.tiny()
+    x, out = run_gpu(w, "bf16")
+    check_full(w, x, out, "bf16")
+    # the same result from the other schedule order
+    _, out2 = run_gpu(w, "bf16", order=1, x=x)
+    for n in out:
+        assert np.array_equal(out[n], out2[n]), n
+
+
+def test_single_segment_and_one_token_segments():
+    """Degenerate trees: one segment (plain causal), a chain of 1-token
+    segments, and a forest of 1-token roots (every token sees only itself)."""
+    rng = np.random.default_rng(5)
+    trees = [W.tree_from_preorder([300], [-1]),
+             W.tree_from_preorder([1] * 40, [-1] + list(range(39))),
+             W.tree_from_preorder([1] * 33, [-1] * 33),
+             W.random_small_tree(rng, max_segments=30, max_len=200)]
+    for tr in trees:
+        w = W.Workload("edge", "", tr, 8, 2, 128, 0.5, 9, None, None)
+        for dtype in ("bf16", "f32"):
+            x, out = run_gpu(w, dtype)
+            check_full(w, x, out, dtype)
+
+
+def test_star_bf16_matches_oracle():
+    w = W.grpo_star()
+    x, out = run_gpu(w, "bf16")
+    check_full(w, x, out, "bf16", groups=[0, w.hkv - 1])
+    check_sums(w, x, out)
+
+
+@pytest.mark.slow
+def test_agent_bf16_sampled():
+    w = W.agent_tree()
+    x, out = run_gpu(w, "bf16")
+    check_sampled(w, x, out, groups=[0, w.hkv - 1])
+    check_sums(w, x, out)
+
+
+@pytest.mark.slow
+def test_forest_bf16_sampled():
+    w = W.grpo_forest()
+    x, out = run_gpu(w, "bf16")
+    check_sampled(w, x, out, groups=[0, w.hkv - 1], extra_rows=128)
+    check_sums(w, x, out)
+
+
+@pytest.mark.slow
+def test_long_bf16_sampled():
+    w = W.long_fragment()
+    x, out = run_gpu(w, "bf16")
+    check_sampled(w, x, out, groups=[0], n_leaves=1, extra_rows=128)
+    check_sums(w, x, out)
+
+
+def test_sibling_isolation_bit_exact():
+    """Changing one branch's K/V leaves the forward output of every token
+    outside that branch's subtree bit-identical."""
+    w = W.tiny()
+    x = W.draw_tensors(w, "bf16")
+    _, out = run_gpu(w, "bf16", x=x)
+    x2 = {n: t.clone() for n, t in x.items()}
+    x2["k"][96:169] = (x2["k"][96:169].float() + 1).to(torch.bfloat16)
+    x2["v"][96:169] = (x2["v"][96:169].float() - 2).to(torch.bfloat16)
+    _, out2 = run_gpu(w, "bf16", x=x2)
+    outside = np.r_[0:96, 169:186]
+    assert np.array_equal(out["o"][outside], out2["o"][outside])
+    assert np.array_equal(out["lse"][:, outside], out2["lse"][:, outside])
+    assert not np.array_equal(out["o"][96:169], out2["o"][96:169])
+
+
+# --------------------------------------------------------------- edge_gather
+
+def _gather(hidden, idx):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = spc.edge_gather(hidden, idx, st)
+    torch.cuda.synchronize()
+    return out, st.item()
+
+
+@pytest.mark.parametrize("name", ["tiny", "star", "agent"])
+def test_edge_gather_bit_exact(name):
+    w = W.get(name)
+    x = W.draw_tensors(w, "bf16", with_hidden=True)
+    hidden = x["hidden"]
+    idx = torch.from_numpy(w.edge_idx)
+    out, st = _gather(hidden.cuda(), idx.cuda())
+    assert st == 0
+    want = hidden.view(torch.int16).numpy()[w.edge_idx]
+    assert np.array_equal(out.cpu().view(torch.int16).numpy(), want)
+
+
+def test_edge_gather_duplicates_fp32_and_bad_index():
+    g = torch.Generator().manual_seed(3)
+    h = torch.randn(100, 36, generator=g)
+    idx = torch.tensor([5, 5, 99, 0, 5], dtype=torch.int32)
+    out, st = _gather(h.cuda(), idx.cuda())
+    assert st == 0
+    assert np.array_equal(out.cpu().view(torch.int32).numpy(), h.view(torch.int32).numpy()[idx.numpy()])
+    bad = torch.tensor([1, 100, -1, 2], dtype=torch.int32)
+    out, st = _gather(h.cuda(), bad.cuda())
+    assert st == spc.SP_DEV_INDEX_RANGE
+    o = out.cpu()
+    assert torch.equal(o[0], h[1]) and torch.equal(o[3], h[2])
+    assert (o[1] == 0).all() and (o[2] == 0).all()
+    empty, st = _gather(h.cuda(), torch.zeros(0, dtype=torch.int32, device="cuda"))
+    assert empty.shape == (0, 36) and st == 0

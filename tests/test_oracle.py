@@ -352,3 +352,16 @@ def test_edge_gather_oracle():
         OG.edge_gather(h, [6])
     with pytest.raises(IndexError):
         OG.edge_gather(h, [-1])
+
+
+def test_subtree_key_grads_equal_full_backward():
+    t = W.tiny().tree
+    rng = np.random.default_rng(17)
+    q, k, v, do = _rand(rng, t.total_tokens, 4, 2, 8)
+    _, dK, dV = A.tree_backward(q, k, v, do, *_tree_args(t), 0.4)
+    for s in range(t.num_segments):
+        a0, a1 = int(t.seg_start[s]), int(t.seg_start[s] + t.seg_len[s])
+        for g in range(2):
+            sk, sv = A.subtree_key_grads(q, k, v, do, *_tree_args(t), 0.4, s, g)
+            np.testing.assert_allclose(sk, dK[a0:a1, g], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(sv, dV[a0:a1, g], rtol=0, atol=1e-12)
