@@ -21,10 +21,12 @@ int check_heads(int32_t dtype, int32_t T, int32_t Hq, int32_t Hkv, int32_t D) {
   return SP_OK;
 }
 
-// Tiling each kernel family accepts (see the header's sp_tree_plan notes).
+// Tiling each kernel family accepts (see the header's sp_tree_plan notes):
+// the tensor-core kernels (bf16) need 128-row query tiles and 128-key blocks;
+// the fp32 kernels take any tiling up to those sizes.
 int check_tiling(const sp_plan &p, int32_t dtype, int32_t G) {
+  if (dtype == SP_BF16) return (p.tile_tokens * G == 128 && p.kv_block == 128) ? SP_OK : SP_ERR_UNSUPPORTED;
   if (p.tile_tokens * G > 128 || p.kv_block > 128) return SP_ERR_UNSUPPORTED;
-  (void)dtype;
   return SP_OK;
 }
 
@@ -121,6 +123,7 @@ int sp_tree_attn_fwd(const sp_plan *p, int32_t dtype, const void *q, const void 
   const int G = Hq / Hkv;
   if (int rc = check_tiling(*p, dtype, G)) return rc;
   const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
+  if (dtype == SP_BF16) return spc::tc_fwd(plan_dev(*p), s, q, k, v, o, lse, d_status, stream);
   return spc::simt_fwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_status, stream);
 }
 
