@@ -1,0 +1,481 @@
+// Tree attention backward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// The backward "accumulates branch contributions into the shared prefix"
+// (#7914, "feat(hybrid): add opt-in shared-prefix attention and Mamba
+// execution", introduction).  In preorder, the queries that can see a key are
+// exactly the key's own later tokens and every token of its segment's
+// subtree: one contiguous run [kv_start, subtree end).  So each CTA owns one
+// block of 128 keys of one KV head, keeps dK and dV for it in TMEM, and walks
+// that query run in 64-row blocks (64 / G tokens x the G query heads of the
+// KV head).  Every child branch below a prefix adds into the same TMEM
+// accumulators; nothing is scattered.  Per query block, FlashAttention-style
+// recomputation from the saved LSE:
+//   S^T  = K Q^T          dP^T = V dO^T                    (tensor cores)
+//   P^T  = exp(S^T - LSE) dS^T = P^T (dP^T - Delta)        (4 softmax warps)
+//   dV  += P^T dO         dK  += dS^T Q                    (tensor cores)
+//   dQ^T = K^T dS^T  -> fp32 atomics into the dQ workspace (4 dQ warps)
+// dQ is formed transposed (M = head_dim) so it needs only 64 TMEM columns per
+// buffer: S^T, dP^T, two dQ^T buffers, dK and dV fill the 512 columns.
+//
+// Roles: warps 0-3 softmax and the dK/dV epilogue (TMEM lane = key row),
+// warps 4-7 dQ readout (TMEM lane = head-dim index), warp 8 TMA producer
+// (Q, dO, and the per-column LSE / Delta staged by the whole warp), warp 9
+// the single-thread MMA issuer.  The MMA issue order is software pipelined:
+// S^T and dP^T of block j are issued before dV, dK and dQ^T of block j-1, so
+// the softmax of block j overlaps the second half of block j-1.
+//
+// Companion kernels: bwd_pre (Delta = rowsum(dO * O) and zeroing the fp32 dQ
+// workspace) and dq_convert (scale and round dQ to bf16).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
+namespace spc {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBK = 128;            // keys per CTA
+constexpr int kBQ = 64;             // query rows per block
+constexpr int kThreads = 320;       // 10 warps
+constexpr int kKChunk = 128 * 128;  // 128 rows x 128 bytes
+constexpr int kQChunk = 64 * 128;   // 64 rows x 128 bytes
+constexpr uint32_t kSpinLimit = 1u << 22;
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int {
+  B_KV_FULL = 0,
+  B_Q_FULL = 1,    // +stage (2)
+  B_Q_EMPTY = 3,   // +stage
+  B_S_FULL = 5,
+  B_S_FREE = 6,
+  B_P_FULL = 7,    // +buffer (2)
+  B_P_FREE = 9,    // +buffer
+  B_DQ_FULL = 11,  // +buffer
+  B_DQ_FREE = 13,  // +buffer
+  B_FINAL = 15,
+  B_COUNT = 16
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kDChunks = D / 64;
+  // K keeps two 64-column chunks even for D = 64 (the second one zeroed) so
+  // that dQ^T = K^T dS^T always runs as an M = 128 MMA.
+  static constexpr int K = 0;
+  static constexpr int V = K + 2 * kKChunk;
+  static constexpr int STAGE = V + kDChunks * kKChunk;
+  static constexpr int Q_OFF = 0;                        // within a stage
+  static constexpr int DO_OFF = kDChunks * kQChunk;
+  static constexpr int STAT_OFF = 2 * kDChunks * kQChunk;  // lse2[64], delta[64]
+  static constexpr int STAGE_BYTES = STAT_OFF + 1024;   // keep 1024-byte alignment
+  static constexpr int PS = STAGE + 2 * STAGE_BYTES;    // two buffers of {P^T, dS^T}
+  static constexpr int PS_BYTES = 2 * kKChunk;
+  static constexpr int BAR = PS + 2 * PS_BYTES;
+  static constexpr int TSLOT = BAR + 8 * B_COUNT;
+  static constexpr int ABORT = TSLOT + 4;
+  static constexpr int BYTES = ABORT + 4 + 1024;
+  static constexpr int ALLOC = BYTES > 120 * 1024 ? BYTES : 120 * 1024;
+  static constexpr uint32_t QTILE_BYTES = kDChunks * kQChunk;  // one of Q / dO for a block
+};
+
+// TMEM columns
+constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DK = 256;
+
+struct Ctl {
+  uint32_t bar0;
+  volatile int *abort;
+  int32_t *d_status;
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * uint32_t(i); }
+  __device__ bool wait(int i, uint32_t parity) const {
+    for (uint32_t it = 0;; ++it) {
+      if (mbar_try_wait(bar(i), parity)) return true;
+      if ((it & 255u) == 255u) {
+        if (*abort) return false;
+        if (it >= kSpinLimit) {
+          *abort = 1;
+          if (d_status) atomicOr(d_status, SP_DEV_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  // Same, agreed by the whole warp (warp-collective tcgen05 loads follow).
+  __device__ bool wait_warp(int i, uint32_t parity) const {
+    const bool r = wait(i, parity);
+    return __all_sync(0xffffffffu, r);
+  }
+  __device__ void drain(int i, uint32_t parity) const {
+    for (uint32_t it = 0; it < kSpinLimit; ++it)
+      if (mbar_try_wait(bar(i), parity)) return;
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
+                  AttnShape s, const float *__restrict__ lse, const float *__restrict__ delta,
+                  float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
+                  int32_t *d_status) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int g = blockIdx.x / plan.n_bwd;
+  const int *blk = plan.bwd + 5 * (blockIdx.x % plan.n_bwd);
+  const int k0 = blk[1], k1 = blk[2], qb = blk[3], qe = blk[4];
+  const int G = s.G, T = s.T, Hq = s.Hq;
+  if (!(0 <= k0 && k0 < k1 && k1 - k0 <= kBK && qb == k0 && k1 <= qe && qe <= T)) {
+    if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
+    return;
+  }
+  const int tpb = kBQ / G;  // query tokens per block
+  const int nq = (qe - qb + tpb - 1) / tpb;
+
+  Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i) {
+      uint32_t cnt = 1;
+      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1 || i == B_DQ_FREE || i == B_DQ_FREE + 1) cnt = 128;
+      mbar_init(ctl.bar(i), cnt);
+    }
+    *ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (D == 64 && warp < 4) {
+    // zero the padding chunk of K (read by the M = 128 dQ^T MMA)
+    uint4 *z = reinterpret_cast<uint4 *>(smem + L::K + kKChunk);
+    for (int i = threadIdx.x; i < kKChunk / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(sbase + L::TSLOT, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(ctl.bar(B_KV_FULL), 2u * L::kDChunks * kKChunk);
+#pragma unroll
+      for (int c = 0; c < L::kDChunks; ++c) {
+        tma_load_3d(sbase + L::K + c * kKChunk, &tm_k, ctl.bar(B_KV_FULL), c * 64, g, k0);
+        tma_load_3d(sbase + L::V + c * kKChunk, &tm_v, ctl.bar(B_KV_FULL), c * 64, g, k0);
+      }
+    }
+    int j = 0;
+    for (; j < nq; ++j) {
+      const int st = j & 1;
+      if (!ctl.wait_warp(B_Q_EMPTY + st, ((j >> 1) & 1) ^ 1)) break;
+      const int qt = qb + j * tpb;
+      const uint32_t stage = L::STAGE + st * L::STAGE_BYTES;
+      float *stat = reinterpret_cast<float *>(smem + stage + L::STAT_OFF);
+      for (int c = lane; c < kBQ; c += 32) {
+        const int tok = qt + c / G, head = g * G + c % G;
+        const bool ok = tok < qe;
+        stat[c] = ok ? __ldg(lse + size_t(head) * T + tok) * kLog2e : 0.f;
+        stat[kBQ + c] = ok ? __ldg(delta + size_t(head) * T + tok) : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(ctl.bar(B_Q_FULL + st), 2u * L::QTILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < L::kDChunks; ++c) {
+          tma_load_3d(sbase + stage + L::Q_OFF + c * kQChunk, &tm_q, ctl.bar(B_Q_FULL + st), c * 64, g * G, qt);
+          tma_load_3d(sbase + stage + L::DO_OFF + c * kQChunk, &tm_do, ctl.bar(B_Q_FULL + st), c * 64, g * G, qt);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0 && *ctl.abort) {
+      ctl.drain(B_KV_FULL, 0);
+      for (int m = j - 2 < 0 ? 0 : j - 2; m < j; ++m) ctl.drain(B_Q_FULL + (m & 1), (m >> 1) & 1);
+    }
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(kBK, kBQ, 0, 0);  // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_bf16_f32(kBK, D, 0, 1);   // dV, dK
+      constexpr uint32_t id_q = idesc_bf16_f32(128, kBQ, 1, 1);  // dQ^T
+      bool ok = ctl.wait(B_KV_FULL, 0);
+      tc_fence_after();
+      for (int j = 0; ok && j <= nq; ++j) {
+        if (j < nq) {
+          const int st = j & 1;
+          const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
+          if (!(ok = ctl.wait(B_Q_FULL + st, (j >> 1) & 1))) break;
+          if (!(ok = ctl.wait(B_S_FREE, (j & 1) ^ 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * kKChunk + (kk & 3) * 32;
+            const uint32_t qa = (kk >> 2) * kQChunk + (kk & 3) * 32;
+            mma_bf16_ss(tmem + T_S, smem_desc_sw128(sbase + L::K + ka, 16, 1024),
+                        smem_desc_sw128(stage + L::Q_OFF + qa, 16, 1024), id_s, kk > 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = (kk >> 2) * kKChunk + (kk & 3) * 32;
+            const uint32_t qa = (kk >> 2) * kQChunk + (kk & 3) * 32;
+            mma_bf16_ss(tmem + T_DP, smem_desc_sw128(sbase + L::V + ka, 16, 1024),
+                        smem_desc_sw128(stage + L::DO_OFF + qa, 16, 1024), id_s, kk > 0);
+          }
+          mma_commit(ctl.bar(B_S_FULL));
+        }
+        if (j >= 1) {
+          const int m = j - 1, st = m & 1, pb = m & 1;
+          const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
+          const uint32_t pt = sbase + L::PS + pb * L::PS_BYTES;  // P^T
+          const uint32_t dst = pt + kKChunk;                    // dS^T
+          if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
+          if (!(ok = ctl.wait(B_DQ_FREE + pb, ((m >> 1) & 1) ^ 1))) break;
+          tc_fence_after();
+          // dV += P^T dO ; dK += dS^T Q   (K = 64 query rows)
+#pragma unroll
+          for (int kk = 0; kk < kBQ / 16; ++kk) {
+            mma_bf16_ss(tmem + T_DK + D, smem_desc_sw128(pt + kk * 32, 16, 1024),
+                        smem_desc_sw128(stage + L::DO_OFF + kk * 2048, kQChunk, 1024), id_kv, (m > 0 || kk > 0));
+          }
+#pragma unroll
+          for (int kk = 0; kk < kBQ / 16; ++kk) {
+            mma_bf16_ss(tmem + T_DK, smem_desc_sw128(dst + kk * 32, 16, 1024),
+                        smem_desc_sw128(stage + L::Q_OFF + kk * 2048, kQChunk, 1024), id_kv, (m > 0 || kk > 0));
+          }
+          // dQ^T = K^T dS^T   (K = 128 keys)
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            mma_bf16_ss(tmem + T_DQ + 64 * pb, smem_desc_sw128(sbase + L::K + kk * 2048, kKChunk, 1024),
+                        smem_desc_sw128(dst + kk * 2048, kQChunk, 1024), id_q, kk > 0);
+          }
+          mma_commit(ctl.bar(B_DQ_FULL + pb));
+          mma_commit(ctl.bar(B_P_FREE + pb));
+          mma_commit(ctl.bar(B_Q_EMPTY + st));
+        }
+      }
+      mma_commit(ctl.bar(B_FINAL));
+      ctl.drain(B_FINAL, 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------- softmax + dK/dV epilogue
+    const int r = threadIdx.x;  // key row = TMEM lane
+    const uint32_t lane_base = uint32_t(32 * warp) << 16;
+    const int key = k0 + r;
+    const bool kvalid = key < k1;
+    const float sl2 = s.scale * kLog2e;
+    bool ok = true;
+    for (int j = 0; j < nq; ++j) {
+      const int st = j & 1, pb = j & 1;
+      const int qt = qb + j * tpb;
+      const float *stat = reinterpret_cast<const float *>(smem + L::STAGE + st * L::STAGE_BYTES + L::STAT_OFF);
+      if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j >> 1) & 1))) break;
+      if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
+      if (!(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;
+      tc_fence_after();
+      const uint32_t prow = sbase + L::PS + pb * L::PS_BYTES + r * 128;
+      const bool nomask = qt + tpb <= qe && qt >= k1 - 1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // 32 query columns at a time
+        uint32_t us[32], ud[32];
+        tmem_ld32(tmem + lane_base + T_S + 32 * h, us);
+        tmem_ld32(tmem + lane_base + T_DP + 32 * h, ud);
+        if (h == 1) {
+          tc_fence_before();
+          mbar_arrive(ctl.bar(B_S_FREE));
+        }
+        float pv[32], dsv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 32 * h + i;
+          bool vis = kvalid;
+          if (!nomask) {
+            const int tok = qt + c / G;
+            vis = vis && tok < qe && key <= tok;
+          }
+          const float p = vis ? ex2(fmaf(__uint_as_float(us[i]), sl2, -stat[c])) : 0.f;
+          pv[i] = p;
+          dsv[i] = p * (__uint_as_float(ud[i]) - stat[kBQ + c]);
+        }
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          const int u8 = 4 * h + u4;
+          const float *x = pv + 8 * u4;
+          const float *y = dsv + 8 * u4;
+          const uint32_t off = (u8 ^ (r & 7)) << 4;
+          st_shared_v4(prow + off, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
+                       pack_bf16(x[6], x[7]));
+          st_shared_v4(prow + kKChunk + off, pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                       pack_bf16(y[6], y[7]));
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(ctl.bar(B_P_FULL + pb));
+    }
+    if (ok && ctl.wait_warp(B_FINAL, 0)) {
+      tc_fence_after();
+      const float sc = s.scale;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // 0: dK (scaled), 1: dV
+        __nv_bfloat16 *dst = (half == 0 ? dk : dv) + (size_t(key) * s.Hkv + g) * D;
+        const float mul = half == 0 ? sc : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + T_DK + half * D + 32 * c, u);
+          if (kvalid) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 w;
+              w.x = pack_bf16(__uint_as_float(u[i]) * mul, __uint_as_float(u[i + 1]) * mul);
+              w.y = pack_bf16(__uint_as_float(u[i + 2]) * mul, __uint_as_float(u[i + 3]) * mul);
+              w.z = pack_bf16(__uint_as_float(u[i + 4]) * mul, __uint_as_float(u[i + 5]) * mul);
+              w.w = pack_bf16(__uint_as_float(u[i + 6]) * mul, __uint_as_float(u[i + 7]) * mul);
+              *reinterpret_cast<uint4 *>(dst + 32 * c + i) = w;
+            }
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- dQ readout
+    const int d = 32 * (warp - 4) + lane;  // TMEM lane = head-dim index
+    const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
+    for (int j = 0; j < nq; ++j) {
+      const int pb = j & 1;
+      const int qt = qb + j * tpb;
+      if (!ctl.wait_warp(B_DQ_FULL + pb, (j >> 1) & 1)) break;
+      tc_fence_after();
+      uint32_t u0[32], u1[32];
+      tmem_ld32(tmem + lane_base + T_DQ + 64 * pb, u0);
+      tmem_ld32(tmem + lane_base + T_DQ + 64 * pb + 32, u1);
+      tc_fence_before();
+      mbar_arrive(ctl.bar(B_DQ_FREE + pb));
+      if (d < D) {
+        // query row c is token qt + c / G, head g * G + c % G
+        float *base = dqacc + (size_t(qt) * Hq + g * G) * D + d;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (qt + c / G < qe) atomicAdd(base + size_t((c / G) * Hq + c % G) * D, __uint_as_float(u0[c]));
+#pragma unroll
+        for (int c = 32; c < 64; ++c)
+          if (qt + c / G < qe) atomicAdd(base + size_t((c / G) * Hq + c % G) * D, __uint_as_float(u1[c - 32]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Delta = rowsum(dO * O) per (token, query head) in fp32, and zero the fp32
+// dQ workspace.  One warp per row; 16-byte loads.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
+                                                      const __nv_bfloat16 *__restrict__ d_o,
+                                                      float *__restrict__ delta, float *__restrict__ dqacc, int T,
+                                                      int Hq) {
+  const int lane = threadIdx.x & 31;
+  const long rows = long(T) * Hq;
+  for (long row = (long(blockIdx.x) * 256 + threadIdx.x) / 32; row < rows; row += long(gridDim.x) * 8) {
+    float acc = 0.f;
+    if (lane * 8 < D) {
+      const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + lane * 8);
+      const uint4 b = *reinterpret_cast<const uint4 *>(d_o + row * D + lane * 8);
+      const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
+      const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x = __bfloat1622float2(pa[i]), y = __bfloat1622float2(pb[i]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    float4 *z = reinterpret_cast<float4 *>(dqacc + row * D);
+    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) delta[size_t(row % Hq) * T + row / Hq] = acc;
+  }
+}
+
+// dq = bf16(scale * dqacc), 8 elements per thread per step.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ dqacc,
+                                                         __nv_bfloat16 *__restrict__ dq, float scale, long n8) {
+  for (long i = long(blockIdx.x) * 256 + threadIdx.x; i < n8; i += long(gridDim.x) * 256) {
+    const float4 a = reinterpret_cast<const float4 *>(dqacc)[2 * i];
+    const float4 b = reinterpret_cast<const float4 *>(dqacc)[2 * i + 1];
+    uint4 w;
+    w.x = pack_bf16(a.x * scale, a.y * scale);
+    w.y = pack_bf16(a.z * scale, a.w * scale);
+    w.z = pack_bf16(b.x * scale, b.y * scale);
+    w.w = pack_bf16(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4 *>(dq)[i] = w;
+  }
+}
+
+template <int D>
+int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
+           const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
+           int32_t *d_status, cudaStream_t st) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long rows = long(s.T) * s.Hq;
+  const int pre_grid = int(std::min<long>((rows + 7) / 8, long(sms) * 16));
+  bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(o),
+                                               static_cast<const __nv_bfloat16 *>(d_o), delta, dqacc, s.T, s.Hq);
+  if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
+
+  CUtensorMap tq, tdo, tk, tv;
+  int rc = encode_bf16_3d(&tq, q, D, s.Hq, s.T, 64, s.G, kBQ / s.G);
+  if (!rc) rc = encode_bf16_3d(&tdo, d_o, D, s.Hq, s.T, 64, s.G, kBQ / s.G);
+  if (!rc) rc = encode_bf16_3d(&tk, k, D, s.Hkv, s.T, 64, 1, kBK);
+  if (!rc) rc = encode_bf16_3d(&tv, v, D, s.Hkv, s.T, 64, 1, kBK);
+  if (rc) return rc;
+  auto kern = bwd_tc_kernel<D>;
+  const int smem = Layout<D>::ALLOC;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return SP_ERR_CUDA;
+  const unsigned grid = unsigned(p.n_bwd) * unsigned(s.Hkv);
+  kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, dqacc, static_cast<__nv_bfloat16 *>(dk),
+                                     static_cast<__nv_bfloat16 *>(dv), d_status);
+  if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
+
+  const long n8 = rows * D / 8;
+  const int cgrid = int(std::min<long>((n8 + 255) / 256, long(sms) * 16));
+  dq_convert_kernel<<<cgrid, 256, 0, st>>>(dqacc, static_cast<__nv_bfloat16 *>(dq), s.scale, n8);
+  return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+}  // namespace
+
+int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
+           const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
+           int32_t *d_status, void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return s.D == 64 ? launch<64>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, st)
+                   : launch<128>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, st);
+}
+
+}  // namespace spc

@@ -101,6 +101,11 @@ struct Ctl {
     }
   }
   // Bounded wait used while draining after an abort (ignores the flag).
+  // Same, agreed by the whole warp (warp-collective tcgen05 loads follow).
+  __device__ bool wait_warp(int i, uint32_t parity) const {
+    const bool r = wait(i, parity);
+    return __all_sync(0xffffffffu, r);
+  }
   __device__ void drain(int i, uint32_t parity) const {
     for (uint32_t it = 0; it < kSpinLimit; ++it)
       if (mbar_try_wait(bar(i), parity)) return;
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool causal = ri == rc - 1;
       for (int kb = kv0; kb < kv1; kb += kBN, ++n) {
         const int sb = n & 1;
-        if (!(ok = ctl.wait(B_S_FULL + sb, (n >> 1) & 1))) break;
+        if (!(ok = ctl.wait_warp(B_S_FULL + sb, (n >> 1) & 1))) break;
         tc_fence_after();
         float sv[kBN];
 #pragma unroll
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run = l_run * alpha + rs;
 
         if (n >= 1) {
-          if (!(ok = ctl.wait(B_PV_DONE, (n - 1) & 1))) break;
+          if (!(ok = ctl.wait_warp(B_PV_DONE, (n - 1) & 1))) break;
           tc_fence_after();
           if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = m_new;
       }
     }
-    if (ok && ctl.wait(B_PV_DONE, (nblocks - 1) & 1)) {
+    if (ok && ctl.wait_warp(B_PV_DONE, (nblocks - 1) & 1)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const bool store = r < rows_valid;

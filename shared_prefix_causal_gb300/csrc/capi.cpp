@@ -127,11 +127,13 @@ int sp_tree_attn_fwd(const sp_plan *p, int32_t dtype, const void *q, const void 
   return spc::simt_fwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_status, stream);
 }
 
+// Workspace: Delta [Hq][T] fp32, then (bf16 only) the fp32 dQ accumulator
+// [T][Hq][D] that the tensor-core backward reduces into.
 size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t Hq, int32_t D) {
-  (void)dtype;
-  (void)D;
-  if (T <= 0 || Hq <= 0) return 0;
-  return align_up(size_t(T) * size_t(Hq) * sizeof(float));  // Delta [Hq][T]
+  if (T <= 0 || Hq <= 0 || D <= 0) return 0;
+  const size_t delta = align_up(size_t(T) * size_t(Hq) * sizeof(float));
+  if (dtype != SP_BF16) return delta;
+  return delta + align_up(size_t(T) * size_t(Hq) * size_t(D) * sizeof(float));
 }
 
 int sp_tree_attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, const void *o,
@@ -154,8 +156,13 @@ int sp_tree_attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void 
   const int G = Hq / Hkv;
   if (int rc = check_tiling(*p, dtype, G)) return rc;
   const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
-  return spc::simt_bwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_o, dq, dk, dv, static_cast<float *>(workspace),
-                       d_status, stream);
+  float *delta = static_cast<float *>(workspace);
+  if (dtype == SP_BF16) {
+    float *dqacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                             align_up(size_t(T) * size_t(Hq) * sizeof(float)));
+    return spc::tc_bwd(plan_dev(*p), s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, stream);
+  }
+  return spc::simt_bwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_o, dq, dk, dv, delta, d_status, stream);
 }
 
 int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_dim, const int32_t *idx, int32_t E,

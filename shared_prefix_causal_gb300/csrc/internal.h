@@ -51,6 +51,10 @@ int simt_bwd(const PlanDev &p, const AttnShape &s, int32_t dtype, const void *q,
 // Tensor-core kernels (sm_103a): bf16 input, tile_tokens * G == 128, kv_block == 128.
 int tc_fwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, void *o, float *lse,
            int32_t *d_status, void *stream);
+// delta: [Hq][T] fp32 scratch; dqacc: [T][Hq][D] fp32 scratch (zeroed inside).
+int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
+           const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
+           int32_t *d_status, void *stream);
 
 // edge_gather (edge_gather.cu).
 int edge_gather(int32_t elem_bytes, const void *hidden, int32_t T, int32_t hidden_dim,

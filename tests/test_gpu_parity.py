@@ -159,11 +159,17 @@ def check_sums(w, x, out):
     for g in range(w.hkv):
         dv = torch.from_numpy(out["dv"][:, g]).double()
         dk = torch.from_numpy(out["dk"][:, g]).double()
-        want = do[:, g * G:(g + 1) * G].sum((0, 1))
-        # bf16 rounding of each row (2^-8 relative) adds up like a random walk
-        bound_v = 8 * np.sqrt(T) * float(dv.pow(2).mean().sqrt()) * 2.0 ** -8
+        dog = do[:, g * G:(g + 1) * G]
+        want = dog.sum((0, 1))
+        # Two rounding sources, each adding up like a random walk: the bf16
+        # outputs (2^-8 relative per row) and, on the tensor-core path, P
+        # rounded to bf16 before P^T dO, so that each query row's weights
+        # sum to 1 + e with |e| <~ 2^-9 (sign random across rows): per head-dim
+        # column that is 2^-9 * ||dO[:, :, d]||_2.
+        bound_v = 8 * np.sqrt(T) * float(dv.pow(2).mean().sqrt()) * 2.0 ** -8 + \
+            4 * 2.0 ** -9 * dog.pow(2).sum((0, 1)).sqrt()
         bound_k = 8 * np.sqrt(T) * float(dk.pow(2).mean().sqrt()) * 2.0 ** -8
-        assert float((dv.sum(0) - want).abs().max()) <= bound_v
+        assert bool(((dv.sum(0) - want).abs() <= bound_v).all())
         assert float(dk.sum(0).abs().max()) <= bound_k
 
 
