@@ -312,7 +312,7 @@ def run_gpu(args):
     bwd_tflops = f_bwd / (med_bwd * 1e-3) / 1e12
     mean_bwd = statistics.mean(bwd_ms)
     mean_fwd = statistics.mean(fwd_ms)
-    e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 else None
+    e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 and not args.no_e2e else None
 
     line = {
         "metric": METRIC,
@@ -451,6 +451,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="agent", choices=list(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--cpu-flops", type=float, default=6e11, help="fp64 flop budget of the CPU-baseline sample")
     ap.add_argument("--ref-flops", type=float, default=1.2e11, help="fp64 flop budget per reference step")
     ap.add_argument("--_oracle-child", dest="oracle_child", default=None, help=argparse.SUPPRESS)
