@@ -167,6 +167,28 @@ SP_API int sp_tree_attn_bwd(const sp_plan *plan, int32_t dtype, const void *q, c
                      int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale, int32_t *d_status,
                      void *stream);
 
+/* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
+#define SP_NOALLOC_SCRATCH_BYTES (64u << 20)
+
+/* tree_attn_bwd without a workspace argument, for callers that cannot
+ * allocate device memory (for example code running under a memory pool that
+ * owns the whole device, or a plugin that is handed only its inputs and
+ * outputs).  The pages have no counterpart: this is a packaging variant of
+ * tree_attn_bwd with identical arguments and results, minus the workspace.
+ *   Scratch: a fixed SP_NOALLOC_SCRATCH_BYTES array in device memory that the
+ *   library holds on every GPU where it is loaded, until process exit.  The
+ *   first call on a device looks up that array's address (do it before any
+ *   stream capture).  All calls on a device share the array, so calls that
+ *   overlap on the GPU race; serialise them.  Nothing is allocated.
+ *   Limit: sp_tree_attn_bwd_workspace_bytes(dtype, T, Hq, D) must not exceed
+ *   SP_NOALLOC_SCRATCH_BYTES (bf16 needs 4 * T * Hq * (D + 1) bytes, e.g.
+ *   T * Hq <= 129,000 rows at D = 128), otherwise SP_ERR_WORKSPACE.
+ * Errors: as sp_tree_attn_bwd. */
+SP_API int sp_tree_attn_bwd_noalloc(const sp_plan *plan, int32_t dtype, const void *q, const void *k,
+                                    const void *v, const void *o, const float *lse, const void *d_o,
+                                    void *dq, void *dk, void *dv, int32_t T, int32_t Hq, int32_t Hkv,
+                                    int32_t D, float softmax_scale, int32_t *d_status, void *stream);
+
 /* edge_gather -- out[e][:] = hidden[idx[e]][:] for e < E: the sampled-edge
  * source rows that go on to the vocabulary projection (issue #7386, fifth
  * bullet; PR #7387, "Summary", fourth bullet).  hidden [T][hidden_dim] and

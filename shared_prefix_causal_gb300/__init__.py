@@ -65,11 +65,16 @@ _c_ws = _sig("sp_tree_attn_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32, _
 _c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_bwd_noalloc = _sig("sp_tree_attn_bwd_noalloc", ctypes.c_int,
+                      [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                       _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_gather = _sig("sp_edge_gather", ctypes.c_int, [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp])
 _c_status = _sig("sp_status_string", ctypes.c_char_p, [ctypes.c_int])
 
 EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
-            "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_edge_gather", "sp_status_string")
+            "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
+            "sp_status_string")
+NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class SPError(RuntimeError):
@@ -201,6 +206,21 @@ def sp_tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, so
     _check(_c_bwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
                   _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D, float(softmax_scale),
                   _ptr(d_status), _stream(stream)), "sp_tree_attn_bwd")
+
+
+def sp_tree_attn_bwd_noalloc(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, softmax_scale: float,
+                             d_status=None, stream=None):
+    """sp_tree_attn_bwd backed by the library's fixed device scratch (no workspace)."""
+    _need_cuda(q, k, v, o, lse, d_o, dq, dk, dv, d_status)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    for t, shp in ((k, (T, Hkv, D)), (v, (T, Hkv, D)), (o, (T, Hq, D)), (d_o, (T, Hq, D)), (dq, (T, Hq, D)),
+                   (dk, (T, Hkv, D)), (dv, (T, Hkv, D))):
+        if tuple(t.shape) != shp or t.dtype != q.dtype:
+            raise ValueError("shape or dtype mismatch")
+    _check(_c_bwd_noalloc(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                          _ptr(dq), _ptr(dk), _ptr(dv), T, Hq, Hkv, D, float(softmax_scale), _ptr(d_status),
+                          _stream(stream)), "sp_tree_attn_bwd_noalloc")
 
 
 def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
