@@ -49,15 +49,17 @@ constexpr int kQChunk = 64 * 128;   // 64 rows x 128 bytes
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 
+constexpr int kStages = 3;  // Q/dO ring depth
+
 enum : int {
   B_KV_FULL = 0,
-  B_Q_FULL = 1,    // +stage (2)
-  B_Q_EMPTY = 3,   // +stage
-  B_S_FULL = 5,
-  B_S_FREE = 6,
-  B_P_FULL = 7,    // +buffer (2)
-  B_P_FREE = 9,    // +buffer
-  B_DQ_FULL = 11,  // +buffer
+  B_Q_FULL = 1,    // +stage (3)
+  B_Q_EMPTY = 4,   // +stage
+  B_S_FULL = 7,
+  B_S_FREE = 8,
+  B_P_FULL = 9,
+  B_P_FREE = 10,
+  B_DQ_FULL = 11,  // +buffer (2)
   B_DQ_FREE = 13,  // +buffer
   B_FINAL = 15,
   B_COUNT = 16
@@ -71,13 +73,13 @@ struct Layout {
   static constexpr int K = 0;
   static constexpr int V = K + 2 * kKChunk;
   static constexpr int STAGE = V + kDChunks * kKChunk;
-  static constexpr int Q_OFF = 0;                        // within a stage
+  static constexpr int Q_OFF = 0;                          // within a stage
   static constexpr int DO_OFF = kDChunks * kQChunk;
   static constexpr int STAT_OFF = 2 * kDChunks * kQChunk;  // lse2[64], delta[64]
-  static constexpr int STAGE_BYTES = STAT_OFF + 1024;   // keep 1024-byte alignment
-  static constexpr int PS = STAGE + 2 * STAGE_BYTES;    // two buffers of {P^T, dS^T}
+  static constexpr int STAGE_BYTES = STAT_OFF + 1024;     // keep 1024-byte alignment
+  static constexpr int PS = STAGE + kStages * STAGE_BYTES;  // {P^T, dS^T}
   static constexpr int PS_BYTES = 2 * kKChunk;
-  static constexpr int BAR = PS + 2 * PS_BYTES;
+  static constexpr int BAR = PS + PS_BYTES;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
   static constexpr int BYTES = ABORT + 4 + 1024;
@@ -106,10 +108,14 @@ struct Ctl {
       }
     }
   }
-  // Same, agreed by the whole warp (warp-collective tcgen05 loads follow).
+  // Same for a whole warp: one lane polls (32 lanes polling one barrier
+  // serialise on it and starve the warps that do the work), the others wait
+  // at __syncwarp, which also orders their later reads after lane 0's acquire.
   __device__ bool wait_warp(int i, uint32_t parity) const {
-    const bool r = wait(i, parity);
-    return __all_sync(0xffffffffu, r);
+    bool r = true;
+    if ((threadIdx.x & 31) == 0) r = wait(i, parity);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
   }
   __device__ void drain(int i, uint32_t parity) const {
     for (uint32_t it = 0; it < kSpinLimit; ++it)
@@ -117,7 +123,7 @@ struct Ctl {
   }
 };
 
-template <int D>
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
@@ -125,27 +131,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
                   int32_t *d_status) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, derived by pointer arithmetic so that accesses
+  // through it stay shared-memory (not generic) accesses
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int g = blockIdx.x / plan.n_bwd;
   const int *blk = plan.bwd + 5 * (blockIdx.x % plan.n_bwd);
   const int k0 = blk[1], k1 = blk[2], qb = blk[3], qe = blk[4];
-  const int G = s.G, T = s.T, Hq = s.Hq;
+  const int T = s.T, Hq = s.Hq;
   if (!(0 <= k0 && k0 < k1 && k1 - k0 <= kBK && qb == k0 && k1 <= qe && qe <= T)) {
     if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
     return;
   }
-  const int tpb = kBQ / G;  // query tokens per block
+  constexpr int tpb = kBQ / G;  // query tokens per block
   const int nq = (qe - qb + tpb - 1) / tpb;
 
   Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1 || i == B_DQ_FREE || i == B_DQ_FREE + 1) cnt = 128;
+      if (i == B_S_FREE || i == B_P_FULL || i == B_DQ_FREE || i == B_DQ_FREE + 1) cnt = 128;
       mbar_init(ctl.bar(i), cnt);
     }
     *ctl.abort = 0;
@@ -180,33 +188,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sbase + L::V + c * kKChunk, &tm_v, ctl.bar(B_KV_FULL), c * 64, g, k0);
       }
     }
+    // LSE (as log2) and Delta of the next block's 64 columns, loaded one block
+    // ahead so their latency hides behind the ring wait.
+    float nl[2], nd[2];
+    auto load_stats = [&](int jj) {
+      const int qt = qb + jj * tpb;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        const int tok = qt + c / G, head = g * G + c % G;
+        const bool ok = jj < nq && tok < qe;
+        nl[h] = ok ? __ldg(lse + size_t(head) * T + tok) * kLog2e : 0.f;
+        nd[h] = ok ? __ldg(delta + size_t(head) * T + tok) : 0.f;
+      }
+    };
+    load_stats(0);
     int j = 0;
     for (; j < nq; ++j) {
-      const int st = j & 1;
-      if (!ctl.wait_warp(B_Q_EMPTY + st, ((j >> 1) & 1) ^ 1)) break;
+      const int st = j % kStages;
+      if (!ctl.wait_warp(B_Q_EMPTY + st, ((j / kStages) & 1) ^ 1)) break;
       const int qt = qb + j * tpb;
       const uint32_t stage = L::STAGE + st * L::STAGE_BYTES;
-      float *stat = reinterpret_cast<float *>(smem + stage + L::STAT_OFF);
-      for (int c = lane; c < kBQ; c += 32) {
-        const int tok = qt + c / G, head = g * G + c % G;
-        const bool ok = tok < qe;
-        stat[c] = ok ? __ldg(lse + size_t(head) * T + tok) * kLog2e : 0.f;
-        stat[kBQ + c] = ok ? __ldg(delta + size_t(head) * T + tok) : 0.f;
-      }
-      __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(ctl.bar(B_Q_FULL + st), 2u * L::QTILE_BYTES);
+        // byte count first, copies next, the one arrival after the stats below
+        mbar_expect_tx(ctl.bar(B_Q_FULL + st), 2u * L::QTILE_BYTES);
 #pragma unroll
         for (int c = 0; c < L::kDChunks; ++c) {
           tma_load_3d(sbase + stage + L::Q_OFF + c * kQChunk, &tm_q, ctl.bar(B_Q_FULL + st), c * 64, g * G, qt);
           tma_load_3d(sbase + stage + L::DO_OFF + c * kQChunk, &tm_do, ctl.bar(B_Q_FULL + st), c * 64, g * G, qt);
         }
       }
+      float *stat = reinterpret_cast<float *>(smem + stage + L::STAT_OFF);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        stat[lane + 32 * h] = nl[h];
+        stat[kBQ + lane + 32 * h] = nd[h];
+      }
       __syncwarp();
+      if (lane == 0) mbar_arrive(ctl.bar(B_Q_FULL + st));
+      load_stats(j + 1);
     }
     if (lane == 0 && *ctl.abort) {
       ctl.drain(B_KV_FULL, 0);
-      for (int m = j - 2 < 0 ? 0 : j - 2; m < j; ++m) ctl.drain(B_Q_FULL + (m & 1), (m >> 1) & 1);
+      for (int m = j - kStages < 0 ? 0 : j - kStages; m < j; ++m)
+        ctl.drain(B_Q_FULL + m % kStages, (m / kStages) & 1);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
@@ -214,58 +239,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(kBK, kBQ, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16_f32(kBK, D, 0, 1);   // dV, dK
       constexpr uint32_t id_q = idesc_bf16_f32(128, kBQ, 1, 1);  // dQ^T
+      // operand descriptors, built once; a K step only moves the start address
+      const uint64_t dk_kmaj = smem_desc_sw128(sbase + L::K, 16, 1024);
+      const uint64_t dv_kmaj = smem_desc_sw128(sbase + L::V, 16, 1024);
+      const uint64_t dk_mn = smem_desc_sw128(sbase + L::K, kKChunk, 1024);
+      const uint64_t dpt = smem_desc_sw128(sbase + L::PS, 16, 1024);            // P^T, K-major
+      const uint64_t dst_kmaj = smem_desc_sw128(sbase + L::PS + kKChunk, 16, 1024);  // dS^T as A
+      const uint64_t dst_mn = smem_desc_sw128(sbase + L::PS + kKChunk, kQChunk, 1024);  // dS^T as B
       bool ok = ctl.wait(B_KV_FULL, 0);
       tc_fence_after();
       for (int j = 0; ok && j <= nq; ++j) {
         if (j < nq) {
-          const int st = j & 1;
+          const int st = j % kStages;
           const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
-          if (!(ok = ctl.wait(B_Q_FULL + st, (j >> 1) & 1))) break;
+          if (!(ok = ctl.wait(B_Q_FULL + st, (j / kStages) & 1))) break;
           if (!(ok = ctl.wait(B_S_FREE, (j & 1) ^ 1))) break;
           tc_fence_after();
+          const uint64_t dq_k = smem_desc_sw128(stage + L::Q_OFF, 16, 1024);
+          const uint64_t ddo_k = smem_desc_sw128(stage + L::DO_OFF, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * kKChunk + (kk & 3) * 32;
-            const uint32_t qa = (kk >> 2) * kQChunk + (kk & 3) * 32;
-            mma_bf16_ss(tmem + T_S, smem_desc_sw128(sbase + L::K + ka, 16, 1024),
-                        smem_desc_sw128(stage + L::Q_OFF + qa, 16, 1024), id_s, kk > 0);
+            const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
+            const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tmem + T_S, dk_kmaj + ka, dq_k + qa, id_s, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = (kk >> 2) * kKChunk + (kk & 3) * 32;
-            const uint32_t qa = (kk >> 2) * kQChunk + (kk & 3) * 32;
-            mma_bf16_ss(tmem + T_DP, smem_desc_sw128(sbase + L::V + ka, 16, 1024),
-                        smem_desc_sw128(stage + L::DO_OFF + qa, 16, 1024), id_s, kk > 0);
+            const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
+            const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tmem + T_DP, dv_kmaj + ka, ddo_k + qa, id_s, kk > 0);
           }
           mma_commit(ctl.bar(B_S_FULL));
         }
         if (j >= 1) {
-          const int m = j - 1, st = m & 1, pb = m & 1;
+          const int m = j - 1, st = m % kStages, pb = m & 1;
           const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
-          const uint32_t pt = sbase + L::PS + pb * L::PS_BYTES;  // P^T
-          const uint32_t dst = pt + kKChunk;                    // dS^T
-          if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
+          if (!(ok = ctl.wait(B_P_FULL, m & 1))) break;
           if (!(ok = ctl.wait(B_DQ_FREE + pb, ((m >> 1) & 1) ^ 1))) break;
           tc_fence_after();
+          const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
+          const uint64_t dq_mn = smem_desc_sw128(stage + L::Q_OFF, kQChunk, 1024);
           // dV += P^T dO ; dK += dS^T Q   (K = 64 query rows)
 #pragma unroll
-          for (int kk = 0; kk < kBQ / 16; ++kk) {
-            mma_bf16_ss(tmem + T_DK + D, smem_desc_sw128(pt + kk * 32, 16, 1024),
-                        smem_desc_sw128(stage + L::DO_OFF + kk * 2048, kQChunk, 1024), id_kv, (m > 0 || kk > 0));
-          }
+          for (int kk = 0; kk < kBQ / 16; ++kk)
+            mma_bf16_ss(tmem + T_DK + D, dpt + ((kk * 32) >> 4), ddo_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
 #pragma unroll
-          for (int kk = 0; kk < kBQ / 16; ++kk) {
-            mma_bf16_ss(tmem + T_DK, smem_desc_sw128(dst + kk * 32, 16, 1024),
-                        smem_desc_sw128(stage + L::Q_OFF + kk * 2048, kQChunk, 1024), id_kv, (m > 0 || kk > 0));
-          }
+          for (int kk = 0; kk < kBQ / 16; ++kk)
+            mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
           // dQ^T = K^T dS^T   (K = 128 keys)
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            mma_bf16_ss(tmem + T_DQ + 64 * pb, smem_desc_sw128(sbase + L::K + kk * 2048, kKChunk, 1024),
-                        smem_desc_sw128(dst + kk * 2048, kQChunk, 1024), id_q, kk > 0);
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss(tmem + T_DQ + 64 * pb, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
           mma_commit(ctl.bar(B_DQ_FULL + pb));
-          mma_commit(ctl.bar(B_P_FREE + pb));
+          mma_commit(ctl.bar(B_P_FREE));
           mma_commit(ctl.bar(B_Q_EMPTY + st));
         }
       }
@@ -281,37 +307,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = s.scale * kLog2e;
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
-      const int st = j & 1, pb = j & 1;
+      const int st = j % kStages;
       const int qt = qb + j * tpb;
       const float *stat = reinterpret_cast<const float *>(smem + L::STAGE + st * L::STAGE_BYTES + L::STAT_OFF);
-      if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j >> 1) & 1))) break;
+      if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j / kStages) & 1))) break;
       if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
-      if (!(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;
       tc_fence_after();
-      const uint32_t prow = sbase + L::PS + pb * L::PS_BYTES + r * 128;
+      const uint32_t prow = sbase + L::PS + r * 128;
       const bool nomask = qt + tpb <= qe && qt >= k1 - 1;
+      const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
+      const int ql = qe - qt;   // tokens of this block inside the query run
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // 32 query columns at a time
         uint32_t us[32], ud[32];
-        tmem_ld32(tmem + lane_base + T_S + 32 * h, us);
-        tmem_ld32(tmem + lane_base + T_DP + 32 * h, ud);
+        tmem_ld32x2(tmem + lane_base + T_S + 32 * h, tmem + lane_base + T_DP + 32 * h, us, ud);
         if (h == 1) {
           tc_fence_before();
           mbar_arrive(ctl.bar(B_S_FREE));
         }
+        // this half's LSE (log2) and Delta, as float4 shared loads
+        float l2[32], dl[32];
+        const float4 *st4 = reinterpret_cast<const float4 *>(stat);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 a = st4[8 * h + q4], b = st4[16 + 8 * h + q4];
+          l2[4 * q4] = a.x, l2[4 * q4 + 1] = a.y, l2[4 * q4 + 2] = a.z, l2[4 * q4 + 3] = a.w;
+          dl[4 * q4] = b.x, dl[4 * q4 + 1] = b.y, dl[4 * q4 + 2] = b.z, dl[4 * q4 + 3] = b.w;
+        }
+        // phases: exponents (masked to -inf), all exp2 back to back, products
         float pv[32], dsv[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c = 32 * h + i;
           bool vis = kvalid;
-          if (!nomask) {
-            const int tok = qt + c / G;
-            vis = vis && tok < qe && key <= tok;
-          }
-          const float p = vis ? ex2(fmaf(__uint_as_float(us[i]), sl2, -stat[c])) : 0.f;
-          pv[i] = p;
-          dsv[i] = p * (__uint_as_float(ud[i]) - stat[kBQ + c]);
+          if (!nomask) vis = vis && c / G < ql && kq <= c / G;
+          pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, -l2[i]) : -INFINITY;
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dsv[i] = pv[i] * (__uint_as_float(ud[i]) - dl[i]);
+        if (h == 0 && !(ok = ctl.wait_warp(B_P_FREE, (j & 1) ^ 1))) break;  // block j-1's MMAs are done
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
           const int u8 = 4 * h + u4;
@@ -324,8 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        pack_bf16(y[6], y[7]));
         }
       }
+      if (!ok) break;
       fence_proxy_async_smem();
-      mbar_arrive(ctl.bar(B_P_FULL + pb));
+      mbar_arrive(ctl.bar(B_P_FULL));
     }
     if (ok && ctl.wait_warp(B_FINAL, 0)) {
       tc_fence_after();
@@ -362,19 +399,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ctl.wait_warp(B_DQ_FULL + pb, (j >> 1) & 1)) break;
       tc_fence_after();
       uint32_t u0[32], u1[32];
-      tmem_ld32(tmem + lane_base + T_DQ + 64 * pb, u0);
-      tmem_ld32(tmem + lane_base + T_DQ + 64 * pb + 32, u1);
+      tmem_ld32x2(tmem + lane_base + T_DQ + 64 * pb, tmem + lane_base + T_DQ + 64 * pb + 32, u0, u1);
       tc_fence_before();
       mbar_arrive(ctl.bar(B_DQ_FREE + pb));
       if (d < D) {
         // query row c is token qt + c / G, head g * G + c % G
         float *base = dqacc + (size_t(qt) * Hq + g * G) * D + d;
+        const size_t tstride = size_t(Hq) * D;
+        if (qt + tpb <= qe) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (qt + c / G < qe) atomicAdd(base + size_t((c / G) * Hq + c % G) * D, __uint_as_float(u0[c]));
+          for (int c = 0; c < 32; ++c) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u0[c]));
 #pragma unroll
-        for (int c = 32; c < 64; ++c)
-          if (qt + c / G < qe) atomicAdd(base + size_t((c / G) * Hq + c % G) * D, __uint_as_float(u1[c - 32]));
+          for (int c = 32; c < 64; ++c)
+            atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u1[c - 32]));
+        } else {
+          const int ql = qe - qt;
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c / G < ql) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u0[c]));
+#pragma unroll
+          for (int c = 32; c < 64; ++c)
+            if (c / G < ql) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u1[c - 32]));
+        }
       }
     }
   }
@@ -434,7 +480,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
   }
 }
 
-template <int D>
+template <int D, int G>
 int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
            int32_t *d_status, cudaStream_t st) {
@@ -448,12 +494,12 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
 
   CUtensorMap tq, tdo, tk, tv;
-  int rc = encode_bf16_3d(&tq, q, D, s.Hq, s.T, 64, s.G, kBQ / s.G);
-  if (!rc) rc = encode_bf16_3d(&tdo, d_o, D, s.Hq, s.T, 64, s.G, kBQ / s.G);
+  int rc = encode_bf16_3d(&tq, q, D, s.Hq, s.T, 64, G, kBQ / G);
+  if (!rc) rc = encode_bf16_3d(&tdo, d_o, D, s.Hq, s.T, 64, G, kBQ / G);
   if (!rc) rc = encode_bf16_3d(&tk, k, D, s.Hkv, s.T, 64, 1, kBK);
   if (!rc) rc = encode_bf16_3d(&tv, v, D, s.Hkv, s.T, 64, 1, kBK);
   if (rc) return rc;
-  auto kern = bwd_tc_kernel<D>;
+  auto kern = bwd_tc_kernel<D, G>;
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
@@ -474,8 +520,13 @@ int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
            int32_t *d_status, void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return s.D == 64 ? launch<64>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, st)
-                   : launch<128>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, st);
+#define SPC_BWD_CASE(DD, GG)                                                                          \
+  if (s.D == DD && s.G == GG)                                                                         \
+    return launch<DD, GG>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, st);
+  SPC_BWD_CASE(64, 1) SPC_BWD_CASE(64, 2) SPC_BWD_CASE(64, 4) SPC_BWD_CASE(64, 8)
+  SPC_BWD_CASE(128, 1) SPC_BWD_CASE(128, 2) SPC_BWD_CASE(128, 4) SPC_BWD_CASE(128, 8)
+#undef SPC_BWD_CASE
+  return SP_ERR_UNSUPPORTED;
 }
 
 }  // namespace spc

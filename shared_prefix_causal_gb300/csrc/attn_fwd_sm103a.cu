@@ -101,10 +101,14 @@ struct Ctl {
     }
   }
   // Bounded wait used while draining after an abort (ignores the flag).
-  // Same, agreed by the whole warp (warp-collective tcgen05 loads follow).
+  // Same for a whole warp: one lane polls (32 lanes polling one barrier
+  // serialise on it and starve the warps that do the work), the others wait
+  // at __syncwarp, which also orders their later reads after lane 0's acquire.
   __device__ bool wait_warp(int i, uint32_t parity) const {
-    const bool r = wait(i, parity);
-    return __all_sync(0xffffffffu, r);
+    bool r = true;
+    if ((threadIdx.x & 31) == 0) r = wait(i, parity);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
   }
   __device__ void drain(int i, uint32_t parity) const {
     for (uint32_t it = 0; it < kSpinLimit; ++it)
@@ -118,8 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, PlanDev plan, AttnShape s,
                   __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, int32_t *d_status) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, derived by pointer arithmetic so that accesses
+  // through it stay shared-memory (not generic) accesses
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -207,6 +213,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
       const uint32_t tO = tmem + 256;
+      // operand descriptors, built once; a K step only moves the start address
+      const uint64_t dq0 = smem_desc_sw128(sbase + L::Q, 16, 1024);
+      const uint64_t dk_s0 = smem_desc_sw128(sbase + L::K, 16, 1024);
+      const uint64_t dk_s1 = smem_desc_sw128(sbase + L::K + L::KV, 16, 1024);
+      const uint64_t dp0 = smem_desc_sw128(sbase + L::P, 16, 1024);
+      const uint64_t dv_s0 = smem_desc_sw128(sbase + L::V, kChunk, 1024);
+      const uint64_t dv_s1 = smem_desc_sw128(sbase + L::V + L::KV, kChunk, 1024);
       if (ctl.wait(B_Q_FULL, 0)) {
         tc_fence_after();
         for (int n = 0; n <= nblocks; ++n) {
@@ -216,12 +229,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ctl.wait(B_K_FULL + st, ph)) break;
             if (!ctl.wait(B_S_FREE + st, ph ^ 1)) break;
             tc_fence_after();
-            const uint32_t kbase = sbase + L::K + st * L::KV;
+            const uint64_t dk = st ? dk_s1 : dk_s0;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * kChunk + (kk & 3) * 32;
-              mma_bf16_ss(tmem + st * 128, smem_desc_sw128(sbase + L::Q + off, 16, 1024),
-                          smem_desc_sw128(kbase + off, 16, 1024), idesc_s, kk > 0);
+              const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(tmem + st * 128, dq0 + off, dk + off, idesc_s, kk > 0);
             }
             mma_commit(ctl.bar(B_S_FULL + st));
             mma_commit(ctl.bar(B_K_EMPTY + st));
@@ -232,12 +244,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ctl.wait(B_P_FULL, m & 1)) break;
             if (!ctl.wait(B_V_FULL + st, ph)) break;
             tc_fence_after();
-            const uint32_t vbase = sbase + L::V + st * L::KV;
+            const uint64_t dv = st ? dv_s1 : dv_s0;
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint32_t poff = (kk >> 2) * kChunk + (kk & 3) * 32;
-              mma_bf16_ss(tO, smem_desc_sw128(sbase + L::P + poff, 16, 1024),
-                          smem_desc_sw128(vbase + kk * 2048, kChunk, 1024), idesc_o, (m > 0 || kk > 0));
+              const uint32_t poff = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+              mma_bf16_ss(tO, dp0 + poff, dv + ((kk * 2048) >> 4), idesc_o, (m > 0 || kk > 0));
             }
             mma_commit(ctl.bar(B_V_EMPTY + st));
             mma_commit(ctl.bar(B_PV_DONE));
@@ -268,56 +279,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float sv[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_base + sb * 128 + 32 * c, u);
+        for (int c = 0; c < kBN / 64; ++c) {
+          uint32_t u0[32], u1[32];
+          tmem_ld32x2(tmem + lane_base + sb * 128 + 64 * c, tmem + lane_base + sb * 128 + 64 * c + 32, u0, u1);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sv[32 * c + j] = __uint_as_float(u[j]);
+          for (int j = 0; j < 32; ++j) {
+            sv[64 * c + j] = __uint_as_float(u0[j]);
+            sv[64 * c + 32 + j] = __uint_as_float(u1[j]);
+          }
         }
         tc_fence_before();
         mbar_arrive(ctl.bar(B_S_FREE + sb));
 
-        float mb = -INFINITY;
+        // scale (and mask) in the log2 domain; row max by a tree of 8 partials
+        float mx[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
         if (kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0)) {
 #pragma unroll
           for (int j = 0; j < kBN; ++j) {
             sv[j] *= sl2;
-            mb = fmaxf(mb, sv[j]);
+            mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
           }
         } else {
           const int lim = causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb;
 #pragma unroll
           for (int j = 0; j < kBN; ++j) {
             sv[j] = j < lim ? sv[j] * sl2 : -INFINITY;
-            mb = fmaxf(mb, sv[j]);
+            mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
           }
         }
+        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         const float m_new = (mb > m_run + kRescaleThreshold) ? mb : m_run;
         const float mref = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = ex2(m_run - mref);
-        float rs = 0.f;
+        // subtract, then all exponentials back to back, then a tree sum
 #pragma unroll
-        for (int j = 0; j < kBN; ++j) {
-          sv[j] = ex2(sv[j] - mref);
-          rs += sv[j];
-        }
+        for (int j = 0; j < kBN; ++j) sv[j] -= mref;
+#pragma unroll
+        for (int j = 0; j < kBN; ++j) sv[j] = ex2(sv[j]);
+        float sm[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) sm[t] = 0.f;
+#pragma unroll
+        for (int j = 0; j < kBN; ++j) sm[j & 7] += sv[j];
+        const float rs = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
         l_run = l_run * alpha + rs;
 
         if (n >= 1) {
           if (!(ok = ctl.wait_warp(B_PV_DONE, (n - 1) & 1))) break;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t u[32];
-              const uint32_t ta = tmem + lane_base + 256 + 32 * c;
-              tmem_ld32(ta, u);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) u[j] = __float_as_uint(__uint_as_float(u[j]) * alpha);
-              tmem_st32(ta, u);
-            }
-            tmem_st_wait();
-          }
         }
         // P row -> shared memory, bf16, K-major with the 128-byte swizzle
 #pragma unroll
@@ -327,6 +339,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float *x = sv + 64 * c + 8 * j;
             st_shared_v4(prow + c * kChunk + ((j ^ (r & 7)) << 4), pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
                          pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+          }
+        }
+        if (n >= 1) {
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const uint32_t ta = tmem + lane_base + 256;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {  // 64 columns at a time
+              uint32_t u0[32], u1[32];
+              tmem_ld32x2(ta + 64 * c, ta + 64 * c + 32, u0, u1);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                u0[j] = __float_as_uint(__uint_as_float(u0[j]) * alpha);
+                u1[j] = __float_as_uint(__uint_as_float(u1[j]) * alpha);
+              }
+              tmem_st32(ta + 64 * c, u0);
+              tmem_st32(ta + 64 * c + 32, u1);
+            }
+            tmem_st_wait();
           }
         }
         fence_proxy_async_smem();
@@ -341,18 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool store = r < rows_valid;
       __nv_bfloat16 *orow = o + (size_t(tok) * s.Hq + head) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem + lane_base + 256 + 32 * c, u);
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t u0[32], u1[32];
+        tmem_ld32x2(tmem + lane_base + 256 + 64 * c, tmem + lane_base + 256 + 64 * c + 32, u0, u1);
         if (store) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
+          for (int j = 0; j < 64; j += 8) {
+            const uint32_t *u = j < 32 ? u0 + j : u1 + (j - 32);
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(u[j]) * inv, __uint_as_float(u[j + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(u[j + 2]) * inv, __uint_as_float(u[j + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(u[j + 4]) * inv, __uint_as_float(u[j + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(u[j + 6]) * inv, __uint_as_float(u[j + 7]) * inv);
-            *reinterpret_cast<uint4 *>(orow + 32 * c + j) = w;
+            w.x = pack_bf16(__uint_as_float(u[0]) * inv, __uint_as_float(u[1]) * inv);
+            w.y = pack_bf16(__uint_as_float(u[2]) * inv, __uint_as_float(u[3]) * inv);
+            w.z = pack_bf16(__uint_as_float(u[4]) * inv, __uint_as_float(u[5]) * inv);
+            w.w = pack_bf16(__uint_as_float(u[6]) * inv, __uint_as_float(u[7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + 64 * c + j) = w;
           }
         }
       }
