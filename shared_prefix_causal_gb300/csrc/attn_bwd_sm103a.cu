@@ -49,16 +49,16 @@ constexpr int kQChunk = 64 * 128;   // 64 rows x 128 bytes
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr int kStages = 3;  // Q/dO ring depth
+constexpr int kStages = 2;  // Q/dO ring depth
 
 enum : int {
   B_KV_FULL = 0,
-  B_Q_FULL = 1,    // +stage (3)
-  B_Q_EMPTY = 4,   // +stage
-  B_S_FULL = 7,
-  B_S_FREE = 8,
-  B_P_FULL = 9,
-  B_P_FREE = 10,
+  B_Q_FULL = 1,    // +stage (2)
+  B_Q_EMPTY = 3,   // +stage
+  B_S_FULL = 5,
+  B_S_FREE = 6,
+  B_P_FULL = 7,    // +buffer (2)
+  B_P_FREE = 9,    // +buffer
   B_DQ_FULL = 11,  // +buffer (2)
   B_DQ_FREE = 13,  // +buffer
   B_FINAL = 15,
@@ -77,9 +77,9 @@ struct Layout {
   static constexpr int DO_OFF = kDChunks * kQChunk;
   static constexpr int STAT_OFF = 2 * kDChunks * kQChunk;  // lse2[64], delta[64]
   static constexpr int STAGE_BYTES = STAT_OFF + 1024;     // keep 1024-byte alignment
-  static constexpr int PS = STAGE + kStages * STAGE_BYTES;  // {P^T, dS^T}
+  static constexpr int PS = STAGE + kStages * STAGE_BYTES;  // two buffers of {P^T, dS^T}
   static constexpr int PS_BYTES = 2 * kKChunk;
-  static constexpr int BAR = PS + PS_BYTES;
+  static constexpr int BAR = PS + 2 * PS_BYTES;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
   static constexpr int BYTES = ABORT + 4 + 1024;
@@ -138,8 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int g = blockIdx.x / plan.n_bwd;
-  const int *blk = plan.bwd + 5 * (blockIdx.x % plan.n_bwd);
+  // items in plan order (longest query run first), the KV heads of an item
+  // adjacent, so the longest runs of every head start in the first wave
+  const int g = blockIdx.x % s.Hkv;
+  const int *blk = plan.bwd + 5 * (blockIdx.x / s.Hkv);
   const int k0 = blk[1], k1 = blk[2], qb = blk[3], qe = blk[4];
   const int T = s.T, Hq = s.Hq;
   if (!(0 <= k0 && k0 < k1 && k1 - k0 <= kBK && qb == k0 && k1 <= qe && qe <= T)) {
@@ -148,12 +150,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   constexpr int tpb = kBQ / G;  // query tokens per block
   const int nq = (qe - qb + tpb - 1) / tpb;
+  // The run is walked from its end back to the diagonal block: CTAs whose runs
+  // end at the same subtree end then read the same Q/dO rows and add into the
+  // same dQ rows at about the same time, while those rows are in L2.
+  auto q_of = [&](int jj) { return qb + (nq - 1 - jj) * tpb; };
 
   Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_S_FREE || i == B_P_FULL || i == B_DQ_FREE || i == B_DQ_FREE + 1) cnt = 128;
+      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1 || i == B_DQ_FREE || i == B_DQ_FREE + 1) cnt = 128;
       mbar_init(ctl.bar(i), cnt);
     }
     *ctl.abort = 0;
@@ -192,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ahead so their latency hides behind the ring wait.
     float nl[2], nd[2];
     auto load_stats = [&](int jj) {
-      const int qt = qb + jj * tpb;
+      const int qt = q_of(jj);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = lane + 32 * h;
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (; j < nq; ++j) {
       const int st = j % kStages;
       if (!ctl.wait_warp(B_Q_EMPTY + st, ((j / kStages) & 1) ^ 1)) break;
-      const int qt = qb + j * tpb;
+      const int qt = q_of(j);
       const uint32_t stage = L::STAGE + st * L::STAGE_BYTES;
       if (lane == 0) {
         // byte count first, copies next, the one arrival after the stats below
@@ -243,9 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk_kmaj = smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dv_kmaj = smem_desc_sw128(sbase + L::V, 16, 1024);
       const uint64_t dk_mn = smem_desc_sw128(sbase + L::K, kKChunk, 1024);
-      const uint64_t dpt = smem_desc_sw128(sbase + L::PS, 16, 1024);            // P^T, K-major
-      const uint64_t dst_kmaj = smem_desc_sw128(sbase + L::PS + kKChunk, 16, 1024);  // dS^T as A
-      const uint64_t dst_mn = smem_desc_sw128(sbase + L::PS + kKChunk, kQChunk, 1024);  // dS^T as B
+      // per P/dS buffer b: P^T (K-major A), dS^T as A (K-major) and as B (MN-major)
+      const uint64_t dpt0 = smem_desc_sw128(sbase + L::PS, 16, 1024);
+      const uint64_t dst_kmaj0 = smem_desc_sw128(sbase + L::PS + kKChunk, 16, 1024);
+      const uint64_t dst_mn0 = smem_desc_sw128(sbase + L::PS + kKChunk, kQChunk, 1024);
+      constexpr uint32_t kPsStep = uint32_t(L::PS_BYTES) >> 4;  // descriptor units between buffers
       bool ok = ctl.wait(B_KV_FULL, 0);
       tc_fence_after();
       for (int j = 0; ok && j <= nq; ++j) {
@@ -274,10 +282,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= 1) {
           const int m = j - 1, st = m % kStages, pb = m & 1;
           const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
-          if (!(ok = ctl.wait(B_P_FULL, m & 1))) break;
+          if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
           if (!(ok = ctl.wait(B_DQ_FREE + pb, ((m >> 1) & 1) ^ 1))) break;
           tc_fence_after();
           const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
+          const uint32_t pso = pb * kPsStep;
+          const uint64_t dpt = dpt0 + pso, dst_kmaj = dst_kmaj0 + pso, dst_mn = dst_mn0 + pso;
           const uint64_t dq_mn = smem_desc_sw128(stage + L::Q_OFF, kQChunk, 1024);
           // dV += P^T dO ; dK += dS^T Q   (K = 64 query rows)
 #pragma unroll
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk)
             mma_bf16_ss(tmem + T_DQ + 64 * pb, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
           mma_commit(ctl.bar(B_DQ_FULL + pb));
-          mma_commit(ctl.bar(B_P_FREE));
+          mma_commit(ctl.bar(B_P_FREE + pb));
           mma_commit(ctl.bar(B_Q_EMPTY + st));
         }
       }
@@ -308,12 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
       const int st = j % kStages;
-      const int qt = qb + j * tpb;
+      const int qt = q_of(j);
       const float *stat = reinterpret_cast<const float *>(smem + L::STAGE + st * L::STAGE_BYTES + L::STAT_OFF);
       if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j / kStages) & 1))) break;
       if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
       tc_fence_after();
-      const uint32_t prow = sbase + L::PS + r * 128;
+      const int pb = j & 1;
+      const uint32_t prow = sbase + L::PS + pb * L::PS_BYTES + r * 128;
       const bool nomask = qt + tpb <= qe && qt >= k1 - 1;
       const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
       const int ql = qe - qt;   // tokens of this block inside the query run
@@ -336,18 +347,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // phases: exponents (masked to -inf), all exp2 back to back, products
         float pv[32], dsv[32];
+        if (nomask && kvalid) {  // two loops: a per-column test inside one loop is far slower
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = 32 * h + i;
-          bool vis = kvalid;
-          if (!nomask) vis = vis && c / G < ql && kq <= c / G;
-          pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, -l2[i]) : -INFINITY;
+          for (int i = 0; i < 32; ++i) pv[i] = fmaf(__uint_as_float(us[i]), sl2, -l2[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 32 * h + i;
+            const bool vis = kvalid && c / G < ql && kq <= c / G;
+            pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, -l2[i]) : -INFINITY;
+          }
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
 #pragma unroll
         for (int i = 0; i < 32; ++i) dsv[i] = pv[i] * (__uint_as_float(ud[i]) - dl[i]);
-        if (h == 0 && !(ok = ctl.wait_warp(B_P_FREE, (j & 1) ^ 1))) break;  // block j-1's MMAs are done
+        if (h == 0 && !(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;  // block j-2's MMAs done
 #pragma unroll
         for (int u4 = 0; u4 < 4; ++u4) {
           const int u8 = 4 * h + u4;
@@ -362,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       fence_proxy_async_smem();
-      mbar_arrive(ctl.bar(B_P_FULL));
+      mbar_arrive(ctl.bar(B_P_FULL + pb));
     }
     if (ok && ctl.wait_warp(B_FINAL, 0)) {
       tc_fence_after();
@@ -395,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
     for (int j = 0; j < nq; ++j) {
       const int pb = j & 1;
-      const int qt = qb + j * tpb;
+      const int qt = q_of(j);
       if (!ctl.wait_warp(B_DQ_FULL + pb, (j >> 1) & 1)) break;
       tc_fence_after();
       uint32_t u0[32], u1[32];
