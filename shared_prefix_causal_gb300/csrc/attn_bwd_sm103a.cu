@@ -49,18 +49,18 @@ constexpr int kQChunk = 64 * 128;   // 64 rows x 128 bytes
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr int kStages = 2;  // Q/dO ring depth
+constexpr int kStages = 3;  // Q/dO ring depth
 
 enum : int {
   B_KV_FULL = 0,
-  B_Q_FULL = 1,    // +stage (2)
-  B_Q_EMPTY = 3,   // +stage
-  B_S_FULL = 5,
-  B_S_FREE = 6,
-  B_P_FULL = 7,    // +buffer (2)
-  B_P_FREE = 9,    // +buffer
-  B_DQ_FULL = 11,  // +buffer (2)
-  B_DQ_FREE = 13,  // +buffer
+  B_Q_FULL = 1,    // +stage (3)
+  B_Q_EMPTY = 4,   // +stage
+  B_S_FULL = 7,
+  B_S_FREE = 8,
+  B_P_FULL = 9,    // +buffer (2)
+  B_P_FREE = 11,   // +buffer
+  B_DQ_FULL = 13,
+  B_DQ_FREE = 14,
   B_FINAL = 15,
   B_COUNT = 16
 };
@@ -77,8 +77,8 @@ struct Layout {
   static constexpr int DO_OFF = kDChunks * kQChunk;
   static constexpr int STAT_OFF = 2 * kDChunks * kQChunk;  // lse2[64], delta[64]
   static constexpr int STAGE_BYTES = STAT_OFF + 1024;     // keep 1024-byte alignment
-  static constexpr int PS = STAGE + kStages * STAGE_BYTES;  // two buffers of {P^T, dS^T}
-  static constexpr int PS_BYTES = 2 * kKChunk;
+  static constexpr int PS = STAGE + kStages * STAGE_BYTES;  // two dS^T buffers
+  static constexpr int PS_BYTES = kKChunk;
   static constexpr int BAR = PS + 2 * PS_BYTES;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
@@ -87,8 +87,9 @@ struct Layout {
   static constexpr uint32_t QTILE_BYTES = kDChunks * kQChunk;  // one of Q / dO for a block
 };
 
-// TMEM columns
-constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_DK = 256;
+// TMEM columns: S^T, dP^T (fp32, 64 each), dQ^T (fp32, 64), two P^T buffers
+// (bf16 pairs, 32 each), dK and dV (fp32, D each; 256 + 2D <= 512)
+constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_P = 192, T_DK = 256;
 
 struct Ctl {
   uint32_t bar0;
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1 || i == B_DQ_FREE || i == B_DQ_FREE + 1) cnt = 128;
+      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1 || i == B_DQ_FREE) cnt = 128;
       mbar_init(ctl.bar(i), cnt);
     }
     *ctl.abort = 0;
@@ -249,10 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk_kmaj = smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dv_kmaj = smem_desc_sw128(sbase + L::V, 16, 1024);
       const uint64_t dk_mn = smem_desc_sw128(sbase + L::K, kKChunk, 1024);
-      // per P/dS buffer b: P^T (K-major A), dS^T as A (K-major) and as B (MN-major)
-      const uint64_t dpt0 = smem_desc_sw128(sbase + L::PS, 16, 1024);
-      const uint64_t dst_kmaj0 = smem_desc_sw128(sbase + L::PS + kKChunk, 16, 1024);
-      const uint64_t dst_mn0 = smem_desc_sw128(sbase + L::PS + kKChunk, kQChunk, 1024);
+      // per dS^T buffer b: dS^T as A (K-major) and as B (MN-major)
+      const uint64_t dst_kmaj0 = smem_desc_sw128(sbase + L::PS, 16, 1024);
+      const uint64_t dst_mn0 = smem_desc_sw128(sbase + L::PS, kQChunk, 1024);
       constexpr uint32_t kPsStep = uint32_t(L::PS_BYTES) >> 4;  // descriptor units between buffers
       bool ok = ctl.wait(B_KV_FULL, 0);
       tc_fence_after();
@@ -283,24 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = j - 1, st = m % kStages, pb = m & 1;
           const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
           if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
-          if (!(ok = ctl.wait(B_DQ_FREE + pb, ((m >> 1) & 1) ^ 1))) break;
+          if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
           tc_fence_after();
           const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
           const uint32_t pso = pb * kPsStep;
-          const uint64_t dpt = dpt0 + pso, dst_kmaj = dst_kmaj0 + pso, dst_mn = dst_mn0 + pso;
+          const uint64_t dst_kmaj = dst_kmaj0 + pso, dst_mn = dst_mn0 + pso;
           const uint64_t dq_mn = smem_desc_sw128(stage + L::Q_OFF, kQChunk, 1024);
-          // dV += P^T dO ; dK += dS^T Q   (K = 64 query rows)
+          // dV += P^T dO (P^T read from TMEM, 8 columns per K step); dK += dS^T Q  (K = 64 query rows)
 #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
-            mma_bf16_ss(tmem + T_DK + D, dpt + ((kk * 32) >> 4), ddo_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
+            mma_bf16_ts(tmem + T_DK + D, tmem + T_P + 32 * pb + 8 * kk, ddo_mn + ((kk * 2048) >> 4), id_kv,
+                        (m > 0 || kk > 0));
 #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
             mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
           // dQ^T = K^T dS^T   (K = 128 keys)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(tmem + T_DQ + 64 * pb, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
-          mma_commit(ctl.bar(B_DQ_FULL + pb));
+            mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
+          mma_commit(ctl.bar(B_DQ_FULL));
           mma_commit(ctl.bar(B_P_FREE + pb));
           mma_commit(ctl.bar(B_Q_EMPTY + st));
         }
@@ -363,20 +364,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) dsv[i] = pv[i] * (__uint_as_float(ud[i]) - dl[i]);
         if (h == 0 && !(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;  // block j-2's MMAs done
+        {  // P^T: 32 query columns as 16 bf16 pairs into this row's TMEM lane
+          uint32_t pk[16];
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+          tmem_st16(tmem + lane_base + T_P + 32 * pb + 16 * h, pk);
+        }
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {  // dS^T: K-major, 128-byte swizzle
           const int u8 = 4 * h + u4;
-          const float *x = pv + 8 * u4;
           const float *y = dsv + 8 * u4;
           const uint32_t off = (u8 ^ (r & 7)) << 4;
-          st_shared_v4(prow + off, pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]),
-                       pack_bf16(x[6], x[7]));
-          st_shared_v4(prow + kKChunk + off, pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+          st_shared_v4(prow + off, pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
                        pack_bf16(y[6], y[7]));
         }
       }
       if (!ok) break;
+      tmem_st_wait();
       fence_proxy_async_smem();
+      tc_fence_before();
       mbar_arrive(ctl.bar(B_P_FULL + pb));
     }
     if (ok && ctl.wait_warp(B_FINAL, 0)) {
@@ -409,14 +415,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int d = 32 * (warp - 4) + lane;  // TMEM lane = head-dim index
     const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
     for (int j = 0; j < nq; ++j) {
-      const int pb = j & 1;
       const int qt = q_of(j);
-      if (!ctl.wait_warp(B_DQ_FULL + pb, (j >> 1) & 1)) break;
+      if (!ctl.wait_warp(B_DQ_FULL, j & 1)) break;
       tc_fence_after();
       uint32_t u0[32], u1[32];
-      tmem_ld32x2(tmem + lane_base + T_DQ + 64 * pb, tmem + lane_base + T_DQ + 64 * pb + 32, u0, u1);
+      tmem_ld32x2(tmem + lane_base + T_DQ, tmem + lane_base + T_DQ + 32, u0, u1);
       tc_fence_before();
-      mbar_arrive(ctl.bar(B_DQ_FREE + pb));
+      mbar_arrive(ctl.bar(B_DQ_FREE));
       if (d < D) {
         // query row c is token qt + c / G, head g * G + c % G
         float *base = dqacc + (size_t(qt) * Hq + g * G) * D + d;
