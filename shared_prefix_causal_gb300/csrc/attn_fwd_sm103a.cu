@@ -7,23 +7,30 @@
 // solution you'd like": each query run attends only to its ancestor path).
 // Outputs O (bf16) and the natural-log LSE (fp32) kept for the backward.
 //
-// One CTA per (query tile, KV head).  A tile is 128 rows = (128 / G) tokens x
-// the G query heads sharing that KV head, so every K/V block read from L2 or
-// HBM feeds a full 128-row MMA even for short segments.  The CTA walks the
-// tile's plan ranges in 128-key blocks:
-//   warp 4  (one lane)  TMA producer: Q once, then K and V blocks into a
-//                       two-stage ring;
-//   warp 5  (one lane)  MMA issuer: S = Q K^T into one of two TMEM S buffers,
-//                       then O += P V into the TMEM O accumulator, software
-//                       pipelined so S of block n+1 runs while the softmax
-//                       of block n is computed;
-//   warps 0-3           softmax: thread r owns row r (TMEM lane r).  Masks
-//                       only where needed (range tail; causal only on blocks
-//                       that reach past the tile's first token), online
-//                       softmax in the exp2 domain with a lazily updated
-//                       reference max (O is rescaled only when the running max
-//                       grows by more than 2^8), P rounded to bf16 into
-//                       swizzled shared memory, epilogue O / l and LSE.
+// One CTA per (pair of query tiles, KV head).  A tile is 128 rows = (128 / G)
+// tokens x the G query heads sharing that KV head, so every K/V block read
+// from L2 or HBM feeds full 128-row MMAs even for short segments.  The two
+// tiles of a pair are neighbours in the plan's schedule (tile k of sibling
+// segments, or consecutive tiles of one segment): they share their ancestor
+// blocks, so the CTA streams the merged list of 128-key blocks once.
+//   warp 8  (one lane)  TMA producer: both Q tiles once, then K and V blocks
+//                       into a two-stage ring;
+//   warp 9  (one lane)  MMA issuer, interleaving the tiles so one tile's
+//                       softmax overlaps the other tile's MMAs:
+//                         PV_a(n), S_a(n+1), PV_b(n), S_b(n+1), ...
+//                       S = Q K^T goes to the tile's TMEM S columns; the
+//                       softmax overwrites them with P (bf16 pairs) and
+//                       O += P V reads P straight from TMEM;
+//   warps 0-3 / 4-7     softmax of tile a / tile b: thread r owns row r (TMEM
+//                       lane r).  Masks only where needed (range tail; causal
+//                       only on blocks that reach past the tile's first
+//                       token), exp2-domain online softmax with a lazily
+//                       updated reference max (O is rescaled in TMEM only when
+//                       the row max grows by more than 2^8), epilogue O / l.
+// TMEM: S_a, O_a, S_b, O_b (128 columns each for D = 128).  tcgen05 MMAs of
+// one thread execute in issue order, so S(n+1) never overwrites P(n) before
+// PV(n) has read it, and the commit that signals S(n+1) also covers PV(n):
+// the softmax always sees a complete O when it rescales.
 // Every mbarrier wait is bounded; on expiry the CTA records SP_DEV_TIMEOUT,
 // stops issuing work, drains what it issued, frees TMEM and returns.
 #include <cuda.h>
@@ -41,11 +48,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kBM = 128;          // query rows per tile
-constexpr int kBN = 128;          // keys per block
-constexpr int kStages = 2;        // K/V ring depth
-constexpr int kThreads = 192;     // 4 softmax warps + producer + MMA
-constexpr int kChunk = 128 * 128; // bytes of one 128-row x 128-byte swizzled chunk
+constexpr int kBM = 128;           // query rows per tile
+constexpr int kBN = 128;           // keys per block
+constexpr int kStages = 2;         // K/V ring depth
+constexpr int kThreads = 320;      // 8 softmax warps + producer + MMA
+constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk
 constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -53,14 +60,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 enum : int {
   B_Q_FULL = 0,
-  B_K_FULL = 1,   // +stage
-  B_K_EMPTY = 3,  // +stage
-  B_V_FULL = 5,
-  B_V_EMPTY = 7,
-  B_S_FULL = 9,   // +buffer
-  B_S_FREE = 11,  // +buffer
-  B_P_FULL = 13,
-  B_PV_DONE = 14,
+  B_K_FULL = 1,    // +stage
+  B_K_EMPTY = 3,   // +stage
+  B_V_FULL = 5,    // +stage
+  B_V_EMPTY = 7,   // +stage
+  B_S_FULL = 9,    // +tile
+  B_P_FULL = 11,   // +tile (128 arrivals)
+  B_O_DONE = 13,   // +tile (one completion per P V of that tile)
   B_MMA_DONE = 15,
   B_COUNT = 16
 };
@@ -68,17 +74,17 @@ enum : int {
 template <int D>
 struct Layout {
   static constexpr int kDChunks = D / 64;
-  static constexpr int Q = 0;
   static constexpr int KV = kDChunks * kChunk;  // bytes of 128 rows x D
-  static constexpr int K = Q + KV;
+  static constexpr int Q = 0;                   // + tile * KV
+  static constexpr int K = 2 * KV;              // + stage * KV
   static constexpr int V = K + kStages * KV;
-  static constexpr int P = V + kStages * KV;
-  static constexpr int BAR = P + 2 * kChunk;
+  static constexpr int BAR = V + kStages * KV;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
   static constexpr int BYTES = ABORT + 4 + 1024;  // + alignment slack
   // at least ~116 KB so two CTAs never share an SM (each takes all 512 TMEM columns)
   static constexpr int ALLOC = BYTES > 120 * 1024 ? BYTES : 120 * 1024;
+  static constexpr uint32_t TILE_COLS = 128 + D;  // S then O, per tile
 };
 
 struct Ctl {
@@ -100,7 +106,6 @@ struct Ctl {
       }
     }
   }
-  // Bounded wait used while draining after an abort (ignores the flag).
   // Same for a whole warp: one lane polls (32 lanes polling one barrier
   // serialise on it and starve the warps that do the work), the others wait
   // at __syncwarp, which also orders their later reads after lane 0's acquire.
@@ -110,6 +115,7 @@ struct Ctl {
     __syncwarp();
     return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
   }
+  // Bounded wait used while draining after an abort (ignores the flag).
   __device__ void drain(int i, uint32_t parity) const {
     for (uint32_t it = 0; it < kSpinLimit; ++it)
       if (mbar_try_wait(bar(i), parity)) return;
@@ -129,19 +135,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int g = blockIdx.x / plan.n_tiles;
-  const int *tile = plan.tiles + 5 * (blockIdx.x % plan.n_tiles);
-  const int q0 = tile[1], q1 = tile[2], rb = tile[3], rc = tile[4];
+  const int g = blockIdx.x / plan.n_pairs;
+  const int *pr = plan.pairs + 4 * (blockIdx.x % plan.n_pairs);
+  const int ta = pr[0], tb = pr[1], bbeg = pr[2], nblk = pr[3];
   const int G = s.G, T = s.T;
-  const int *rng = plan.ranges + 2 * rb;
+  const int *pb = plan.pblk + 4 * bbeg;
+  const int *tla = plan.tiles + 5 * ta;
+  const int *tlb = tb >= 0 ? plan.tiles + 5 * tb : nullptr;
+  const int qa0 = tla[1], qa1 = tla[2];
+  const int qb0 = tlb ? tlb[1] : 0, qb1 = tlb ? tlb[2] : 0;
 
-  // Validate the work item (uniform over the CTA) and count its key blocks.
-  bool bad = !(0 <= q0 && q0 < q1 && q1 <= T && rc >= 1);
-  int nblocks = 0;
-  for (int i = 0; !bad && i < rc; ++i) {
-    const int a = rng[2 * i], b = rng[2 * i + 1];
-    if (!(0 <= a && a < b && b <= T)) bad = true;
-    nblocks += (b - a + kBN - 1) / kBN;
+  // Validate the work item (uniform over the CTA).
+  bool bad = !(0 <= ta && ta < plan.n_tiles && tb < plan.n_tiles && nblk >= 1 && 0 <= qa0 && qa0 < qa1 &&
+               qa1 <= T && (!tlb || (0 <= qb0 && qb0 < qb1 && qb1 <= T)));
+  for (int i = 0; !bad && i < nblk; ++i) {
+    const int kb = pb[4 * i], ea = pb[4 * i + 1], eb = pb[4 * i + 2];
+    if (!(0 <= kb && kb < T && ea <= T && eb <= T && (ea > kb || eb > kb) && (ea == 0 || ea > kb) &&
+          (eb == 0 || eb > kb) && (tlb || eb == 0)))
+      bad = true;
   }
   if (bad) {
     if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
@@ -150,14 +161,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status};
   if (threadIdx.x == 0) {
-    for (int i = 0; i < B_COUNT; ++i) {
-      const uint32_t cnt = (i == B_S_FREE || i == B_S_FREE + 1 || i == B_P_FULL) ? 128u : 1u;
-      mbar_init(ctl.bar(i), cnt);
-    }
+    for (int i = 0; i < B_COUNT; ++i) mbar_init(ctl.bar(i), (i == B_P_FULL || i == B_P_FULL + 1) ? 128u : 1u);
     *ctl.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(sbase + L::TSLOT, 512);
     tmem_relinquish();
   }
@@ -166,37 +174,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
       prefetch_tmap(&tm_v);
-      mbar_arrive_expect_tx(ctl.bar(B_Q_FULL), L::KV);
+      mbar_arrive_expect_tx(ctl.bar(B_Q_FULL), (tlb ? 2u : 1u) * L::KV);
 #pragma unroll
-      for (int c = 0; c < L::kDChunks; ++c)
-        tma_load_3d(sbase + L::Q + c * kChunk, &tm_q, ctl.bar(B_Q_FULL), c * 64, g * G, q0);
+      for (int c = 0; c < L::kDChunks; ++c) {
+        tma_load_3d(sbase + L::Q + c * kChunk, &tm_q, ctl.bar(B_Q_FULL), c * 64, g * G, qa0);
+        if (tlb) tma_load_3d(sbase + L::Q + L::KV + c * kChunk, &tm_q, ctl.bar(B_Q_FULL), c * 64, g * G, qb0);
+      }
       int n = 0;
-      bool ok = true;
-      for (int ri = 0; ok && ri < rc; ++ri) {
-        const int kv0 = rng[2 * ri], kv1 = rng[2 * ri + 1];
-        for (int kb = kv0; kb < kv1; kb += kBN, ++n) {
-          const int st = n & 1;
-          const uint32_t ph = (n >> 1) & 1;
-          if (!(ok = ctl.wait(B_K_EMPTY + st, ph ^ 1))) break;
-          mbar_arrive_expect_tx(ctl.bar(B_K_FULL + st), L::KV);
+      for (; n < nblk; ++n) {
+        const int st = n & 1, kb = pb[4 * n];
+        const uint32_t ph = (n >> 1) & 1;
+        if (!ctl.wait(B_K_EMPTY + st, ph ^ 1)) break;
+        mbar_arrive_expect_tx(ctl.bar(B_K_FULL + st), L::KV);
 #pragma unroll
-          for (int c = 0; c < L::kDChunks; ++c)
-            tma_load_3d(sbase + L::K + st * L::KV + c * kChunk, &tm_k, ctl.bar(B_K_FULL + st), c * 64, g, kb);
-          if (!(ok = ctl.wait(B_V_EMPTY + st, ph ^ 1))) {
-            ctl.drain(B_K_FULL + st, ph);
-            break;
-          }
-          mbar_arrive_expect_tx(ctl.bar(B_V_FULL + st), L::KV);
-#pragma unroll
-          for (int c = 0; c < L::kDChunks; ++c)
-            tma_load_3d(sbase + L::V + st * L::KV + c * kChunk, &tm_v, ctl.bar(B_V_FULL + st), c * 64, g, kb);
+        for (int c = 0; c < L::kDChunks; ++c)
+          tma_load_3d(sbase + L::K + st * L::KV + c * kChunk, &tm_k, ctl.bar(B_K_FULL + st), c * 64, g, kb);
+        if (!ctl.wait(B_V_EMPTY + st, ph ^ 1)) {
+          ctl.drain(B_K_FULL + st, ph);
+          break;
         }
+        mbar_arrive_expect_tx(ctl.bar(B_V_FULL + st), L::KV);
+#pragma unroll
+        for (int c = 0; c < L::kDChunks; ++c)
+          tma_load_3d(sbase + L::V + st * L::KV + c * kChunk, &tm_v, ctl.bar(B_V_FULL + st), c * 64, g, kb);
       }
       if (*ctl.abort) {
         // let the last fills of each stage land before the CTA exits
@@ -207,165 +213,176 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
-      const uint32_t tO = tmem + 256;
       // operand descriptors, built once; a K step only moves the start address
-      const uint64_t dq0 = smem_desc_sw128(sbase + L::Q, 16, 1024);
+      const uint64_t dq_a = smem_desc_sw128(sbase + L::Q, 16, 1024);
+      const uint64_t dq_b = smem_desc_sw128(sbase + L::Q + L::KV, 16, 1024);
       const uint64_t dk_s0 = smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dk_s1 = smem_desc_sw128(sbase + L::K + L::KV, 16, 1024);
-      const uint64_t dp0 = smem_desc_sw128(sbase + L::P, 16, 1024);
       const uint64_t dv_s0 = smem_desc_sw128(sbase + L::V, kChunk, 1024);
       const uint64_t dv_s1 = smem_desc_sw128(sbase + L::V + L::KV, kChunk, 1024);
-      if (ctl.wait(B_Q_FULL, 0)) {
-        tc_fence_after();
-        for (int n = 0; n <= nblocks; ++n) {
-          if (n < nblocks) {
-            const int st = n & 1;
-            const uint32_t ph = (n >> 1) & 1;
-            if (!ctl.wait(B_K_FULL + st, ph)) break;
-            if (!ctl.wait(B_S_FREE + st, ph ^ 1)) break;
-            tc_fence_after();
-            const uint64_t dk = st ? dk_s1 : dk_s0;
+      uint32_t pcount_a = 0, pcount_b = 0;  // P V issued per tile
+      // S_t(n) = Q_t K_n^T into tile t's S columns
+      auto issue_s = [&](int t, int n) {
+        const uint64_t dk = (n & 1) ? dk_s1 : dk_s0;
+        const uint64_t dq = t ? dq_b : dq_a;
+        const uint32_t tsc = tmem + t * L::TILE_COLS;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
-              mma_bf16_ss(tmem + st * 128, dq0 + off, dk + off, idesc_s, kk > 0);
-            }
-            mma_commit(ctl.bar(B_S_FULL + st));
-            mma_commit(ctl.bar(B_K_EMPTY + st));
-          }
-          if (n >= 1) {
-            const int m = n - 1, st = m & 1;
-            const uint32_t ph = (m >> 1) & 1;
-            if (!ctl.wait(B_P_FULL, m & 1)) break;
-            if (!ctl.wait(B_V_FULL + st, ph)) break;
-            tc_fence_after();
-            const uint64_t dv = st ? dv_s1 : dv_s0;
-#pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk) {
-              const uint32_t poff = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
-              mma_bf16_ss(tO, dp0 + poff, dv + ((kk * 2048) >> 4), idesc_o, (m > 0 || kk > 0));
-            }
-            mma_commit(ctl.bar(B_V_EMPTY + st));
-            mma_commit(ctl.bar(B_PV_DONE));
-          }
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tsc, dq + off, dk + off, idesc_s, kk > 0);
         }
+        mma_commit(ctl.bar(B_S_FULL + t));
+      };
+      // O_t += P_t(n) V_n with P read from tile t's S columns
+      auto issue_pv = [&](int t, int n, bool accumulate) {
+        const uint64_t dv = (n & 1) ? dv_s1 : dv_s0;
+        const uint32_t tsc = tmem + t * L::TILE_COLS;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(tsc + 128, tsc + 8 * kk, dv + ((kk * 2048) >> 4), idesc_o, (accumulate || kk > 0));
+        mma_commit(ctl.bar(B_O_DONE + t));
+      };
+      bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_K_FULL, 0);
+      if (ok) {
+        tc_fence_after();
+        if (pb[1]) issue_s(0, 0);
+        if (pb[2]) issue_s(1, 0);
+        mma_commit(ctl.bar(B_K_EMPTY));
+      }
+      for (int n = 0; ok && n < nblk; ++n) {
+        const int st = n & 1;
+        const bool last = n + 1 == nblk;
+        const bool ua = pb[4 * n + 1] != 0, ub = pb[4 * n + 2] != 0;
+        const bool ua1 = !last && pb[4 * (n + 1) + 1] != 0, ub1 = !last && pb[4 * (n + 1) + 2] != 0;
+        if (!(ok = ctl.wait(B_V_FULL + st, (n >> 1) & 1))) break;
+        if (ua) {
+          if (!(ok = ctl.wait(B_P_FULL, pcount_a & 1))) break;
+          tc_fence_after();
+          issue_pv(0, n, pcount_a > 0);
+          ++pcount_a;
+        }
+        // block n+1's K tile: needed from here on
+        if (!last && !(ok = ctl.wait(B_K_FULL + (st ^ 1), ((n + 1) >> 1) & 1))) break;
+        tc_fence_after();
+        if (ua1) issue_s(0, n + 1);
+        if (ub) {
+          if (!(ok = ctl.wait(B_P_FULL + 1, pcount_b & 1))) break;
+          tc_fence_after();
+          issue_pv(1, n, pcount_b > 0);
+          ++pcount_b;
+        }
+        if (ub1) issue_s(1, n + 1);
+        if (!last) mma_commit(ctl.bar(B_K_EMPTY + (st ^ 1)));
+        mma_commit(ctl.bar(B_V_EMPTY + st));
       }
       mma_commit(ctl.bar(B_MMA_DONE));
       ctl.drain(B_MMA_DONE, 0);
     }
   } else {
     // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;
-    const uint32_t lane_base = uint32_t(32 * warp) << 16;
+    const int t = warp >> 2;  // tile handled by this warpgroup
+    const int r = threadIdx.x & 127;
+    const bool active = t == 0 || tlb != nullptr;
+    const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
+    const uint32_t ts = tmem + t * L::TILE_COLS + lane_base;  // this row's S (then P) columns; O at +128
+    const int q0 = t ? qb0 : qa0, q1 = t ? qb1 : qa1;
     const int rows_valid = (q1 - q0) * G;
     const int tok = q0 + r / G;
     const int head = g * G + r % G;
     const float sl2 = s.scale * kLog2e;
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    int n = 0;
-    const uint32_t prow = sbase + L::P + r * 128;
-    for (int ri = 0; ok && ri < rc; ++ri) {
-      const int kv0 = rng[2 * ri], kv1 = rng[2 * ri + 1];
-      const bool causal = ri == rc - 1;
-      for (int kb = kv0; kb < kv1; kb += kBN, ++n) {
-        const int sb = n & 1;
-        if (!(ok = ctl.wait_warp(B_S_FULL + sb, (n >> 1) & 1))) break;
-        tc_fence_after();
-        float sv[kBN];
+    uint32_t used = 0;  // blocks this tile has processed
+    for (int n = 0; active && n < nblk; ++n) {
+      const int kb = pb[4 * n], kv1 = pb[4 * n + 1 + t];
+      if (kv1 == 0) continue;
+      const bool causal = (pb[4 * n + 3] >> t) & 1;
+      if (!(ok = ctl.wait_warp(B_S_FULL + t, used & 1))) break;
+      tc_fence_after();
+      float sv[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN / 64; ++c) {
+      for (int c = 0; c < kBN / 64; ++c) {
+        uint32_t u0[32], u1[32];
+        tmem_ld32x2(ts + 64 * c, ts + 64 * c + 32, u0, u1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          sv[64 * c + j] = __uint_as_float(u0[j]);
+          sv[64 * c + 32 + j] = __uint_as_float(u1[j]);
+        }
+      }
+      // row max of the raw scores (masked ones set to -inf) by a tree of 8
+      // partials; the scale is applied to the max (it is positive)
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+      const bool full = kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0);
+      if (full) {
+#pragma unroll
+        for (int j = 0; j < kBN; ++j) mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
+      } else {
+        const int lim = causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb;
+#pragma unroll
+        for (int j = 0; j < kBN; ++j) {
+          sv[j] = j < lim ? sv[j] : -INFINITY;
+          mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
+        }
+      }
+      const float mb = sl2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = (mb > m_run + kRescaleThreshold) ? mb : m_run;
+      const float mref = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2(m_run - mref);
+      // exponents with one FFMA each, then all exponentials back to back, then
+      // a tree sum and P as bf16 pairs over the first 64 S columns (read by
+      // the P V MMA)
+      const float nm = -mref;
+#pragma unroll
+      for (int j = 0; j < kBN; ++j) sv[j] = fmaf(sv[j], sl2, nm);
+#pragma unroll
+      for (int j = 0; j < kBN; ++j) sv[j] = ex2(sv[j]);
+      float sm[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sm[i] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kBN; ++j) sm[j & 7] += sv[j];
+      l_run = l_run * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
+      m_run = m_new;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(sv[32 * c + 2 * i], sv[32 * c + 2 * i + 1]);
+        tmem_st16(ts + 16 * c, pk);
+      }
+      // O already holds every earlier block (see the header note): rescale it
+      // in TMEM, 64 columns at a time, when any row of the warp needs it (P is
+      // stored first so its registers are free).
+      if (used > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t u0[32], u1[32];
-          tmem_ld32x2(tmem + lane_base + sb * 128 + 64 * c, tmem + lane_base + sb * 128 + 64 * c + 32, u0, u1);
+          const uint32_t ta_ = ts + 128 + 64 * c;
+          tmem_ld32x2(ta_, ta_ + 32, u0, u1);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            sv[64 * c + j] = __uint_as_float(u0[j]);
-            sv[64 * c + 32 + j] = __uint_as_float(u1[j]);
+            u0[j] = __float_as_uint(__uint_as_float(u0[j]) * alpha);
+            u1[j] = __float_as_uint(__uint_as_float(u1[j]) * alpha);
           }
+          tmem_st32(ta_, u0);
+          tmem_st32(ta_ + 32, u1);
         }
-        tc_fence_before();
-        mbar_arrive(ctl.bar(B_S_FREE + sb));
-
-        // scale (and mask) in the log2 domain; row max by a tree of 8 partials
-        float mx[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
-        if (kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0)) {
-#pragma unroll
-          for (int j = 0; j < kBN; ++j) {
-            sv[j] *= sl2;
-            mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
-          }
-        } else {
-          const int lim = causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb;
-#pragma unroll
-          for (int j = 0; j < kBN; ++j) {
-            sv[j] = j < lim ? sv[j] * sl2 : -INFINITY;
-            mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
-          }
-        }
-        const float mb = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float m_new = (mb > m_run + kRescaleThreshold) ? mb : m_run;
-        const float mref = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2(m_run - mref);
-        // subtract, then all exponentials back to back, then a tree sum
-#pragma unroll
-        for (int j = 0; j < kBN; ++j) sv[j] -= mref;
-#pragma unroll
-        for (int j = 0; j < kBN; ++j) sv[j] = ex2(sv[j]);
-        float sm[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) sm[t] = 0.f;
-#pragma unroll
-        for (int j = 0; j < kBN; ++j) sm[j & 7] += sv[j];
-        const float rs = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-        l_run = l_run * alpha + rs;
-
-        if (n >= 1) {
-          if (!(ok = ctl.wait_warp(B_PV_DONE, (n - 1) & 1))) break;
-          tc_fence_after();
-        }
-        // P row -> shared memory, bf16, K-major with the 128-byte swizzle
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float *x = sv + 64 * c + 8 * j;
-            st_shared_v4(prow + c * kChunk + ((j ^ (r & 7)) << 4), pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                         pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-          }
-        }
-        if (n >= 1) {
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            const uint32_t ta = tmem + lane_base + 256;
-#pragma unroll
-            for (int c = 0; c < D / 64; ++c) {  // 64 columns at a time
-              uint32_t u0[32], u1[32];
-              tmem_ld32x2(ta + 64 * c, ta + 64 * c + 32, u0, u1);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                u0[j] = __float_as_uint(__uint_as_float(u0[j]) * alpha);
-                u1[j] = __float_as_uint(__uint_as_float(u1[j]) * alpha);
-              }
-              tmem_st32(ta + 64 * c, u0);
-              tmem_st32(ta + 64 * c + 32, u1);
-            }
-            tmem_st_wait();
-          }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        mbar_arrive(ctl.bar(B_P_FULL));
-        m_run = m_new;
       }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(ctl.bar(B_P_FULL + t));
+      ++used;
     }
-    if (ok && ctl.wait_warp(B_PV_DONE, (nblocks - 1) & 1)) {
+    if (active && ok && used > 0 && ctl.wait_warp(B_O_DONE + t, (used - 1) & 1)) {
       tc_fence_after();
       const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
       const bool store = r < rows_valid;
@@ -373,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t u0[32], u1[32];
-        tmem_ld32x2(tmem + lane_base + 256 + 64 * c, tmem + lane_base + 256 + 64 * c + 32, u0, u1);
+        tmem_ld32x2(ts + 128 + 64 * c, ts + 128 + 64 * c + 32, u0, u1);
         if (store) {
 #pragma unroll
           for (int j = 0; j < 64; j += 8) {
@@ -393,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -403,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, void *o, float *lse,
            int32_t *d_status, cudaStream_t st) {
+  if (!p.pairs || p.n_pairs <= 0) return SP_ERR_NOT_UPLOADED;
   CUtensorMap tq, tk, tv;
   const int G = s.G;
   int rc = encode_bf16_3d(&tq, q, D, s.Hq, s.T, 64, G, kBM / G);
@@ -413,7 +431,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
-  const unsigned grid = unsigned(p.n_tiles) * unsigned(s.Hkv);
+  const unsigned grid = unsigned(p.n_pairs) * unsigned(s.Hkv);
   kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, p, s, static_cast<__nv_bfloat16 *>(o), lse, d_status);
   return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }

@@ -31,7 +31,8 @@ int check_tiling(const sp_plan &p, int32_t dtype, int32_t G) {
 }
 
 spc::PlanDev plan_dev(const sp_plan &p) {
-  return {p.d_tiles, p.d_ranges, p.d_bwd, p.n_tiles(), p.n_bwd(), p.tile_tokens, p.kv_block};
+  return {p.d_tiles, p.d_ranges, p.d_bwd, p.n_tiles(), p.n_bwd(), p.tile_tokens, p.kv_block,
+          p.d_pairs, p.d_pblk, p.n_pairs()};
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -81,16 +82,26 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   if (!p) return SP_ERR_INVALID_ARG;
   if (p->d_tiles) return SP_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  try {
+    spc::build_pairs(*p, 128);
+  } catch (...) {
+    return SP_ERR_INVALID_ARG;
+  }
   const size_t bt = p->tiles.size() * 4, br = p->ranges.size() * 4, bb = p->bwd.size() * 4;
-  const size_t total = align_up(bt) + align_up(br) + align_up(bb) + 256;
+  const size_t bp = p->pairs.size() * 4, bk = p->pblk.size() * 4;
+  const size_t total = align_up(bt) + align_up(br) + align_up(bb) + align_up(bp) + align_up(bk) + 256;
   char *base = nullptr;
   if (cudaMalloc(&base, total) != cudaSuccess) return SP_ERR_CUDA;
   int32_t *dt = reinterpret_cast<int32_t *>(base);
   int32_t *dr = reinterpret_cast<int32_t *>(base + align_up(bt));
   int32_t *db = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br));
+  int32_t *dp = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br) + align_up(bb));
+  int32_t *dk = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br) + align_up(bb) + align_up(bp));
   if ((bt && cudaMemcpyAsync(dt, p->tiles.data(), bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (br && cudaMemcpyAsync(dr, p->ranges.data(), br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (bb && cudaMemcpyAsync(db, p->bwd.data(), bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (bp && cudaMemcpyAsync(dp, p->pairs.data(), bp, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (bk && cudaMemcpyAsync(dk, p->pblk.data(), bk, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       cudaStreamSynchronize(st) != cudaSuccess) {
     cudaFree(base);
     return SP_ERR_CUDA;
@@ -98,6 +109,8 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   p->d_tiles = dt;
   p->d_ranges = dr;
   p->d_bwd = db;
+  p->d_pairs = dp;
+  p->d_pblk = dk;
   cudaGetDevice(&p->device);
   return SP_OK;
 }

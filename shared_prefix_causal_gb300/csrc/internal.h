@@ -14,12 +14,17 @@ struct sp_plan {
   std::vector<int32_t> tiles;   // [n][5]
   std::vector<int32_t> ranges;  // [m][2]
   std::vector<int32_t> bwd;     // [k][5]
+  // forward work items derived from the tiles (built at upload): pairs of
+  // consecutive tiles and, per pair, the merged list of 128-key blocks
+  std::vector<int32_t> pairs;   // [p][4] = {tile_a, tile_b or -1, blk_begin, blk_count}
+  std::vector<int32_t> pblk;    // [b][4] = {kb, end_a or 0, end_b or 0, causal bits}
   // device copies (owned), valid after sp_plan_upload
-  int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr;
+  int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr, *d_pairs = nullptr, *d_pblk = nullptr;
   int device = -1;
   int32_t n_tiles() const { return int32_t(tiles.size() / 5); }
   int32_t n_ranges() const { return int32_t(ranges.size() / 2); }
   int32_t n_bwd() const { return int32_t(bwd.size() / 5); }
+  int32_t n_pairs() const { return int32_t(pairs.size() / 4); }
 };
 
 namespace spc {
@@ -27,6 +32,8 @@ namespace spc {
 // Plan builder (plan.cpp).  Returns SP_OK or SP_ERR_INVALID_TREE/ARG.
 int build_plan(const sp_tree_desc &tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
                sp_plan &plan);
+// Forward pairs and merged block lists from the tiles (see sp_plan::pairs).
+void build_pairs(sp_plan &plan, int32_t block_keys);
 
 // Device-side view of a plan passed to kernels by value.
 struct PlanDev {
@@ -34,6 +41,9 @@ struct PlanDev {
   const int32_t *ranges;
   const int32_t *bwd;
   int32_t n_tiles, n_bwd, tile_tokens, kv_block;
+  const int32_t *pairs;
+  const int32_t *pblk;
+  int32_t n_pairs;
 };
 
 struct AttnShape {

@@ -159,4 +159,54 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
   return SP_OK;
 }
 
+// Pairs tiles (2i, 2i+1) in schedule order -- tile k of sibling segments, or
+// neighbouring tiles of one segment -- and merges their key blocks by start:
+// a block is a 128-key window starting at kb that tile a and/or tile b reads,
+// each with its own range end and causal flag.  Shared ancestor blocks then
+// appear once, so one K/V load feeds both tiles.
+void build_pairs(sp_plan &plan, int32_t block_keys) {
+  plan.pairs.clear();
+  plan.pblk.clear();
+  const int32_t nt = plan.n_tiles();
+  struct B {
+    int32_t kb, end;
+    bool causal;
+  };
+  auto blocks = [&](int32_t t, std::vector<B> &out) {
+    out.clear();
+    const int32_t *tl = &plan.tiles[5 * size_t(t)];
+    for (int32_t r = 0; r < tl[4]; ++r) {
+      const int32_t a = plan.ranges[2 * size_t(tl[3] + r)], e = plan.ranges[2 * size_t(tl[3] + r) + 1];
+      for (int32_t kb = a; kb < e; kb += block_keys) out.push_back({kb, e, r == tl[4] - 1});
+    }
+  };
+  std::vector<B> ba, bb;
+  for (int32_t t = 0; t < nt; t += 2) {
+    const int32_t tb = t + 1 < nt ? t + 1 : -1;
+    blocks(t, ba);
+    if (tb >= 0)
+      blocks(tb, bb);
+    else
+      bb.clear();
+    const int32_t begin = int32_t(plan.pblk.size() / 4);
+    size_t i = 0, j = 0;
+    while (i < ba.size() || j < bb.size()) {
+      int32_t kb, ea = 0, eb = 0, flags = 0;
+      if (j >= bb.size() || (i < ba.size() && ba[i].kb < bb[j].kb)) {
+        kb = ba[i].kb, ea = ba[i].end, flags = ba[i].causal ? 1 : 0;
+        ++i;
+      } else if (i >= ba.size() || bb[j].kb < ba[i].kb) {
+        kb = bb[j].kb, eb = bb[j].end, flags = bb[j].causal ? 2 : 0;
+        ++j;
+      } else {
+        kb = ba[i].kb, ea = ba[i].end, eb = bb[j].end;
+        flags = (ba[i].causal ? 1 : 0) | (bb[j].causal ? 2 : 0);
+        ++i, ++j;
+      }
+      plan.pblk.insert(plan.pblk.end(), {kb, ea, eb, flags});
+    }
+    plan.pairs.insert(plan.pairs.end(), {t, tb, begin, int32_t(plan.pblk.size() / 4) - begin});
+  }
+}
+
 }  // namespace spc
