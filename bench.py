@@ -211,6 +211,23 @@ def run_oracle_sample(w, flop_budget: float, reps: int = 1):
 
 # --------------------------------------------------------------- GPU leg
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest value any rank holds (the job's time is its slowest rank's).
+
+    Replicas only: this timing reduction is the one collective; no data moves
+    between ranks."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, ranks: int, slowest_ms: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest time."""
+    return units_per_rank * ranks / (slowest_ms * 1e-3)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -295,15 +312,13 @@ def run_gpu(args):
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the timed region")
     if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, dev)
 
     pairs = useful_pairs(w.tree)
     f_fwd = 4.0 * D * w.hq * pairs
     f_bwd = 10.0 * D * w.hq * pairs
     ms_step = total_ms / args.steps
-    value = ws * (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12
+    value = job_throughput(f_fwd + f_bwd, ws, ms_step) / 1e12
     peaks, peak_src = load_peaks()
     p_burst = _peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
     p_sust = _peak_value(peaks, "bf16_tflops_sustained") or p_burst

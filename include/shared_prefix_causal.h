@@ -200,6 +200,14 @@ SP_API int sp_tree_attn_bwd_noalloc(const sp_plan *plan, int32_t dtype, const vo
 SP_API int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_dim,
                    const int32_t *idx, int32_t E, void *out, int32_t *d_status, void *stream);
 
+/* Diagnostic for failure-detection tests (the pages have no counterpart):
+ * launches one warp that waits, with the attention kernels' bounded wait, on
+ * an mbarrier nothing ever arrives at.  After spin_limit (>= 256) polls the
+ * wait gives up and ORs SP_DEV_TIMEOUT into *d_status (device int32, required).
+ * Nothing hangs and the CUDA context stays usable.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA. */
+SP_API int sp_debug_wait_timeout(int32_t spin_limit, int32_t *d_status, void *stream);
+
 /* Static English text for a status code (never NULL). */
 SP_API const char *sp_status_string(int status);
 

@@ -70,10 +70,11 @@ _c_bwd_noalloc = _sig("sp_tree_attn_bwd_noalloc", ctypes.c_int,
                        _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_gather = _sig("sp_edge_gather", ctypes.c_int, [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp])
 _c_status = _sig("sp_status_string", ctypes.c_char_p, [ctypes.c_int])
+_c_wait_timeout = _sig("sp_debug_wait_timeout", ctypes.c_int, [_i32, _vp, _vp])
 
 EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
-            "sp_status_string")
+            "sp_status_string", "sp_debug_wait_timeout")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -234,6 +235,11 @@ def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
         raise ValueError("shape or dtype mismatch")
     _check(_c_gather(_dtype_code(hidden), _ptr(hidden), T, Hd, _ptr(idx), E, _ptr(out), _ptr(d_status),
                      _stream(stream)), "sp_edge_gather")
+
+
+def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
+    _need_cuda(d_status)
+    _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream)), "sp_debug_wait_timeout")
 
 
 # ------------------------------------------------------------ conveniences

@@ -33,6 +33,7 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "pipeline.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
 
@@ -46,7 +47,6 @@ constexpr int kBQ = 64;             // query rows per block
 constexpr int kThreads = 320;       // 10 warps
 constexpr int kKChunk = 128 * 128;  // 128 rows x 128 bytes
 constexpr int kQChunk = 64 * 128;   // 64 rows x 128 bytes
-constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kStages = 3;  // Q/dO ring depth
@@ -91,38 +91,6 @@ struct Layout {
 // (bf16 pairs, 32 each), dK and dV (fp32, D each; 256 + 2D <= 512)
 constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_P = 192, T_DK = 256;
 
-struct Ctl {
-  uint32_t bar0;
-  volatile int *abort;
-  int32_t *d_status;
-  __device__ uint32_t bar(int i) const { return bar0 + 8u * uint32_t(i); }
-  __device__ bool wait(int i, uint32_t parity) const {
-    for (uint32_t it = 0;; ++it) {
-      if (mbar_try_wait(bar(i), parity)) return true;
-      if ((it & 255u) == 255u) {
-        if (*abort) return false;
-        if (it >= kSpinLimit) {
-          *abort = 1;
-          if (d_status) atomicOr(d_status, SP_DEV_TIMEOUT);
-          return false;
-        }
-      }
-    }
-  }
-  // Same for a whole warp: one lane polls (32 lanes polling one barrier
-  // serialise on it and starve the warps that do the work), the others wait
-  // at __syncwarp, which also orders their later reads after lane 0's acquire.
-  __device__ bool wait_warp(int i, uint32_t parity) const {
-    bool r = true;
-    if ((threadIdx.x & 31) == 0) r = wait(i, parity);
-    __syncwarp();
-    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-  }
-  __device__ void drain(int i, uint32_t parity) const {
-    for (uint32_t it = 0; it < kSpinLimit; ++it)
-      if (mbar_try_wait(bar(i), parity)) return;
-  }
-};
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -156,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // same dQ rows at about the same time, while those rows are in L2.
   auto q_of = [&](int jj) { return qb + (nq - 1 - jj) * tpb; };
 
-  Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status};
+  Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status, kSpinLimit};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;

@@ -40,6 +40,7 @@
 #include <cmath>
 
 #include "internal.h"
+#include "pipeline.cuh"
 #include "sm103_ptx.cuh"
 #include "tma_host.h"
 
@@ -53,7 +54,6 @@ constexpr int kBN = 128;           // keys per block
 constexpr int kStages = 2;         // K/V ring depth
 constexpr int kThreads = 320;      // 8 softmax warps + producer + MMA
 constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk
-constexpr uint32_t kSpinLimit = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -87,40 +87,6 @@ struct Layout {
   static constexpr uint32_t TILE_COLS = 128 + D;  // S then O, per tile
 };
 
-struct Ctl {
-  uint32_t bar0;
-  volatile int *abort;
-  int32_t *d_status;
-  __device__ uint32_t bar(int i) const { return bar0 + 8u * uint32_t(i); }
-  // Bounded wait; false if it expired here or another role gave up first.
-  __device__ bool wait(int i, uint32_t parity) const {
-    for (uint32_t it = 0;; ++it) {
-      if (mbar_try_wait(bar(i), parity)) return true;
-      if ((it & 255u) == 255u) {
-        if (*abort) return false;
-        if (it >= kSpinLimit) {
-          *abort = 1;
-          if (d_status) atomicOr(d_status, SP_DEV_TIMEOUT);
-          return false;
-        }
-      }
-    }
-  }
-  // Same for a whole warp: one lane polls (32 lanes polling one barrier
-  // serialise on it and starve the warps that do the work), the others wait
-  // at __syncwarp, which also orders their later reads after lane 0's acquire.
-  __device__ bool wait_warp(int i, uint32_t parity) const {
-    bool r = true;
-    if ((threadIdx.x & 31) == 0) r = wait(i, parity);
-    __syncwarp();
-    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-  }
-  // Bounded wait used while draining after an abort (ignores the flag).
-  __device__ void drain(int i, uint32_t parity) const {
-    for (uint32_t it = 0; it < kSpinLimit; ++it)
-      if (mbar_try_wait(bar(i), parity)) return;
-  }
-};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -159,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return;
   }
 
-  Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status};
+  Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status, kSpinLimit};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) mbar_init(ctl.bar(i), (i == B_P_FULL || i == B_P_FULL + 1) ? 128u : 1u);
     *ctl.abort = 0;

@@ -1,0 +1,55 @@
+// Bounded mbarrier waits shared by the tensor-core kernels.
+#pragma once
+
+#include <cstdint>
+
+#include "../../include/shared_prefix_causal.h"
+#include "sm103_ptx.cuh"
+
+namespace spc {
+
+// Polls of one mbarrier before a wait gives up (a few milliseconds to seconds
+// of wall time; legitimate waits in these kernels take microseconds).
+constexpr uint32_t kSpinLimit = 1u << 22;
+
+// Barrier array base, the CTA's abort flag (shared memory) and the caller's
+// status word.  Every wait is bounded: when one expires it sets the abort
+// flag and SP_DEV_TIMEOUT; waits elsewhere in the CTA then give up at their
+// next check, so the CTA winds down instead of hanging.
+struct Ctl {
+  uint32_t bar0;
+  volatile int *abort;
+  int32_t *d_status;
+  uint32_t limit = kSpinLimit;
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * uint32_t(i); }
+  // Bounded wait; false if it expired here or another role gave up first.
+  __device__ bool wait(int i, uint32_t parity) const {
+    for (uint32_t it = 0;; ++it) {
+      if (ptx::mbar_try_wait(bar(i), parity)) return true;
+      if ((it & 255u) == 255u) {
+        if (*abort) return false;
+        if (it >= limit) {
+          *abort = 1;
+          if (d_status) atomicOr(d_status, SP_DEV_TIMEOUT);
+          return false;
+        }
+      }
+    }
+  }
+  // Same for a whole warp: one lane polls (32 lanes polling one barrier
+  // serialise on it and starve the warps that do the work), the others wait
+  // at __syncwarp, which also orders their later reads after lane 0's acquire.
+  __device__ bool wait_warp(int i, uint32_t parity) const {
+    bool r = true;
+    if ((threadIdx.x & 31) == 0) r = wait(i, parity);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+  }
+  // Bounded wait used while draining after an abort (ignores the flag).
+  __device__ void drain(int i, uint32_t parity) const {
+    for (uint32_t it = 0; it < limit; ++it)
+      if (ptx::mbar_try_wait(bar(i), parity)) return;
+  }
+};
+
+}  // namespace spc
