@@ -167,6 +167,27 @@ SP_API int sp_tree_attn_bwd(const sp_plan *plan, int32_t dtype, const void *q, c
                      int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale, int32_t *d_status,
                      void *stream);
 
+/* Bytes of device workspace sp_edge_gather_bwd needs (per-token counts and
+ * offsets, one int per edge). */
+SP_API size_t sp_edge_gather_bwd_workspace_bytes(int32_t T, int32_t E);
+
+/* edge_gather backward -- grad_hidden[t][:] = sum of grad_out[e][:] over the
+ * edges e with idx[e] == t, zero for tokens that are no edge's source.  Each
+ * sampled action's gradient flows back to its source token's hidden state;
+ * a branch-point token shared by several actions receives their sum (one loss
+ * owner per action: issue #7386, "Describe the solution you'd like", fifth
+ * bullet).  Sums run in ascending e with fp32 accumulation, so results are
+ * identical from run to run.
+ *   grad_out [E][hidden_dim], grad_hidden [T][hidden_dim] in dtype (fully
+ *   overwritten); idx [E] int32 (device); hidden_dim a multiple of 8;
+ *   workspace: at least sp_edge_gather_bwd_workspace_bytes(T, E) bytes.
+ * An index outside [0, T) sets SP_DEV_INDEX_RANGE and its row is dropped.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_ALIGNMENT,
+ * SP_ERR_WORKSPACE, SP_ERR_CUDA. */
+SP_API int sp_edge_gather_bwd(int32_t dtype, const void *grad_out, int32_t E, int32_t hidden_dim,
+                              const int32_t *idx, int32_t T, void *grad_hidden, void *workspace,
+                              size_t workspace_bytes, int32_t *d_status, void *stream);
+
 /* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (64u << 20)
 

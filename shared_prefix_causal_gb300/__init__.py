@@ -70,11 +70,14 @@ _c_bwd_noalloc = _sig("sp_tree_attn_bwd_noalloc", ctypes.c_int,
                        _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_gather = _sig("sp_edge_gather", ctypes.c_int, [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp])
 _c_status = _sig("sp_status_string", ctypes.c_char_p, [ctypes.c_int])
+_c_gather_bwd_ws = _sig("sp_edge_gather_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32])
+_c_gather_bwd = _sig("sp_edge_gather_bwd", ctypes.c_int,
+                     [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, ctypes.c_size_t, _vp, _vp])
 _c_wait_timeout = _sig("sp_debug_wait_timeout", ctypes.c_int, [_i32, _vp, _vp])
 
 EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
-            "sp_status_string", "sp_debug_wait_timeout")
+            "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -237,6 +240,24 @@ def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
                      _stream(stream)), "sp_edge_gather")
 
 
+def sp_edge_gather_bwd_workspace_bytes(T: int, E: int) -> int:
+    return int(_c_gather_bwd_ws(T, E))
+
+
+def sp_edge_gather_bwd(grad_out, idx, grad_hidden, workspace, d_status=None, stream=None):
+    _need_cuda(grad_out, idx, grad_hidden, workspace, d_status)
+    import torch
+    if idx.dtype != torch.int32:
+        raise ValueError("edge indices must be int32")
+    E, Hd = grad_out.shape
+    T = grad_hidden.shape[0]
+    if tuple(grad_hidden.shape) != (T, Hd) or grad_hidden.dtype != grad_out.dtype or idx.shape[0] != E:
+        raise ValueError("shape or dtype mismatch")
+    ws = workspace.numel() * workspace.element_size()
+    _check(_c_gather_bwd(_dtype_code(grad_out), _ptr(grad_out), E, Hd, _ptr(idx), T, _ptr(grad_hidden),
+                         _ptr(workspace), ws, _ptr(d_status), _stream(stream)), "sp_edge_gather_bwd")
+
+
 def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
     _need_cuda(d_status)
     _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream)), "sp_debug_wait_timeout")
@@ -273,6 +294,15 @@ def tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, softmax_scale: float, worksp
     ws = bwd_workspace(q) if workspace is None else workspace
     sp_tree_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, ws, softmax_scale, d_status)
     return dq, dk, dv
+
+
+def edge_gather_bwd(grad_out, idx, num_tokens: int, d_status=None):
+    import torch
+    gh = torch.empty((num_tokens, grad_out.shape[1]), dtype=grad_out.dtype, device=grad_out.device)
+    ws = torch.empty(max(16, sp_edge_gather_bwd_workspace_bytes(num_tokens, idx.shape[0])), dtype=torch.uint8,
+                     device=grad_out.device)
+    sp_edge_gather_bwd(grad_out, idx, gh, ws, d_status)
+    return gh
 
 
 def edge_gather(hidden, idx, d_status=None):

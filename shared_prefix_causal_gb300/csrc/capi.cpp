@@ -188,6 +188,26 @@ int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_
   return spc::edge_gather(dtype == SP_BF16 ? 2 : 4, hidden, T, hidden_dim, idx, E, out, d_status, stream);
 }
 
+size_t sp_edge_gather_bwd_workspace_bytes(int32_t T, int32_t E) {
+  if (T < 0 || E < 0) return 0;
+  return spc::edge_gather_bwd_workspace(T, E);
+}
+
+int sp_edge_gather_bwd(int32_t dtype, const void *grad_out, int32_t E, int32_t hidden_dim, const int32_t *idx,
+                       int32_t T, void *grad_hidden, void *workspace, size_t workspace_bytes, int32_t *d_status,
+                       void *stream) {
+  if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_UNSUPPORTED;
+  if (T < 0 || E < 0 || hidden_dim <= 0) return SP_ERR_INVALID_ARG;
+  if (T == 0) return SP_OK;
+  if (!grad_hidden || (E > 0 && (!grad_out || !idx))) return SP_ERR_INVALID_ARG;
+  if (hidden_dim % 8) return SP_ERR_UNSUPPORTED;
+  if (!aligned16(grad_hidden) || (E > 0 && !aligned16(grad_out))) return SP_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < spc::edge_gather_bwd_workspace(T, E)) return SP_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return SP_ERR_ALIGNMENT;
+  return spc::edge_gather_bwd(dtype == SP_BF16 ? 2 : 4, grad_out, E, hidden_dim, idx, T, grad_hidden, workspace,
+                              d_status, stream);
+}
+
 const char *sp_status_string(int status) {
   switch (status) {
     case SP_OK: return "ok";

@@ -66,7 +66,10 @@ int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
            int32_t *d_status, void *stream);
 
-// edge_gather (edge_gather.cu).
+// edge_gather and its backward (edge_gather.cu).
+size_t edge_gather_bwd_workspace(int32_t T, int32_t E);
+int edge_gather_bwd(int32_t elem_bytes, const void *grad_out, int32_t E, int32_t hidden_dim, const int32_t *idx,
+                    int32_t T, void *grad_hidden, void *workspace, int32_t *d_status, void *stream);
 int edge_gather(int32_t elem_bytes, const void *hidden, int32_t T, int32_t hidden_dim,
                 const int32_t *idx, int32_t E, void *out, int32_t *d_status, void *stream);
 

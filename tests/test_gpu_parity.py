@@ -290,3 +290,64 @@ def test_edge_gather_duplicates_fp32_and_bad_index():
     assert (o[1] == 0).all() and (o[2] == 0).all()
     empty, st = _gather(h.cuda(), torch.zeros(0, dtype=torch.int32, device="cuda"))
     assert empty.shape == (0, 36) and st == 0
+
+
+# ---------------------------------------------------------- edge_gather backward
+
+def _gather_bwd(grad_out, idx, T):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gh = spc.edge_gather_bwd(grad_out, idx, T, st)
+    torch.cuda.synchronize()
+    return gh, st.item()
+
+
+@pytest.mark.parametrize("name", ["tiny", "star", "agent"])
+def test_edge_gather_bwd_matches_oracle(name):
+    from oracle import gather as OG
+    w = W.get(name)
+    g = torch.Generator().manual_seed(w.seed + 100)
+    # the configs' indices, plus duplicates (several actions sharing one source token)
+    idx = np.concatenate([w.edge_idx, w.edge_idx[:5], w.edge_idx[:2]]).astype(np.int32)
+    grad = torch.randn(len(idx), w.hidden_dim, generator=g).to(torch.bfloat16)
+    gh, st = _gather_bwd(grad.cuda(), torch.from_numpy(idx).cuda(), w.T)
+    assert st == 0
+    got = gh.cpu()
+    # the oracle runs on the touched tokens only (compacted), untouched rows must be zero
+    touched, cidx = np.unique(idx, return_inverse=True)
+    ref = OG.edge_gather_backward(grad.double().numpy(), cidx, len(touched))
+    refabs = OG.edge_gather_backward(grad.double().abs().numpy(), cidx, len(touched))
+    untouched = np.ones(w.T, dtype=bool)
+    untouched[touched] = False
+    assert bool((got[torch.from_numpy(untouched)] == 0).all())
+    gt = got[torch.from_numpy(touched)]
+    counts = np.bincount(cidx, minlength=len(touched))
+    single = counts == 1
+    # one source per token: an exact copy of that action's row
+    assert np.array_equal(gt[torch.from_numpy(single)].view(torch.int16).numpy(),
+                          torch.from_numpy(ref[single]).to(torch.bfloat16).view(torch.int16).numpy())
+    # several sources: fp32 sum, rounded once to bf16 (half an ulp: at most 2^-8 relative), plus fp32 rounding
+    multi = ~single
+    assert multi.any()
+    err = (gt[torch.from_numpy(multi)].double() - torch.from_numpy(ref[multi])).abs()
+    bound = torch.from_numpy(np.abs(ref[multi])) * 2.0 ** -8 + torch.from_numpy(refabs[multi]) * 2.0 ** -22
+    assert bool((err <= bound).all())
+    # same result on every run
+    gh2, _ = _gather_bwd(grad.cuda(), torch.from_numpy(idx).cuda(), w.T)
+    assert torch.equal(gh2.cpu().view(torch.int16), got.view(torch.int16))
+
+
+def test_edge_gather_bwd_fp32_empty_and_bad_index():
+    from oracle import gather as OG
+    g = torch.Generator().manual_seed(7)
+    grad = torch.randn(6, 16, generator=g)
+    idx = torch.tensor([4, 0, 4, 4, 9, 2], dtype=torch.int32)
+    gh, st = _gather_bwd(grad.cuda(), idx.cuda(), 10)
+    assert st == 0
+    ref = OG.edge_gather_backward(grad.double().numpy(), idx.numpy(), 10)
+    refabs = OG.edge_gather_backward(grad.double().abs().numpy(), idx.numpy(), 10)
+    assert np.all(np.abs(gh.cpu().double().numpy() - ref) <= refabs * 2.0 ** -22)
+    none, st = _gather_bwd(torch.zeros(0, 16).cuda(), torch.zeros(0, dtype=torch.int32).cuda(), 5)
+    assert st == 0 and (none == 0).all()
+    bad, st = _gather_bwd(grad[:2].cuda(), torch.tensor([1, 10], dtype=torch.int32).cuda(), 10)
+    assert st == spc.SP_DEV_INDEX_RANGE
+    assert torch.equal(bad.cpu()[1], grad[0]) and (bad.cpu()[[0, 2, 3]] == 0).all()

@@ -365,3 +365,19 @@ def test_subtree_key_grads_equal_full_backward():
             sk, sv = A.subtree_key_grads(q, k, v, do, *_tree_args(t), 0.4, s, g)
             np.testing.assert_allclose(sk, dK[a0:a1, g], rtol=0, atol=1e-12)
             np.testing.assert_allclose(sv, dV[a0:a1, g], rtol=0, atol=1e-12)
+
+
+def test_edge_gather_backward_is_the_adjoint_of_the_gather():
+    """<gather(h), g> == <h, gather_backward(g)> for random h, g (duplicates included)."""
+    rng = np.random.default_rng(31)
+    T, Hd = 40, 6
+    idx = np.concatenate([rng.integers(0, T, 25), [3, 3, 3, 17]])
+    h = rng.standard_normal((T, Hd))
+    g = rng.standard_normal((len(idx), Hd))
+    lhs = float((OG.edge_gather(h, idx) * g).sum())
+    rhs = float((h * OG.edge_gather_backward(g, idx, T)).sum())
+    assert abs(lhs - rhs) < 1e-12
+    gb = OG.edge_gather_backward(g, idx, T)
+    assert np.array_equal(gb[3], g[np.nonzero(idx == 3)[0]].sum(0))
+    untouched = np.setdiff1d(np.arange(T), idx)
+    assert (gb[untouched] == 0).all()
