@@ -138,3 +138,16 @@ def test_attention_argument_checks_fail_before_device_work():
     assert g(0, fake, 186, 3, fake, 4, fake, None, None) == -3        # row not a multiple of 16 bytes
     assert g(0, fake, 186, 256, fake, -1, fake, None, None) == -2
     assert g(0, ctypes.c_void_p((1 << 20) + 2), 186, 256, fake, 4, fake, None, None) == -4
+
+
+def test_bench_traffic_is_null_when_kernel_sources_change(monkeypatch):
+    import bench
+    assert bench.measured_traffic("tiny", "bwd_tc_kernel") is None  # never captured
+    for cfg, ks in bench.MEASURED_TRAFFIC.items():
+        for k, (nbytes, digest) in ks.items():
+            assert len(digest) == 16 and nbytes > 0
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent", {"bwd_tc_kernel": (1.0, "0" * 16)})
+    assert bench.measured_traffic("agent", "bwd_tc_kernel") is None
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent",
+                        {"bwd_tc_kernel": (7.0, bench.sources_digest("bwd_tc_kernel"))})
+    assert bench.measured_traffic("agent", "bwd_tc_kernel") == 7
