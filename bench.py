@@ -48,10 +48,10 @@ TRAFFIC_SOURCES = {
     "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
 }
 MEASURED_TRAFFIC = {
-    "agent": {"fwd_tc_kernel": (813.46e6 + 510.24e6, "572190e5a2faec78"),
-              "bwd_tc_kernel": (36.98e9 + 18.58e9, "a758a2d882b2ac68")},
-    "star": {"fwd_tc_kernel": (94.24e6 + 26.92e6, "572190e5a2faec78"),
-             "bwd_tc_kernel": (669.17e6 + 312.03e6, "a758a2d882b2ac68")},
+    "agent": {"fwd_tc_kernel": (814.13e6 + 510.82e6, "46ff7e4ca9802a8a"),
+              "bwd_tc_kernel": (13.45e9 + 6.80e9, "ad429f0c5f0c3095")},
+    "star": {"fwd_tc_kernel": (94.23e6 + 26.93e6, "46ff7e4ca9802a8a"),
+             "bwd_tc_kernel": (331.03e6 + 132.79e6, "ad429f0c5f0c3095")},
 }
 
 

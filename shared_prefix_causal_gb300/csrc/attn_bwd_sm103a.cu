@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
                   AttnShape s, const float *__restrict__ lse, const float *__restrict__ delta,
                   float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
-                  int32_t *d_status) {
+                  int32_t *d_status, int head_chunk) {
   using L = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic so that accesses
@@ -107,10 +107,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // items in plan order (longest query run first), the KV heads of an item
-  // adjacent, so the longest runs of every head start in the first wave
-  const int g = blockIdx.x % s.Hkv;
-  const int *blk = plan.bwd + 5 * (blockIdx.x / s.Hkv);
+  // Key blocks in launch order (grouped by query-run end), head_chunk KV heads
+  // at a time: CTA b runs block (b mod head_chunk*n_bwd) / head_chunk of head
+  // chunk b / (head_chunk*n_bwd).
+  const int span = head_chunk * plan.n_bwd;
+  const int item = (blockIdx.x % span) / head_chunk;
+  const int g = (blockIdx.x / span) * head_chunk + blockIdx.x % head_chunk;
+  const int *blk = plan.bwd + 5 * item;
   const int k0 = blk[1], k1 = blk[2], qb = blk[3], qe = blk[4];
   const int T = s.T, Hq = s.Hq;
   if (!(0 <= k0 && k0 < k1 && k1 - k0 <= kBK && qb == k0 && k1 <= qe && qe <= T)) {
@@ -468,6 +471,21 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
   }
 }
 
+// How many KV heads' key blocks run together.  Fewer heads in flight means
+// fewer distinct Q/dO/dQ rows, so CTAs walking the same query run share them
+// through L2; but a chunk must hold enough work that its longest query run does
+// not finish long after the rest.  Pick the smallest divisor c of Hkv for which
+// a chunk's average work per SM is at least twice the longest run, in query
+// blocks plus a fixed per-CTA cost.
+int bwd_head_chunk(const PlanDev &p, const AttnShape &s, int sms) {
+  const double tpb = double(kBQ / s.G), fixed = 6.0;
+  const double total = double(p.bwd_run_sum) / tpb + fixed * p.n_bwd;
+  const double longest = double(p.bwd_run_max) / tpb + fixed;
+  for (int c = 1; c < s.Hkv; ++c)
+    if (s.Hkv % c == 0 && c * total / double(sms) >= 2.0 * longest) return c;
+  return s.Hkv;
+}
+
 template <int D, int G>
 int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
@@ -492,8 +510,9 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
   const unsigned grid = unsigned(p.n_bwd) * unsigned(s.Hkv);
+  const int head_chunk = bwd_head_chunk(p, s, sms);
   kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, dqacc, static_cast<__nv_bfloat16 *>(dk),
-                                     static_cast<__nv_bfloat16 *>(dv), d_status);
+                                     static_cast<__nv_bfloat16 *>(dv), d_status, head_chunk);
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
 
   const long n8 = rows * D / 8;

@@ -32,7 +32,7 @@ int check_tiling(const sp_plan &p, int32_t dtype, int32_t G) {
 
 spc::PlanDev plan_dev(const sp_plan &p) {
   return {p.d_tiles, p.d_ranges, p.d_bwd, p.n_tiles(), p.n_bwd(), p.tile_tokens, p.kv_block,
-          p.d_pairs, p.d_pblk, p.n_pairs()};
+          p.d_pairs, p.d_pblk, p.n_pairs(), p.bwd_run_sum, p.bwd_run_max};
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -84,6 +84,7 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   try {
     spc::build_pairs(*p, 128);
+    spc::build_bwd_schedule(*p);
   } catch (...) {
     return SP_ERR_INVALID_ARG;
   }
@@ -99,7 +100,7 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   int32_t *dk = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br) + align_up(bb) + align_up(bp));
   if ((bt && cudaMemcpyAsync(dt, p->tiles.data(), bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (br && cudaMemcpyAsync(dr, p->ranges.data(), br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      (bb && cudaMemcpyAsync(db, p->bwd.data(), bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (bb && cudaMemcpyAsync(db, p->bwd_sched.data(), bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (bp && cudaMemcpyAsync(dp, p->pairs.data(), bp, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (bk && cudaMemcpyAsync(dk, p->pblk.data(), bk, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       cudaStreamSynchronize(st) != cudaSuccess) {

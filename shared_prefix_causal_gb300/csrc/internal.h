@@ -18,6 +18,11 @@ struct sp_plan {
   // consecutive tiles and, per pair, the merged list of 128-key blocks
   std::vector<int32_t> pairs;   // [p][4] = {tile_a, tile_b or -1, blk_begin, blk_count}
   std::vector<int32_t> pblk;    // [b][4] = {kb, end_a or 0, end_b or 0, causal bits}
+  // backward key blocks in launch order (built at upload; same rows as bwd),
+  // and the total and longest query-run length over them
+  std::vector<int32_t> bwd_sched;  // [k][5]
+  int64_t bwd_run_sum = 0;
+  int32_t bwd_run_max = 0;
   // device copies (owned), valid after sp_plan_upload
   int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr, *d_pairs = nullptr, *d_pblk = nullptr;
   int device = -1;
@@ -32,6 +37,9 @@ namespace spc {
 // Plan builder (plan.cpp).  Returns SP_OK or SP_ERR_INVALID_TREE/ARG.
 int build_plan(const sp_tree_desc &tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
                sp_plan &plan);
+// Backward launch order (see sp_plan::bwd_sched): rows grouped by the end of
+// their query run, latest first, longest run first within a group.
+void build_bwd_schedule(sp_plan &plan);
 // Forward pairs and merged block lists from the tiles (see sp_plan::pairs).
 void build_pairs(sp_plan &plan, int32_t block_keys);
 
@@ -44,6 +52,8 @@ struct PlanDev {
   const int32_t *pairs;
   const int32_t *pblk;
   int32_t n_pairs;
+  int64_t bwd_run_sum;  // sum of q1 - q0 over the bwd rows
+  int32_t bwd_run_max;  // longest q1 - q0
 };
 
 struct AttnShape {

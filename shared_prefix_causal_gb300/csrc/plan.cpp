@@ -209,4 +209,29 @@ void build_pairs(sp_plan &plan, int32_t block_keys) {
   }
 }
 
+// Launch order of the backward's key blocks.  Each CTA re-reads Q and dO along
+// its block's query run and adds dQ partials there, so CTAs that run at the
+// same time should walk the same rows: blocks whose runs end at the same token
+// (the same subtree end) are launched together and walk from that end in step.
+// Within a group the longest run goes first.
+void build_bwd_schedule(sp_plan &plan) {
+  const int32_t n = plan.n_bwd();
+  const int32_t *b = plan.bwd.data();
+  std::vector<int32_t> idx(n);
+  std::iota(idx.begin(), idx.end(), 0);
+  auto len = [&](int32_t i) { return b[5 * i + 4] - b[5 * i + 3]; };
+  std::stable_sort(idx.begin(), idx.end(), [&](int32_t x, int32_t y) {
+    if (b[5 * x + 4] != b[5 * y + 4]) return b[5 * x + 4] > b[5 * y + 4];
+    return len(x) > len(y);
+  });
+  plan.bwd_sched.clear();
+  plan.bwd_run_sum = 0;
+  plan.bwd_run_max = 0;
+  for (int32_t i : idx) {
+    plan.bwd_sched.insert(plan.bwd_sched.end(), b + 5 * i, b + 5 * i + 5);
+    plan.bwd_run_sum += len(i);
+    plan.bwd_run_max = std::max(plan.bwd_run_max, len(i));
+  }
+}
+
 }  // namespace spc
