@@ -27,10 +27,11 @@ Modules: ``tree`` (validation, ancestry, brute-force visibility), ``plan``
 (per-query-tile ancestor KV ranges and the backward KV-block table, derived
 independently of the C++ planner), ``attention`` (leaf-unrolled forward and
 backward, plus the dense tree-mask route for tiny trees), ``gather``
-(sampled-edge selection).
+(sampled-edge selection and its adjoint), ``lm_head`` (log-probability of each
+sampled action through the vocabulary projection, and its backward).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 against brute force, library routines, finite differences or invariants; no
 function is "parity unpinned".
 """
-from . import tree, plan, attention, gather  # noqa: F401
+from . import tree, plan, attention, gather, lm_head  # noqa: F401

@@ -381,3 +381,91 @@ def test_edge_gather_backward_is_the_adjoint_of_the_gather():
     assert np.array_equal(gb[3], g[np.nonzero(idx == 3)[0]].sum(0))
     untouched = np.setdiff1d(np.arange(T), idx)
     assert (gb[untouched] == 0).all()
+
+
+# ------------------------------------------------------------ vocabulary head (log-probabilities)
+
+def _lmh_case(E=5, V=11, Hd=7, seed=0):
+    r = np.random.default_rng(seed)
+    return r.standard_normal((E, Hd)), r.standard_normal((V, Hd)) * 0.7, r.integers(0, V, E)
+
+
+def test_lm_head_zero_weight_gives_uniform_distribution():
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case()
+    lp, lse = LH.edge_logprob(h, np.zeros_like(w), y)
+    np.testing.assert_allclose(lp, -np.log(w.shape[0]), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, np.log(w.shape[0]), rtol=0, atol=1e-15)
+
+
+def test_lm_head_probabilities_sum_to_one_over_the_vocabulary():
+    from oracle import lm_head as LH
+    h, w, _ = _lmh_case(E=3, V=9)
+    total = np.zeros(3)
+    for v in range(9):
+        lp, _ = LH.edge_logprob(h, w, np.full(3, v))
+        total += np.exp(lp)
+    np.testing.assert_allclose(total, 1.0, rtol=0, atol=1e-13)
+
+
+def test_lm_head_matches_scipy_log_softmax():
+    from scipy.special import log_softmax
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case(E=6, V=13, Hd=5, seed=3)
+    lp, _ = LH.edge_logprob(h, w, y)
+    ref = log_softmax(np.einsum("ed,vd->ev", h, w), axis=1)[np.arange(6), y]
+    np.testing.assert_allclose(lp, ref, rtol=0, atol=1e-12)
+
+
+def test_lm_head_is_invariant_to_a_shift_shared_by_all_vocabulary_rows():
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case(seed=4)
+    a = np.random.default_rng(5).standard_normal(w.shape[1])
+    lp0, lse0 = LH.edge_logprob(h, w, y)
+    lp1, lse1 = LH.edge_logprob(h, w + a[None, :], y)
+    np.testing.assert_allclose(lp1, lp0, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse1 - lse0, h @ a, rtol=0, atol=1e-12)
+
+
+def test_lm_head_does_not_overflow_on_large_logits():
+    from oracle import lm_head as LH
+    h = np.array([[1.0, 0.0]])
+    w = np.array([[2000.0, 0.0], [0.0, 0.0], [1990.0, 0.0]])
+    lp, lse = LH.edge_logprob(h, w, np.array([0]))
+    assert np.isfinite(lp).all() and np.isfinite(lse).all()
+    np.testing.assert_allclose(lp, -np.log1p(np.exp(-10.0) + np.exp(-2000.0)), rtol=0, atol=1e-12)
+
+
+def test_lm_head_backward_matches_finite_differences():
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case(E=3, V=5, Hd=4, seed=6)
+    g = np.random.default_rng(7).standard_normal(3)
+    dh, dw = LH.edge_logprob_backward(h, w, y, g)
+    loss = lambda hh, ww: float(np.dot(g, LH.edge_logprob(hh, ww, y)[0]))
+    eps = 1e-6
+    for arr, grad, which in ((h, dh, 0), (w, dw, 1)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            lp_ = loss(p, w) if which == 0 else loss(h, p)
+            lm_ = loss(m, w) if which == 0 else loss(h, m)
+            num[idx] = (lp_ - lm_) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=0, atol=1e-7)
+
+
+def test_lm_head_backward_vanishes_when_all_vocabulary_rows_are_equal():
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case(seed=8)
+    w_eq = np.tile(w[:1], (w.shape[0], 1))
+    dh, _ = LH.edge_logprob_backward(h, w_eq, y, np.ones(len(y)))
+    np.testing.assert_allclose(dh, 0.0, rtol=0, atol=1e-13)
+
+
+def test_lm_head_rejects_labels_outside_the_vocabulary():
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case()
+    y[0] = w.shape[0]
+    with pytest.raises(IndexError):
+        LH.edge_logprob(h, w, y)
