@@ -188,6 +188,31 @@ SP_API int sp_edge_gather_bwd(int32_t dtype, const void *grad_out, int32_t E, in
                               const int32_t *idx, int32_t T, void *grad_hidden, void *workspace,
                               size_t workspace_bytes, int32_t *d_status, void *stream);
 
+/* Bytes of device workspace sp_edge_logprob needs: 8 * E * ceil(V / 256)
+ * (per-tile row maxima and sums) + 4 * E (label logits), each 256-aligned. */
+SP_API size_t sp_edge_logprob_workspace_bytes(int32_t E, int32_t V);
+
+/* Vocabulary head over the sampled-edge states -- the log-probability that
+ * each sampled action assigns to its own token.  Only sampled-edge source
+ * states go through the projection, and each action owns exactly one loss
+ * term (issue #7386, "Describe the solution you'd like", fifth bullet;
+ * PR #7387, "Summary", fourth bullet).  For e in [0, E):
+ *     logits[e][v] = sum_d hidden_sel[e][d] * weight[v][d]   (fp32 accumulation)
+ *     lse[e]       = log sum_v exp(logits[e][v])
+ *     logprob[e]   = logits[e][labels[e]] - lse[e]
+ * The [E][V] logits are never written to memory.
+ *   dtype: SP_BF16 only.  hidden_sel [E][Hd] (e.g. sp_edge_gather's output)
+ *   and weight [V][Hd] (a linear layer's weight layout), row-major, 16-byte
+ *   aligned, Hd a multiple of 8; labels [E] int32 (device); logprob, lse [E]
+ *   fp32 (device, caller-owned, fully overwritten); workspace at least
+ *   sp_edge_logprob_workspace_bytes(E, V) bytes, 256-byte aligned.
+ * A label outside [0, V) sets SP_DEV_INDEX_RANGE and yields NaN for that
+ * action.  Errors: SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED (dtype, Hd),
+ * SP_ERR_ALIGNMENT, SP_ERR_WORKSPACE, SP_ERR_CUDA. */
+SP_API int sp_edge_logprob(int32_t dtype, const void *hidden_sel, int32_t E, int32_t Hd, const void *weight,
+                           int32_t V, const int32_t *labels, float *logprob, float *lse, void *workspace,
+                           size_t workspace_bytes, int32_t *d_status, void *stream);
+
 /* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (64u << 20)
 

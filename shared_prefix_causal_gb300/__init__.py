@@ -70,6 +70,9 @@ _c_bwd_noalloc = _sig("sp_tree_attn_bwd_noalloc", ctypes.c_int,
                        _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_gather = _sig("sp_edge_gather", ctypes.c_int, [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp])
 _c_status = _sig("sp_status_string", ctypes.c_char_p, [ctypes.c_int])
+_c_lmh_ws = _sig("sp_edge_logprob_workspace_bytes", ctypes.c_size_t, [_i32, _i32])
+_c_lmh = _sig("sp_edge_logprob", ctypes.c_int,
+              [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp])
 _c_gather_bwd_ws = _sig("sp_edge_gather_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32])
 _c_gather_bwd = _sig("sp_edge_gather_bwd", ctypes.c_int,
                      [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, ctypes.c_size_t, _vp, _vp])
@@ -77,7 +80,8 @@ _c_wait_timeout = _sig("sp_debug_wait_timeout", ctypes.c_int, [_i32, _vp, _vp])
 
 EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
-            "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd")
+            "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
+            "sp_edge_logprob_workspace_bytes", "sp_edge_logprob")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -258,6 +262,24 @@ def sp_edge_gather_bwd(grad_out, idx, grad_hidden, workspace, d_status=None, str
                          _ptr(workspace), ws, _ptr(d_status), _stream(stream)), "sp_edge_gather_bwd")
 
 
+def sp_edge_logprob_workspace_bytes(E: int, V: int) -> int:
+    return int(_c_lmh_ws(E, V))
+
+
+def sp_edge_logprob(hidden_sel, weight, labels, logprob, lse, workspace, d_status=None, stream=None):
+    _need_cuda(hidden_sel, weight, labels, logprob, lse, workspace, d_status)
+    import torch
+    if labels.dtype != torch.int32 or logprob.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise ValueError("labels must be int32, logprob and lse float32")
+    E, Hd = hidden_sel.shape
+    V = weight.shape[0]
+    if weight.shape[1] != Hd or labels.shape[0] != E or logprob.shape[0] != E or lse.shape[0] != E:
+        raise ValueError("shape mismatch")
+    ws = workspace.numel() * workspace.element_size()
+    _check(_c_lmh(_dtype_code(hidden_sel), _ptr(hidden_sel), E, Hd, _ptr(weight), V, _ptr(labels), _ptr(logprob),
+                  _ptr(lse), _ptr(workspace), ws, _ptr(d_status), _stream(stream)), "sp_edge_logprob")
+
+
 def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
     _need_cuda(d_status)
     _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream)), "sp_debug_wait_timeout")
@@ -294,6 +316,18 @@ def tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, softmax_scale: float, worksp
     ws = bwd_workspace(q) if workspace is None else workspace
     sp_tree_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, ws, softmax_scale, d_status)
     return dq, dk, dv
+
+
+def edge_logprob(hidden_sel, weight, labels, d_status=None):
+    """(logprob [E], lse [E]) of each action's label through the vocabulary head."""
+    import torch
+    E = hidden_sel.shape[0]
+    lp = torch.empty(E, dtype=torch.float32, device=hidden_sel.device)
+    lse = torch.empty(E, dtype=torch.float32, device=hidden_sel.device)
+    ws = torch.empty(max(256, sp_edge_logprob_workspace_bytes(E, weight.shape[0])), dtype=torch.uint8,
+                     device=hidden_sel.device)
+    sp_edge_logprob(hidden_sel, weight, labels, lp, lse, ws, d_status)
+    return lp, lse
 
 
 def edge_gather_bwd(grad_out, idx, num_tokens: int, d_status=None):

@@ -209,6 +209,26 @@ int sp_edge_gather_bwd(int32_t dtype, const void *grad_out, int32_t E, int32_t h
                               d_status, stream);
 }
 
+size_t sp_edge_logprob_workspace_bytes(int32_t E, int32_t V) {
+  if (E < 0 || V < 1) return 0;
+  return spc::lmh_workspace(E, V);
+}
+
+int sp_edge_logprob(int32_t dtype, const void *hidden_sel, int32_t E, int32_t Hd, const void *weight, int32_t V,
+                    const int32_t *labels, float *logprob, float *lse, void *workspace, size_t workspace_bytes,
+                    int32_t *d_status, void *stream) {
+  if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_INVALID_ARG;
+  if (dtype != SP_BF16) return SP_ERR_UNSUPPORTED;
+  if (E < 0 || V < 1 || Hd < 1) return SP_ERR_INVALID_ARG;
+  if (Hd % 8) return SP_ERR_UNSUPPORTED;
+  if (E == 0) return SP_OK;
+  if (!hidden_sel || !weight || !labels || !logprob || !lse) return SP_ERR_INVALID_ARG;
+  if (!aligned16(hidden_sel) || !aligned16(weight)) return SP_ERR_ALIGNMENT;
+  if (!workspace || workspace_bytes < spc::lmh_workspace(E, V)) return SP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SP_ERR_ALIGNMENT;
+  return spc::lmh_fwd(hidden_sel, E, Hd, weight, V, labels, logprob, lse, workspace, d_status, stream);
+}
+
 const char *sp_status_string(int status) {
   switch (status) {
     case SP_OK: return "ok";

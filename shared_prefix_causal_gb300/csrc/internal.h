@@ -77,6 +77,11 @@ int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
            int32_t *d_status, void *stream);
 
 // edge_gather and its backward (edge_gather.cu).
+// Vocabulary head (lm_head_sm103a.cu): per-action log-probability of the
+// sampled label through the projection h W^T, bf16 inputs, fp32 outputs.
+size_t lmh_workspace(int32_t E, int32_t V);
+int lmh_fwd(const void *hidden_sel, int32_t E, int32_t Hd, const void *weight, int32_t V, const int32_t *labels,
+            float *logprob, float *lse, void *workspace, int32_t *d_status, void *stream);
 size_t edge_gather_bwd_workspace(int32_t T, int32_t E);
 int edge_gather_bwd(int32_t elem_bytes, const void *grad_out, int32_t E, int32_t hidden_dim, const int32_t *idx,
                     int32_t T, void *grad_hidden, void *workspace, int32_t *d_status, void *stream);

@@ -45,4 +45,17 @@ int encode_bf16_3d(CUtensorMap *map, const void *base, int inner, int mid, int o
   return r == CUDA_SUCCESS ? SP_OK : SP_ERR_CUDA;
 }
 
+int encode_bf16_2d(CUtensorMap *map, const void *base, int cols, int rows, int box_cols, int box_rows) {
+  EncodeFn fn = encoder();
+  if (!fn) return SP_ERR_CUDA;
+  const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  const cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SP_OK : SP_ERR_CUDA;
+}
+
 }  // namespace spc

@@ -242,6 +242,34 @@ def draw_tensors(w: Workload, dtype: str = "bf16", with_hidden: bool = False) ->
     return out
 
 
+# Vocabulary size for the sampled-edge vocabulary head.  The pages give none;
+# 131,072 entries is a common size for large-vocabulary language models.
+LM_HEAD_VOCAB = 131072
+
+
+def draw_lm_head(num_actions: int, hidden_dim: int, vocab: int = LM_HEAD_VOCAB, seed: int = 0,
+                 weight_scale: float = 2.0) -> dict:
+    """Vocabulary-head weight, sampled labels and upstream gradients (CPU torch tensors).
+
+    hidden_sel ``[num_actions, hidden_dim]`` bf16 ~ N(0, 1) (distributed like
+    rows gathered from the workloads' hidden tensors); weight
+    ``[vocab, hidden_dim]`` bf16 ~ N(0, 1) * weight_scale / sqrt(hidden_dim)
+    (so logits have a standard deviation of about weight_scale); labels
+    ``[num_actions]`` int32 uniform in [0, vocab); grad_logprob
+    ``[num_actions]`` fp32 ~ N(0, 1).
+    """
+    import torch
+    gen = torch.Generator("cpu")
+    gen.manual_seed(seed)
+    hidden_sel = _randn_chunked(gen, num_actions, (hidden_dim,))
+    weight = _randn_chunked(gen, vocab, (hidden_dim,))
+    weight.mul_(weight_scale / float(np.sqrt(hidden_dim)))
+    labels = torch.randint(0, vocab, (num_actions,), generator=gen, dtype=torch.int64).to(torch.int32)
+    grad = torch.randn(num_actions, generator=gen)
+    return {"hidden_sel": hidden_sel.to(torch.bfloat16), "weight": weight.to(torch.bfloat16), "labels": labels,
+            "grad_logprob": grad}
+
+
 def random_small_tree(rng: np.random.Generator, max_segments: int = 8, max_len: int = 24,
                       forest: bool = True) -> Tree:
     """A small random preorder tree (or forest) for brute-force comparisons."""
