@@ -213,6 +213,30 @@ SP_API int sp_edge_logprob(int32_t dtype, const void *hidden_sel, int32_t E, int
                            int32_t V, const int32_t *labels, float *logprob, float *lse, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, void *stream);
 
+/* Bytes of device workspace sp_edge_logprob_bwd needs: 2 * E * V (bf16 dlogits). */
+SP_API size_t sp_edge_logprob_bwd_workspace_bytes(int32_t E, int32_t V);
+
+/* Backward of sp_edge_logprob for upstream gradients grad_logprob[e] =
+ * dL/dlogprob[e] (each sampled action's single loss term, issue #7386,
+ * "Describe the solution you'd like", fifth bullet; the projection backward
+ * that PR #7387 "Validation And Known Limitations" reports as passing):
+ *     dlogits[e][v]    = grad_logprob[e] * (1[v == labels[e]] - exp(logits[e][v] - lse[e]))
+ *     d_hidden_sel[e]  = sum_v dlogits[e][v] * weight[v]          [E][Hd] fp32
+ *     d_weight[v]      = sum_e dlogits[e][v] * hidden_sel[e]      [V][Hd] fp32
+ * The logits are recomputed; dlogits is rounded to bf16 in the workspace and
+ * both products accumulate in fp32.  Outputs are overwritten; pass NULL for
+ * one to skip it.  lse is sp_edge_logprob's output.  Requirements as for
+ * sp_edge_logprob, plus V a multiple of 8 and a workspace of at least
+ * sp_edge_logprob_bwd_workspace_bytes(E, V) bytes, 256-byte aligned; feed
+ * d_hidden_sel to sp_edge_gather_bwd (dtype SP_F32) for the hidden-state
+ * gradient.  A label outside [0, V) sets SP_DEV_INDEX_RANGE (no one-hot term).
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_ALIGNMENT,
+ * SP_ERR_WORKSPACE, SP_ERR_CUDA. */
+SP_API int sp_edge_logprob_bwd(int32_t dtype, const void *hidden_sel, int32_t E, int32_t Hd, const void *weight,
+                               int32_t V, const int32_t *labels, const float *lse, const float *grad_logprob,
+                               float *d_hidden_sel, float *d_weight, void *workspace, size_t workspace_bytes,
+                               int32_t *d_status, void *stream);
+
 /* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (64u << 20)
 

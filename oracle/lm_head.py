@@ -73,3 +73,22 @@ def edge_logprob_backward(hidden_sel, weight, labels, grad_logprob):
     dz[np.arange(E), labels] += 1.0
     dz *= g[:, None]
     return dz @ weight, dz.T @ hidden_sel
+
+
+def weight_grad_rows(hidden_sel, weight, labels, grad_logprob, vocab_rows):
+    """Rows ``vocab_rows`` of ``edge_logprob_backward``'s d_weight.
+
+    The same definition, evaluated only for the requested vocabulary rows:
+    the softmax still normalises over the whole vocabulary (the [E, V] logits
+    are formed in full), only the columns of dlogits that those rows need are
+    built.  For checking a large d_weight one row at a time.
+    """
+    hidden_sel, weight, labels = _check(hidden_sel, weight, labels)
+    g = np.asarray(grad_logprob, dtype=np.float64)
+    rows = np.asarray(vocab_rows, dtype=np.int64)
+    z = logits(hidden_sel, weight)
+    lse = log_sum_exp_rows(z)
+    dz = -np.exp(z[:, rows] - lse[:, None])
+    dz += (labels[:, None] == rows[None, :])
+    dz *= g[:, None]
+    return dz.T @ hidden_sel

@@ -73,6 +73,9 @@ _c_status = _sig("sp_status_string", ctypes.c_char_p, [ctypes.c_int])
 _c_lmh_ws = _sig("sp_edge_logprob_workspace_bytes", ctypes.c_size_t, [_i32, _i32])
 _c_lmh = _sig("sp_edge_logprob", ctypes.c_int,
               [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp])
+_c_lmh_bwd_ws = _sig("sp_edge_logprob_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32])
+_c_lmh_bwd = _sig("sp_edge_logprob_bwd", ctypes.c_int,
+                  [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp])
 _c_gather_bwd_ws = _sig("sp_edge_gather_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32])
 _c_gather_bwd = _sig("sp_edge_gather_bwd", ctypes.c_int,
                      [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, ctypes.c_size_t, _vp, _vp])
@@ -81,7 +84,8 @@ _c_wait_timeout = _sig("sp_debug_wait_timeout", ctypes.c_int, [_i32, _vp, _vp])
 EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
-            "sp_edge_logprob_workspace_bytes", "sp_edge_logprob")
+            "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
+            "sp_edge_logprob_bwd")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -280,6 +284,27 @@ def sp_edge_logprob(hidden_sel, weight, labels, logprob, lse, workspace, d_statu
                   _ptr(lse), _ptr(workspace), ws, _ptr(d_status), _stream(stream)), "sp_edge_logprob")
 
 
+def sp_edge_logprob_bwd_workspace_bytes(E: int, V: int) -> int:
+    return int(_c_lmh_bwd_ws(E, V))
+
+
+def sp_edge_logprob_bwd(hidden_sel, weight, labels, lse, grad_logprob, d_hidden_sel, d_weight, workspace,
+                        d_status=None, stream=None):
+    _need_cuda(hidden_sel, weight, labels, lse, grad_logprob, d_hidden_sel, d_weight, workspace, d_status)
+    import torch
+    E, Hd = hidden_sel.shape
+    V = weight.shape[0]
+    for t, shape in ((d_hidden_sel, (E, Hd)), (d_weight, (V, Hd))):
+        if t is not None and (tuple(t.shape) != shape or t.dtype != torch.float32):
+            raise ValueError("gradient outputs must be float32 [E, Hd] and [V, Hd]")
+    if labels.dtype != torch.int32 or lse.dtype != torch.float32 or grad_logprob.dtype != torch.float32:
+        raise ValueError("labels int32, lse and grad_logprob float32")
+    ws = workspace.numel() * workspace.element_size()
+    _check(_c_lmh_bwd(_dtype_code(hidden_sel), _ptr(hidden_sel), E, Hd, _ptr(weight), V, _ptr(labels), _ptr(lse),
+                      _ptr(grad_logprob), _ptr(d_hidden_sel), _ptr(d_weight), _ptr(workspace), ws, _ptr(d_status),
+                      _stream(stream)), "sp_edge_logprob_bwd")
+
+
 def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
     _need_cuda(d_status)
     _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream)), "sp_debug_wait_timeout")
@@ -328,6 +353,18 @@ def edge_logprob(hidden_sel, weight, labels, d_status=None):
                      device=hidden_sel.device)
     sp_edge_logprob(hidden_sel, weight, labels, lp, lse, ws, d_status)
     return lp, lse
+
+
+def edge_logprob_bwd(hidden_sel, weight, labels, lse, grad_logprob, d_status=None):
+    """(d_hidden_sel [E, Hd], d_weight [V, Hd]) in fp32."""
+    import torch
+    E, Hd = hidden_sel.shape
+    V = weight.shape[0]
+    dh = torch.empty((E, Hd), dtype=torch.float32, device=hidden_sel.device)
+    dw = torch.empty((V, Hd), dtype=torch.float32, device=hidden_sel.device)
+    ws = torch.empty(max(256, sp_edge_logprob_bwd_workspace_bytes(E, V)), dtype=torch.uint8, device=hidden_sel.device)
+    sp_edge_logprob_bwd(hidden_sel, weight, labels, lse, grad_logprob, dh, dw, ws, d_status)
+    return dh, dw
 
 
 def edge_gather_bwd(grad_out, idx, num_tokens: int, d_status=None):

@@ -229,6 +229,36 @@ int sp_edge_logprob(int32_t dtype, const void *hidden_sel, int32_t E, int32_t Hd
   return spc::lmh_fwd(hidden_sel, E, Hd, weight, V, labels, logprob, lse, workspace, d_status, stream);
 }
 
+size_t sp_edge_logprob_bwd_workspace_bytes(int32_t E, int32_t V) {
+  if (E < 0 || V < 1) return 0;
+  return spc::lmh_bwd_workspace(E, V);
+}
+
+int sp_edge_logprob_bwd(int32_t dtype, const void *hidden_sel, int32_t E, int32_t Hd, const void *weight, int32_t V,
+                        const int32_t *labels, const float *lse, const float *grad_logprob, float *d_hidden_sel,
+                        float *d_weight, void *workspace, size_t workspace_bytes, int32_t *d_status, void *stream) {
+  if (dtype != SP_BF16 && dtype != SP_F32) return SP_ERR_INVALID_ARG;
+  if (dtype != SP_BF16) return SP_ERR_UNSUPPORTED;
+  if (E < 0 || V < 1 || Hd < 1) return SP_ERR_INVALID_ARG;
+  if (Hd % 8 || V % 8) return SP_ERR_UNSUPPORTED;
+  if (!d_hidden_sel && !d_weight) return SP_OK;
+  if (!weight || (E > 0 && (!hidden_sel || !labels || !lse || !grad_logprob))) return SP_ERR_INVALID_ARG;
+  if (!aligned16(weight) || (E > 0 && !aligned16(hidden_sel)) || (d_hidden_sel && !aligned16(d_hidden_sel)) ||
+      (d_weight && !aligned16(d_weight)))
+    return SP_ERR_ALIGNMENT;
+  if (E == 0) {
+    // no actions: the weight gradient is zero
+    if (d_weight && cudaMemsetAsync(d_weight, 0, size_t(V) * Hd * sizeof(float),
+                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return SP_ERR_CUDA;
+    return SP_OK;
+  }
+  if (!workspace || workspace_bytes < spc::lmh_bwd_workspace(E, V)) return SP_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SP_ERR_ALIGNMENT;
+  return spc::lmh_bwd(hidden_sel, E, Hd, weight, V, labels, lse, grad_logprob, d_hidden_sel, d_weight, workspace,
+                      d_status, stream);
+}
+
 const char *sp_status_string(int status) {
   switch (status) {
     case SP_OK: return "ok";

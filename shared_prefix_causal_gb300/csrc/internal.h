@@ -82,6 +82,12 @@ int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
 size_t lmh_workspace(int32_t E, int32_t V);
 int lmh_fwd(const void *hidden_sel, int32_t E, int32_t Hd, const void *weight, int32_t V, const int32_t *labels,
             float *logprob, float *lse, void *workspace, int32_t *d_status, void *stream);
+// Backward: bf16 dlogits [E][V] in the workspace, then fp32 d_hidden_sel
+// [E][Hd] and d_weight [V][Hd] (either may be null).  V % 8 == 0.
+size_t lmh_bwd_workspace(int32_t E, int32_t V);
+int lmh_bwd(const void *hidden_sel, int32_t E, int32_t Hd, const void *weight, int32_t V, const int32_t *labels,
+            const float *lse, const float *grad_logprob, float *d_hidden_sel, float *d_weight, void *workspace,
+            int32_t *d_status, void *stream);
 size_t edge_gather_bwd_workspace(int32_t T, int32_t E);
 int edge_gather_bwd(int32_t elem_bytes, const void *grad_out, int32_t E, int32_t hidden_dim, const int32_t *idx,
                     int32_t T, void *grad_hidden, void *workspace, int32_t *d_status, void *stream);

@@ -81,3 +81,81 @@ def test_edge_logprob_after_gather_on_tiny():
     ref_sel = OG.edge_gather(hid.double().numpy(), w.edge_idx)
     rlp, _ = LH.edge_logprob(ref_sel, x["weight"].double().numpy(), x["labels"].numpy())
     assert np.abs(lp.double().numpy() - rlp).max() <= TOL
+
+
+# ------------------------------------------------------------------ backward
+#
+# dlogits is rounded to bf16 (half an ulp: at most 2^-8 relative per element,
+# about 2^-9 / sqrt(3) in rms for uniform rounding errors) before the two
+# fp32-accumulated products, so d_hidden_sel and d_weight agree with the fp64
+# oracle to a relative L2 error of about 1e-3; the tests use 5e-3 (the pages'
+# gradient threshold is 2.5e-2).
+GRAD_TOL = 5e-3
+
+
+def _rel_l2(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def _bwd(h, w, y, g):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hc, wc, yc = h.cuda(), w.cuda(), y.cuda()
+    _, lse = spc.edge_logprob(hc, wc, yc, st)
+    dh, dw = spc.edge_logprob_bwd(hc, wc, yc, lse, g.cuda(), st)
+    torch.cuda.synchronize()
+    return dh.cpu(), dw.cpu(), st.item()
+
+
+@pytest.mark.parametrize("E,V,Hd", [(1, 8, 8), (5, 304, 64), (300, 1000, 200), (129, 520, 136), (260, 4096, 512)])
+def test_edge_logprob_bwd_matches_oracle(E, V, Hd):
+    x = W.draw_lm_head(E, Hd, V, seed=E + 2 * V)
+    h, w, y, g = x["hidden_sel"], x["weight"], x["labels"], x["grad_logprob"]
+    dh, dw, st = _bwd(h, w, y, g)
+    assert st == 0
+    rdh, rdw = LH.edge_logprob_backward(h.double().numpy(), w.double().numpy(), y.numpy(), g.double().numpy())
+    assert _rel_l2(dh, rdh) <= GRAD_TOL
+    assert _rel_l2(dw, rdw) <= GRAD_TOL
+    # vocabulary rows that no action samples get only the softmax part; the sampled ones the one-hot too
+    for v in np.unique(y.numpy())[:3]:
+        assert _rel_l2(dw[v], rdw[v]) <= 4 * GRAD_TOL
+
+
+def test_edge_logprob_bwd_full_size_sampled_rows():
+    """3419 actions, hidden 4096, vocabulary 131,072: all lse, sampled d_hidden_sel and d_weight rows."""
+    w = W.get("agent")
+    E = len(w.edge_idx)
+    x = W.draw_lm_head(E, w.hidden_dim, seed=4)
+    h, wt, y, g = x["hidden_sel"], x["weight"], x["labels"], x["grad_logprob"]
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    hc, wc, yc = h.cuda(), wt.cuda(), y.cuda()
+    lp, lse = spc.edge_logprob(hc, wc, yc, st)
+    dh, dw = spc.edge_logprob_bwd(hc, wc, yc, lse, g.cuda(), st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    hd, wd, yn, gd = h.double().numpy(), wt.double().numpy(), y.numpy(), g.double().numpy()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([[0, 127, 128, E - 1], rng.integers(0, E, 6)]))
+    rdh, _ = LH.edge_logprob_backward(hd[rows], wd, yn[rows], gd[rows])  # rows of d_hidden_sel are independent
+    assert _rel_l2(dh.cpu()[rows], rdh) <= GRAD_TOL
+    vrows = np.unique(np.concatenate([yn[:4], [0, 255, 256, 131071], rng.integers(0, 131072, 4)]))
+    rdw = LH.weight_grad_rows(hd, wd, yn, gd, vrows)
+    assert _rel_l2(dw.cpu()[vrows], rdw) <= GRAD_TOL
+    assert torch.isfinite(dw).all() and torch.isfinite(dh).all()
+
+
+def test_edge_logprob_bwd_skips_outputs_and_handles_no_actions():
+    x = W.draw_lm_head(6, 64, 296, seed=2)
+    h, w, y, g = (x[k].cuda() for k in ("hidden_sel", "weight", "labels", "grad_logprob"))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _, lse = spc.edge_logprob(h, w, y, st)
+    ws = torch.empty(spc.sp_edge_logprob_bwd_workspace_bytes(6, 296), dtype=torch.uint8, device="cuda")
+    dh = torch.full((6, 64), 7.0, device="cuda")
+    spc.sp_edge_logprob_bwd(h, w, y, lse, g, dh, None, ws, st)
+    dh_all, _ = spc.edge_logprob_bwd(h, w, y, lse, g, st)
+    torch.cuda.synchronize()
+    assert torch.equal(dh, dh_all) and st.item() == 0
+    dw0 = torch.full((296, 64), 7.0, device="cuda")
+    spc.sp_edge_logprob_bwd(h[:0], w, y[:0], lse[:0], g[:0], None, dw0, ws, st)
+    torch.cuda.synchronize()
+    assert (dw0 == 0).all()

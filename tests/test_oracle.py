@@ -469,3 +469,12 @@ def test_lm_head_rejects_labels_outside_the_vocabulary():
     y[0] = w.shape[0]
     with pytest.raises(IndexError):
         LH.edge_logprob(h, w, y)
+
+
+def test_lm_head_weight_grad_rows_equals_the_full_backward():
+    from oracle import lm_head as LH
+    h, w, y = _lmh_case(E=7, V=12, Hd=5, seed=9)
+    g = np.random.default_rng(10).standard_normal(7)
+    _, dw = LH.edge_logprob_backward(h, w, y, g)
+    rows = np.array([y[0], 11, 0, y[3], 5])
+    np.testing.assert_allclose(LH.weight_grad_rows(h, w, y, g, rows), dw[rows], rtol=0, atol=1e-13)
