@@ -360,6 +360,8 @@ def run_gpu(args):
     mean_bwd = statistics.mean(bwd_ms)
     mean_fwd = statistics.mean(fwd_ms)
     e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 and not args.no_e2e else None
+    lm_head = run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust) \
+        if gathered is not None and not args.no_lm_head else None
 
     # compulsory bytes: every input read once, every output written once
     algo_fwd = T * (2 * w.hq * D * 2 + 2 * w.hkv * D * 2 + 4 * w.hq)
@@ -408,6 +410,7 @@ def run_gpu(args):
                                          else [LAUNCHES_PER_STEP["fwd"], LAUNCHES_PER_STEP["bwd"]]),
         "clocks": clk,
         "e2e": e2e,
+        "lm_head": lm_head,
     }
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
         cb = run_oracle_sample(w, args.cpu_flops)
@@ -418,6 +421,53 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust):
+    """The sampled-edge vocabulary head after the step: log-probabilities of the
+    gathered states (forward) and their gradients, then the gradient's scatter
+    back to the hidden states.  Timed separately from the attention step."""
+    import torch
+    E, Hd = gathered.shape
+    x = W.draw_lm_head(E, Hd, args.lm_vocab, seed=w.seed)
+    V = x["weight"].shape[0]
+    wt, y, g = x["weight"].to(dev), x["labels"].to(dev), x["grad_logprob"].to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    lp = torch.empty(E, dtype=torch.float32, device=dev)
+    lse = torch.empty(E, dtype=torch.float32, device=dev)
+    dh = torch.empty((E, Hd), dtype=torch.float32, device=dev)
+    dw = torch.empty((V, Hd), dtype=torch.float32, device=dev)
+    ghid = torch.empty((w.T, Hd), dtype=torch.float32, device=dev)
+    ws_f = torch.empty(spc.sp_edge_logprob_workspace_bytes(E, V), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(spc.sp_edge_logprob_bwd_workspace_bytes(E, V), dtype=torch.uint8, device=dev)
+    ws_g = torch.empty(max(256, spc.sp_edge_gather_bwd_workspace_bytes(w.T, E)), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    times = {"fwd": [], "bwd": [], "gather_bwd": []}
+    for i in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        spc.sp_edge_logprob(gathered, wt, y, lp, lse, ws_f, st)
+        ev[1].record(stream)
+        spc.sp_edge_logprob_bwd(gathered, wt, y, lse, g, dh, dw, ws_b, st)
+        ev[2].record(stream)
+        spc.sp_edge_gather_bwd(dh, idx, ghid, ws_g, st)
+        ev[3].record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            times["fwd"].append(ev[0].elapsed_time(ev[1]))
+            times["bwd"].append(ev[1].elapsed_time(ev[2]))
+            times["gather_bwd"].append(ev[2].elapsed_time(ev[3]))
+    if st.item() != 0:
+        raise RuntimeError(f"device status {st.item()} in the vocabulary head")
+    f = 2.0 * E * Hd * V
+    t_f, t_b = statistics.median(times["fwd"]), statistics.median(times["bwd"])
+    return {"actions": E, "hidden": Hd, "vocab": V, "dtype": "bf16 in, fp32 accumulate",
+            "fwd": {"ms": round(t_f, 4), "tflops": round(f / t_f / 1e9, 1),
+                    "frac_of_peak": round(f / t_f / 1e9 / p_burst, 4) if p_burst else None},
+            "bwd": {"ms": round(t_b, 4), "tflops": round(3 * f / t_b / 1e9, 1),
+                    "frac_of_peak": round(3 * f / t_b / 1e9 / p_sust, 4) if p_sust else None},
+            "gather_bwd_ms": round(statistics.median(times["gather_bwd"]), 4),
+            "flops": {"fwd": f, "bwd": 3 * f}, "launches_per_step": {"fwd": 2, "bwd": 3, "gather_bwd": 5}}
 
 
 def run_e2e(args, spc, w, x, dev, flops_per_step):
@@ -504,6 +554,8 @@ def main():
     ap.add_argument("--config", default="agent", choices=list(W.CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--no-lm-head", action="store_true", help="skip the vocabulary-head measurement")
+    ap.add_argument("--lm-vocab", type=int, default=W.LM_HEAD_VOCAB, help="vocabulary size of the vocabulary head")
     ap.add_argument("--cpu-flops", type=float, default=6e11, help="fp64 flop budget of the CPU-baseline sample")
     ap.add_argument("--ref-flops", type=float, default=1.2e11, help="fp64 flop budget per reference step")
     ap.add_argument("--_oracle-child", dest="oracle_child", default=None, help=argparse.SUPPRESS)
