@@ -198,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float *stat = reinterpret_cast<float *>(smem + stage + L::STAT_OFF);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        stat[lane + 32 * h] = nl[h];
-        stat[kBQ + lane + 32 * h] = nd[h];
+      for (int h = 0; h < 2; ++h) {  // staged negated: the consumers add them
+        stat[lane + 32 * h] = -nl[h];
+        stat[kBQ + lane + 32 * h] = -nd[h];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(ctl.bar(B_Q_FULL + st));
@@ -308,32 +308,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(ctl.bar(B_S_FREE));
         }
-        // this half's LSE (log2) and Delta, as float4 shared loads
-        float l2[32], dl[32];
+        // this half's -LSE (log2) and -Delta, as float4 shared loads
+        float nl2[32], ndl[32];
         const float4 *st4 = reinterpret_cast<const float4 *>(stat);
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const float4 a = st4[8 * h + q4], b = st4[16 + 8 * h + q4];
-          l2[4 * q4] = a.x, l2[4 * q4 + 1] = a.y, l2[4 * q4 + 2] = a.z, l2[4 * q4 + 3] = a.w;
-          dl[4 * q4] = b.x, dl[4 * q4 + 1] = b.y, dl[4 * q4 + 2] = b.z, dl[4 * q4 + 3] = b.w;
+          nl2[4 * q4] = a.x, nl2[4 * q4 + 1] = a.y, nl2[4 * q4 + 2] = a.z, nl2[4 * q4 + 3] = a.w;
+          ndl[4 * q4] = b.x, ndl[4 * q4 + 1] = b.y, ndl[4 * q4 + 2] = b.z, ndl[4 * q4 + 3] = b.w;
         }
-        // phases: exponents (masked to -inf), all exp2 back to back, products
+        // phases: exponents (masked to -inf), all exp2 back to back, products;
+        // paired fp32 instructions where the columns need no test
         float pv[32], dsv[32];
         if (nomask && kvalid) {  // two loops: a per-column test inside one loop is far slower
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pv[i] = fmaf(__uint_as_float(us[i]), sl2, -l2[i]);
+          for (int i = 0; i < 32; i += 2)
+            ffma2(pv[i], pv[i + 1], __uint_as_float(us[i]), __uint_as_float(us[i + 1]), sl2, sl2, nl2[i],
+                  nl2[i + 1]);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int c = 32 * h + i;
             const bool vis = kvalid && c / G < ql && kq <= c / G;
-            pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, -l2[i]) : -INFINITY;
+            pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, nl2[i]) : -INFINITY;
           }
         }
 #pragma unroll
         for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) dsv[i] = pv[i] * (__uint_as_float(ud[i]) - dl[i]);
+        for (int i = 0; i < 32; i += 2) {
+          float t0, t1;
+          fadd2(t0, t1, __uint_as_float(ud[i]), __uint_as_float(ud[i + 1]), ndl[i], ndl[i + 1]);
+          fmul2(dsv[i], dsv[i + 1], pv[i], pv[i + 1], t0, t1);
+        }
         if (h == 0 && !(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;  // block j-2's MMAs done
         {  // P^T: 32 query columns as 16 bf16 pairs into this row's TMEM lane
           uint32_t pk[16];

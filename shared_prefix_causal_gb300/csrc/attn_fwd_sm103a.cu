@@ -287,19 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
       const bool full = kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0);
-      if (full) {
-#pragma unroll
-        for (int j = 0; j < kBN; ++j) mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
-      } else {
+      if (!full) {
         const int lim = causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb;
 #pragma unroll
-        for (int j = 0; j < kBN; ++j) {
-          sv[j] = j < lim ? sv[j] : -INFINITY;
-          mx[j & 7] = fmaxf(mx[j & 7], sv[j]);
-        }
+        for (int j = 0; j < kBN; ++j) sv[j] = j < lim ? sv[j] : -INFINITY;
       }
-      const float mb = sl2 * fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      // three-input maxima: two new scores per instruction
+#pragma unroll
+      for (int j = 0; j < kBN; j += 2) mx[(j >> 1) & 7] = fmax3(mx[(j >> 1) & 7], sv[j], sv[j + 1]);
+      const float mb = sl2 * fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       const float m_new = (mb > m_run + kRescaleThreshold) ? mb : m_run;
       const float mref = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = ex2(m_run - mref);
@@ -307,15 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a tree sum and P as bf16 pairs over the first 64 S columns (read by
       // the P V MMA)
       const float nm = -mref;
+      // paired fp32 arithmetic: one instruction per two scores
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) sv[j] = fmaf(sv[j], sl2, nm);
+      for (int j = 0; j < kBN; j += 2) ffma2(sv[j], sv[j + 1], sv[j], sv[j + 1], sl2, sl2, nm, nm);
 #pragma unroll
       for (int j = 0; j < kBN; ++j) sv[j] = ex2(sv[j]);
       float sm[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sm[i] = 0.f;
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) sm[j & 7] += sv[j];
+      for (int j = 0; j < kBN; j += 2) {
+        const int i = (j >> 1) & 3;
+        fadd2(sm[2 * i], sm[2 * i + 1], sm[2 * i], sm[2 * i + 1], sv[j], sv[j + 1]);
+      }
       l_run = l_run * alpha + (((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7])));
       m_run = m_new;
 #pragma unroll

@@ -92,7 +92,10 @@ __global__ void __launch_bounds__(kThreads) gb_count_kernel(const int32_t *__res
   }
 }
 
-// off[0] = 0, off[t + 1] = off[t] + cnt[t]; one CTA, 1024-token chunks.
+// off[0] = 0, off[t + 1] = off[t] + cnt[t]; one CTA over chunks of 8192
+// tokens: thread i scans tokens [8i, 8i+8) of the chunk (two 16-byte loads,
+// coalesced across the warp), one block-wide scan of the thread totals, and a
+// carry from chunk to chunk.
 __global__ void __launch_bounds__(1024) gb_scan_kernel(const int32_t *__restrict__ cnt, int32_t T, int32_t *off) {
   __shared__ int32_t warp_sum[32];
   __shared__ int32_t carry;
@@ -102,10 +105,19 @@ __global__ void __launch_bounds__(1024) gb_scan_kernel(const int32_t *__restrict
     off[0] = 0;
   }
   __syncthreads();
-  for (int base = 0; base < T; base += 1024) {
-    const int t = base + threadIdx.x;
-    const int32_t x = t < T ? cnt[t] : 0;
-    int32_t inc = x;  // inclusive scan within the warp
+  for (int base = 0; base < T; base += 8192) {
+    const int t0 = base + 8 * int(threadIdx.x);
+    int32_t x[8];
+    if (t0 + 8 <= T) {
+      const int4 a = *reinterpret_cast<const int4 *>(cnt + t0), b = *reinterpret_cast<const int4 *>(cnt + t0 + 4);
+      x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) x[k] = t0 + k < T ? cnt[t0 + k] : 0;
+    }
+#pragma unroll
+    for (int k = 1; k < 8; ++k) x[k] += x[k - 1];  // inclusive within the thread
+    int32_t inc = x[7];                           // inclusive over the warp's threads
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int32_t y = __shfl_up_sync(0xffffffffu, inc, d);
@@ -114,17 +126,19 @@ __global__ void __launch_bounds__(1024) gb_scan_kernel(const int32_t *__restrict
     if (lane == 31) warp_sum[w] = inc;
     __syncthreads();
     if (w == 0) {
-      int32_t s = warp_sum[lane];
+      int32_t v = warp_sum[lane];
 #pragma unroll
       for (int d = 1; d < 32; d <<= 1) {
-        const int32_t y = __shfl_up_sync(0xffffffffu, s, d);
-        if (lane >= d) s += y;
+        const int32_t y = __shfl_up_sync(0xffffffffu, v, d);
+        if (lane >= d) v += y;
       }
-      warp_sum[lane] = s;  // inclusive over warps
+      warp_sum[lane] = v;  // inclusive over warps
     }
     __syncthreads();
-    const int32_t before = carry + (w > 0 ? warp_sum[w - 1] : 0);
-    if (t < T) off[t + 1] = before + inc;
+    const int32_t before = carry + (w > 0 ? warp_sum[w - 1] : 0) + inc - x[7];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (t0 + k < T) off[t0 + k + 1] = before + x[k];
     __syncthreads();
     if (threadIdx.x == 0) carry += warp_sum[31];
     __syncthreads();
@@ -141,43 +155,53 @@ __global__ void __launch_bounds__(kThreads) gb_fill_kernel(const int32_t *__rest
   }
 }
 
+// 16 bytes of a row: 4 fp32 or 8 bf16 values, accumulated in fp32.
 template <typename Tv>
-__device__ __forceinline__ void add8(float (&a)[8], const Tv *p);
+struct Vec16;
 template <>
-__device__ __forceinline__ void add8<float>(float (&a)[8], const float *p) {
-  const float4 x = *reinterpret_cast<const float4 *>(p), y = *reinterpret_cast<const float4 *>(p + 4);
-  a[0] += x.x, a[1] += x.y, a[2] += x.z, a[3] += x.w, a[4] += y.x, a[5] += y.y, a[6] += y.z, a[7] += y.w;
-}
+struct Vec16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void add(float (&a)[N], const float *p) {
+    const float4 x = *reinterpret_cast<const float4 *>(p);
+    a[0] += x.x, a[1] += x.y, a[2] += x.z, a[3] += x.w;
+  }
+  static __device__ __forceinline__ void store(float *p, const float (&a)[N]) {
+    *reinterpret_cast<float4 *>(p) = make_float4(a[0], a[1], a[2], a[3]);
+  }
+};
 template <>
-__device__ __forceinline__ void add8<__nv_bfloat16>(float (&a)[8], const __nv_bfloat16 *p) {
-  const uint4 u = *reinterpret_cast<const uint4 *>(p);
-  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void add(float (&a)[N], const __nv_bfloat16 *p) {
+    const uint4 u = *reinterpret_cast<const uint4 *>(p);
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(h[i]);
-    a[2 * i] += f.x, a[2 * i + 1] += f.y;
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      a[2 * i] += f.x, a[2 * i + 1] += f.y;
+    }
   }
-}
-__device__ __forceinline__ void store8(float *p, const float (&a)[8]) {
-  *reinterpret_cast<float4 *>(p) = make_float4(a[0], a[1], a[2], a[3]);
-  *reinterpret_cast<float4 *>(p + 4) = make_float4(a[4], a[5], a[6], a[7]);
-}
-__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&a)[8]) {
-  uint4 u;
-  uint32_t *w = reinterpret_cast<uint32_t *>(&u);
+  static __device__ __forceinline__ void store(__nv_bfloat16 *p, const float (&a)[N]) {
+    uint4 u;
+    uint32_t *w = reinterpret_cast<uint32_t *>(&u);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
-    w[i] = *reinterpret_cast<uint32_t *>(&h);
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(a[2 * i], a[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(p) = u;
   }
-  *reinterpret_cast<uint4 *>(p) = u;
-}
+};
 
 // One warp per token: order the bucket by action index, then sum its rows.
+// Each lane owns 16 consecutive bytes of every 512-byte stretch of the row,
+// so a warp's loads and stores cover whole sectors.
 template <typename Tv>
 __global__ void __launch_bounds__(kThreads) gb_reduce_kernel(const Tv *__restrict__ grad_out, int32_t hidden_dim,
                                                              int32_t T, const int32_t *__restrict__ off,
                                                              int32_t *list, Tv *__restrict__ grad_hidden) {
+  using V16 = Vec16<Tv>;
+  constexpr int kN = V16::N;
   const int lane = threadIdx.x & 31;
   for (int t = blockIdx.x * kWarps + (threadIdx.x >> 5); t < T; t += gridDim.x * kWarps) {
     const int32_t b = off[t], n = off[t + 1] - b;
@@ -195,10 +219,12 @@ __global__ void __launch_bounds__(kThreads) gb_reduce_kernel(const Tv *__restric
     }
     __syncwarp();
     Tv *dst = grad_hidden + size_t(t) * hidden_dim;
-    for (int c = lane * 8; c < hidden_dim; c += 256) {
-      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int i = 0; i < n; ++i) add8(a, grad_out + size_t(bucket[i]) * hidden_dim + c);
-      store8(dst + c, a);
+    for (int c = lane * kN; c < hidden_dim; c += 32 * kN) {
+      float a[kN];
+#pragma unroll
+      for (int i = 0; i < kN; ++i) a[i] = 0.f;
+      for (int i = 0; i < n; ++i) V16::add(a, grad_out + size_t(bucket[i]) * hidden_dim + c);
+      V16::store(dst + c, a);
     }
   }
 }
