@@ -237,6 +237,21 @@ SP_API int sp_edge_logprob_bwd(int32_t dtype, const void *hidden_sel, int32_t E,
                                float *d_hidden_sel, float *d_weight, void *workspace, size_t workspace_bytes,
                                int32_t *d_status, void *stream);
 
+/* sp_tree_attn_bwd with a deterministic dQ: same arguments, workspace and
+ * errors, same dK/dV bits.  Instead of adding every key block's dQ partial
+ * into an fp32 buffer with atomics (whose order, and so rounding, varies from
+ * run to run), each query tile walks its own ancestor key ranges and
+ * accumulates dQ in a fixed order (the per-run gradient accumulation of
+ * "[ENHANCEMENT] Shared-prefix training ...", issue #7386, "Describe the
+ * solution you'd like", made reproducible).  dQ, dK and dV are identical bit
+ * for bit on every call with the same inputs.  Costs three more tensor-core
+ * products per (query tile, key block) than the default path. */
+SP_API int sp_tree_attn_bwd_deterministic(const sp_plan *plan, int32_t dtype, const void *q, const void *k,
+                                          const void *v, const void *o, const float *lse, const void *d_o, void *dq,
+                                          void *dk, void *dv, void *workspace, size_t workspace_bytes, int32_t T,
+                                          int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
+                                          int32_t *d_status, void *stream);
+
 /* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (64u << 20)
 

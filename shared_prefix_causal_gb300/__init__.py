@@ -65,6 +65,9 @@ _c_ws = _sig("sp_tree_attn_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32, _
 _c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_bwd_det = _sig("sp_tree_attn_bwd_deterministic", ctypes.c_int,
+                  [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                   _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_bwd_noalloc = _sig("sp_tree_attn_bwd_noalloc", ctypes.c_int,
                       [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                        _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
@@ -85,7 +88,7 @@ EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
-            "sp_edge_logprob_bwd")
+            "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -206,7 +209,7 @@ def sp_tree_attn_bwd_workspace_bytes(dtype: int, T: int, Hq: int, D: int) -> int
 
 
 def sp_tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale: float,
-                     d_status=None, stream=None):
+                     d_status=None, stream=None, _fn=None):
     _need_cuda(q, k, v, o, lse, d_o, dq, dk, dv, workspace, d_status)
     T, Hq, D = q.shape
     Hkv = k.shape[1]
@@ -215,9 +218,17 @@ def sp_tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, so
         if tuple(t.shape) != shp or t.dtype != q.dtype:
             raise ValueError("shape or dtype mismatch")
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(_c_bwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
-                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D, float(softmax_scale),
-                  _ptr(d_status), _stream(stream)), "sp_tree_attn_bwd")
+    fn, name = _fn or (_c_bwd, "sp_tree_attn_bwd")
+    _check(fn(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D, float(softmax_scale),
+              _ptr(d_status), _stream(stream)), name)
+
+
+def sp_tree_attn_bwd_deterministic(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale: float,
+                                   d_status=None, stream=None):
+    """sp_tree_attn_bwd with dQ formed per query tile (no atomics): identical bits on every run."""
+    sp_tree_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale, d_status, stream,
+                     _fn=(_c_bwd_det, "sp_tree_attn_bwd_deterministic"))
 
 
 def sp_tree_attn_bwd_noalloc(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, softmax_scale: float,
@@ -335,11 +346,13 @@ def bwd_workspace(q) -> "torch.Tensor":
     return torch.empty(max(n, 16), dtype=torch.uint8, device=q.device)
 
 
-def tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, softmax_scale: float, workspace=None, d_status=None):
+def tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, softmax_scale: float, workspace=None, d_status=None,
+                  deterministic: bool = False):
     import torch
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = bwd_workspace(q) if workspace is None else workspace
-    sp_tree_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, ws, softmax_scale, d_status)
+    fn = sp_tree_attn_bwd_deterministic if deterministic else sp_tree_attn_bwd
+    fn(plan, q, k, v, o, lse, d_o, dq, dk, dv, ws, softmax_scale, d_status)
     return dq, dk, dv
 
 

@@ -92,7 +92,7 @@ struct Layout {
 constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_P = 192, T_DK = 256;
 
 
-template <int D, int G>
+template <int D, int G, bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = j - 1, st = m % kStages, pb = m & 1;
           const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
           if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
-          if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
+          if (kDQ && !(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
           tc_fence_after();
           const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
           const uint32_t pso = pb * kPsStep;
@@ -268,11 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
             mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
-          // dQ^T = K^T dS^T   (K = 128 keys)
+          if constexpr (kDQ) {
+            // dQ^T = K^T dS^T   (K = 128 keys)
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
-          mma_commit(ctl.bar(B_DQ_FULL));
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
+            mma_commit(ctl.bar(B_DQ_FULL));
+          }
           mma_commit(ctl.bar(B_P_FREE + pb));
           mma_commit(ctl.bar(B_Q_EMPTY + st));
         }
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else {
+  } else if constexpr (kDQ) {
     // ------------------------------------------------------- dQ readout
     const int d = 32 * (warp - 4) + lane;  // TMEM lane = head-dim index
     const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Delta = rowsum(dO * O) per (token, query head) in fp32, and zero the fp32
-// dQ workspace.  One warp per row; 16-byte loads.
+// dQ workspace (when there is one).  One warp per row; 16-byte loads.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ d_o,
@@ -457,8 +459,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
     }
 #pragma unroll
     for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float4 *z = reinterpret_cast<float4 *>(dqacc + row * D);
-    for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dqacc) {
+      float4 *z = reinterpret_cast<float4 *>(dqacc + row * D);
+      for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (lane == 0) delta[size_t(row % Hq) * T + row / Hq] = acc;
   }
 }
@@ -496,14 +500,15 @@ int bwd_head_chunk(const PlanDev &p, const AttnShape &s, int sms) {
 template <int D, int G>
 int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
-           int32_t *d_status, cudaStream_t st) {
+           bool deterministic, int32_t *d_status, cudaStream_t st) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long rows = long(s.T) * s.Hq;
   const int pre_grid = int(std::min<long>((rows + 7) / 8, long(sms) * 16));
   bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(o),
-                                               static_cast<const __nv_bfloat16 *>(d_o), delta, dqacc, s.T, s.Hq);
+                                               static_cast<const __nv_bfloat16 *>(d_o), delta,
+                                               deterministic ? nullptr : dqacc, s.T, s.Hq);
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
 
   CUtensorMap tq, tdo, tk, tv;
@@ -512,7 +517,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (!rc) rc = encode_bf16_3d(&tk, k, D, s.Hkv, s.T, 64, 1, kBK);
   if (!rc) rc = encode_bf16_3d(&tv, v, D, s.Hkv, s.T, 64, 1, kBK);
   if (rc) return rc;
-  auto kern = bwd_tc_kernel<D, G>;
+  auto kern = deterministic ? bwd_tc_kernel<D, G, false> : bwd_tc_kernel<D, G, true>;
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
@@ -521,6 +526,8 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, dqacc, static_cast<__nv_bfloat16 *>(dk),
                                      static_cast<__nv_bfloat16 *>(dv), d_status, head_chunk);
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
+  // dQ without atomics: every query tile walks its own key blocks
+  if (deterministic) return tc_dq(p, s, q, k, v, lse, d_o, dq, delta, d_status, st);
 
   const long n8 = rows * D / 8;
   const int cgrid = int(std::min<long>((n8 + 255) / 256, long(sms) * 16));
@@ -532,11 +539,11 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
 
 int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
-           int32_t *d_status, void *stream) {
+           bool deterministic, int32_t *d_status, void *stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 #define SPC_BWD_CASE(DD, GG)                                                                          \
   if (s.D == DD && s.G == GG)                                                                         \
-    return launch<DD, GG>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, st);
+    return launch<DD, GG>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, deterministic, d_status, st);
   SPC_BWD_CASE(64, 1) SPC_BWD_CASE(64, 2) SPC_BWD_CASE(64, 4) SPC_BWD_CASE(64, 8)
   SPC_BWD_CASE(128, 1) SPC_BWD_CASE(128, 2) SPC_BWD_CASE(128, 4) SPC_BWD_CASE(128, 8)
 #undef SPC_BWD_CASE

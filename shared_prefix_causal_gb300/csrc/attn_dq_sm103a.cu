@@ -1,0 +1,341 @@
+// Deterministic dQ of shared-prefix tree attention: each query tile walks
+// its own ancestor key ranges ("[ENHANCEMENT] Shared-prefix training with
+// context parallelism for exact agent trajectories", issue #7386, "Describe
+// the solution you'd like": each query run attends to its ancestor path; PR
+// #7387 "TreePackedSeqParams", "Summary": causal attention over each query
+// segment's ancestors) and accumulates
+//
+//   dQ = scale * sum_keys dS K,   dS = P o (dP - Delta),  P = exp(scale Q K^T - LSE),  dP = dO V^T
+//
+// in TMEM, in the plan's fixed block order, so dQ is the same bit for bit on
+// every run (the atomic path adds key blocks' partials in arrival order).
+//
+// dq_tc_kernel: one CTA per (128-row query tile, KV head), KV head outermost
+// so a head's K/V stays in L2 while its tiles run.  Warps 0-3: elementwise
+// (thread = query row = TMEM lane); warp 4: TMA producer (Q and dO once, K/V
+// blocks through a 2-stage ring); warp 5: tcgen05 MMA issuer.  Per key block
+// n the MMA thread issues S = Q K^T and dP = dO V^T (SS), and, once the
+// elementwise warps have stored dS(n) as bf16 pairs in TMEM, dQ += dS(n) K(n)
+// (A read from TMEM, K as an MN-major B).  S(n+1) and dP(n+1) are issued as
+// soon as S(n) and dP(n) have been read, so they run while dS(n) is formed;
+// dS alternates between two TMEM buffers.
+// TMEM: S 128 + dP 128 + dQ D + 2 x 64 (dS) <= 512 columns.
+//
+// Every wait is bounded (Ctl): on expiry the CTA sets SP_DEV_TIMEOUT, stops
+// issuing, drains its copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "internal.h"
+#include "pipeline.cuh"
+#include "sm103_ptx.cuh"
+#include "tma_host.h"
+
+namespace spc {
+namespace {
+
+using namespace ptx;
+
+constexpr int kBM = 128;           // query rows per tile (tokens x query heads of one KV head)
+constexpr int kBN = 128;           // keys per block
+constexpr int kStages = 2;         // K/V ring depth
+constexpr int kThreads = 192;      // 4 elementwise warps, producer, MMA
+constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum : int {
+  B_Q_FULL = 0,
+  B_KV_FULL = 1,   // +stage
+  B_KV_EMPTY = 3,  // +stage
+  B_S_FULL = 5,
+  B_S_FREE = 6,    // 4 warp arrivals
+  B_DS_FULL = 7,   // +buffer, 4 warp arrivals
+  B_DS_FREE = 9,   // +buffer
+  B_DQ_DONE = 11,
+  B_COUNT = 12
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kDChunks = D / 64;
+  static constexpr int KV = kDChunks * kChunk;  // bytes of 128 rows x D
+  static constexpr int Q = 0;
+  static constexpr int DO = KV;
+  static constexpr int K = 2 * KV;  // + stage * KV
+  static constexpr int V = K + kStages * KV;
+  static constexpr int BAR = V + kStages * KV;
+  static constexpr int TSLOT = BAR + 8 * B_COUNT;
+  static constexpr int ABORT = TSLOT + 4;
+  static constexpr int BYTES = ABORT + 4 + 1024;
+  // at least ~116 KB so two CTAs never share an SM (each takes all 512 TMEM columns)
+  static constexpr int ALLOC = BYTES > 120 * 1024 ? BYTES : 120 * 1024;
+};
+
+constexpr uint32_t T_S = 0, T_DP = 128, T_DQ = 256, T_DS = 384;
+
+// Walks a tile's key blocks: ranges in plan order, 128 keys at a time.
+struct BlockWalk {
+  const int *rg;
+  int rc, r, kb;
+  __device__ BlockWalk(const int *ranges, int count) : rg(ranges), rc(count), r(0), kb(ranges[0]) {}
+  __device__ int end() const { return rg[2 * r + 1]; }
+  __device__ bool causal() const { return r == rc - 1; }
+  __device__ void next() {
+    kb += kBN;
+    if (kb >= rg[2 * r + 1] && ++r < rc) kb = rg[2 * r];
+  }
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
+                 AttnShape s, const float *__restrict__ lse, const float *__restrict__ delta,
+                 __nv_bfloat16 *__restrict__ dq, int32_t *d_status) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = s.T;
+
+  const int g = blockIdx.x / plan.n_tiles;
+  const int *tl = plan.tiles + 5 * (blockIdx.x % plan.n_tiles);
+  const int q0 = tl[1], q1 = tl[2], rb = tl[3], rc = tl[4];
+  const int *rg = plan.ranges + 2 * rb;
+  // Validate the work item (uniform over the CTA) and count its key blocks.
+  bool bad = !(0 <= q0 && q0 < q1 && q1 <= T && (q1 - q0) * G <= kBM && rc >= 1);
+  int nblk = 0;
+  for (int i = 0; !bad && i < rc; ++i) {
+    const int a = rg[2 * i], e = rg[2 * i + 1];
+    if (!(0 <= a && a < e && e <= T)) bad = true;
+    nblk += (e - a + kBN - 1) / kBN;
+  }
+  if (bad) {
+    if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
+    return;
+  }
+
+  Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status, kSpinLimit};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < B_COUNT; ++i)
+      mbar_init(ctl.bar(i), (i == B_S_FREE || i == B_DS_FULL || i == B_DS_FULL + 1) ? 4u : 1u);
+    *ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(sbase + L::TSLOT, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_do);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      mbar_arrive_expect_tx(ctl.bar(B_Q_FULL), 2u * L::KV);
+#pragma unroll
+      for (int c = 0; c < L::kDChunks; ++c) {
+        tma_load_3d(sbase + L::Q + c * kChunk, &tm_q, ctl.bar(B_Q_FULL), c * 64, g * G, q0);
+        tma_load_3d(sbase + L::DO + c * kChunk, &tm_do, ctl.bar(B_Q_FULL), c * 64, g * G, q0);
+      }
+      BlockWalk w(rg, rc);
+      int n = 0;
+      for (; n < nblk; ++n, w.next()) {
+        const int st = n & 1;
+        if (!ctl.wait(B_KV_EMPTY + st, ((n >> 1) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(ctl.bar(B_KV_FULL + st), 2u * L::KV);
+#pragma unroll
+        for (int c = 0; c < L::kDChunks; ++c) {
+          tma_load_3d(sbase + L::K + st * L::KV + c * kChunk, &tm_k, ctl.bar(B_KV_FULL + st), c * 64, g, w.kb);
+          tma_load_3d(sbase + L::V + st * L::KV + c * kChunk, &tm_v, ctl.bar(B_KV_FULL + st), c * 64, g, w.kb);
+        }
+      }
+      if (*ctl.abort) {
+        // let the fills still in flight land before the CTA exits
+        ctl.drain(B_Q_FULL, 0);
+        for (int m = n - kStages < 0 ? 0 : n - kStages; m < n; ++m) ctl.drain(B_KV_FULL + (m & 1), (m >> 1) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(kBM, kBN, 0, 0);  // S = Q K^T, dP = dO V^T
+      constexpr uint32_t id_q = idesc_bf16_f32(kBM, D, 0, 1);    // dQ += dS K (K as MN-major B)
+      const uint64_t dq_a = smem_desc_sw128(sbase + L::Q, 16, 1024);
+      const uint64_t ddo_a = smem_desc_sw128(sbase + L::DO, 16, 1024);
+      // S(n), dP(n) into TMEM; one commit for both
+      auto issue_s = [&](int n) {
+        const uint32_t kst = sbase + L::K + (n & 1) * L::KV, vst = sbase + L::V + (n & 1) * L::KV;
+        const uint64_t dk = smem_desc_sw128(kst, 16, 1024), dv = smem_desc_sw128(vst, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + T_S, dq_a + off, dk + off, id_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + T_DP, ddo_a + off, dv + off, id_s, kk > 0);
+        }
+        mma_commit(ctl.bar(B_S_FULL));
+      };
+      bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_KV_FULL, 0);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      for (int n = 0; ok && n < nblk; ++n) {
+        const int st = n & 1;
+        if (n + 1 < nblk) {
+          // S(n) and dP(n) have been read out: S(n+1), dP(n+1) may overwrite them
+          if (!(ok = ctl.wait(B_S_FREE, n & 1))) break;
+          if (!(ok = ctl.wait(B_KV_FULL + (st ^ 1), ((n + 1) >> 1) & 1))) break;
+          tc_fence_after();
+          issue_s(n + 1);
+        }
+        if (!(ok = ctl.wait(B_DS_FULL + st, (n >> 1) & 1))) break;
+        tc_fence_after();
+        const uint64_t dk_mn = smem_desc_sw128(sbase + L::K + st * L::KV, kChunk, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(tmem + T_DQ, tmem + T_DS + 64 * st + 8 * kk, dk_mn + ((kk * 2048) >> 4), id_q,
+                      (n > 0 || kk > 0));
+        mma_commit(ctl.bar(B_DS_FREE + st));
+        mma_commit(ctl.bar(B_KV_EMPTY + st));
+      }
+      mma_commit(ctl.bar(B_DQ_DONE));
+      ctl.drain(B_DQ_DONE, 0);
+    }
+  } else {
+    // --------------------------------------------------------- elementwise
+    const int r = threadIdx.x;  // query row = TMEM lane
+    const uint32_t lane_base = uint32_t(32 * warp) << 16;
+    const int tok = q0 + r / G, head = g * G + r % G;
+    const bool rowv = tok < q1;
+    const float sl2 = s.scale * kLog2e;
+    const float nl2 = rowv ? -__ldg(lse + size_t(head) * T + tok) * kLog2e : 0.f;
+    const float ndl = rowv ? -__ldg(delta + size_t(head) * T + tok) : 0.f;
+    BlockWalk w(rg, rc);
+    bool ok = true;
+    for (int n = 0; n < nblk; ++n, w.next()) {
+      const int st = n & 1;
+      if (!(ok = ctl.wait_warp(B_S_FULL, n & 1))) break;
+      tc_fence_after();
+      const int kv1 = w.end(), kb = w.kb;
+      const bool causal = w.causal();
+      // every row of the tile sees every key of the block
+      const bool full = kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0);
+      // keys [kb, kb + lim) visible to this row
+      const int lim = !rowv ? 0 : (causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb);
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t us[32], ud[32];
+        tmem_ld32x2(tmem + lane_base + T_S + 32 * c, tmem + lane_base + T_DP + 32 * c, us, ud);
+        if (c == kBN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ctl.bar(B_S_FREE));
+        }
+        float pv[32], dsv[32];
+        if (full && rowv) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2)
+            ffma2(pv[i], pv[i + 1], __uint_as_float(us[i]), __uint_as_float(us[i + 1]), sl2, sl2, nl2, nl2);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pv[i] = 32 * c + i < lim ? fmaf(__uint_as_float(us[i]), sl2, nl2) : -INFINITY;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float t0, t1;
+          fadd2(t0, t1, __uint_as_float(ud[i]), __uint_as_float(ud[i + 1]), ndl, ndl);
+          fmul2(dsv[i], dsv[i + 1], pv[i], pv[i + 1], t0, t1);
+        }
+        // dS(n) goes to buffer st once dQ(n-2) has read it
+        if (c == 0 && !(ok = ctl.wait_warp(B_DS_FREE + st, ((n >> 1) & 1) ^ 1))) break;
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(dsv[2 * i], dsv[2 * i + 1]);
+        tmem_st16(tmem + lane_base + T_DS + 64 * st + 16 * c, pk);
+      }
+      if (!ok) break;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctl.bar(B_DS_FULL + st));
+    }
+    if (ok && ctl.wait_warp(B_DQ_DONE, 0)) {
+      tc_fence_after();
+      __nv_bfloat16 *row = dq + (size_t(tok) * s.Hq + head) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + T_DQ + 32 * c, u);
+        if (rowv) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(u[i]) * s.scale, __uint_as_float(u[i + 1]) * s.scale);
+            v.y = pack_bf16(__uint_as_float(u[i + 2]) * s.scale, __uint_as_float(u[i + 3]) * s.scale);
+            v.z = pack_bf16(__uint_as_float(u[i + 4]) * s.scale, __uint_as_float(u[i + 5]) * s.scale);
+            v.w = pack_bf16(__uint_as_float(u[i + 6]) * s.scale, __uint_as_float(u[i + 7]) * s.scale);
+            *reinterpret_cast<uint4 *>(row + 32 * c + i) = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int G>
+int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,
+           const void *d_o, void *dq, const float *delta, int32_t *d_status, cudaStream_t st) {
+  CUtensorMap tq, tdo, tk, tv;
+  int rc = encode_bf16_3d(&tq, q, D, s.Hq, s.T, 64, G, kBM / G);
+  if (!rc) rc = encode_bf16_3d(&tdo, d_o, D, s.Hq, s.T, 64, G, kBM / G);
+  if (!rc) rc = encode_bf16_3d(&tk, k, D, s.Hkv, s.T, 64, 1, kBN);
+  if (!rc) rc = encode_bf16_3d(&tv, v, D, s.Hkv, s.T, 64, 1, kBN);
+  if (rc) return rc;
+  auto kern = dq_tc_kernel<D, G>;
+  const int smem = Layout<D>::ALLOC;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return SP_ERR_CUDA;
+  const unsigned grid = unsigned(p.n_tiles) * unsigned(s.Hkv);
+  kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, static_cast<__nv_bfloat16 *>(dq), d_status);
+  return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+}  // namespace
+
+int tc_dq(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,
+          const void *d_o, void *dq, const float *delta, int32_t *d_status, void *stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define SPC_DQ_CASE(DD, GG) \
+  if (s.D == DD && s.G == GG) return launch<DD, GG>(p, s, q, k, v, lse, d_o, dq, delta, d_status, st);
+  SPC_DQ_CASE(64, 1) SPC_DQ_CASE(64, 2) SPC_DQ_CASE(64, 4) SPC_DQ_CASE(64, 8)
+  SPC_DQ_CASE(128, 1) SPC_DQ_CASE(128, 2) SPC_DQ_CASE(128, 4) SPC_DQ_CASE(128, 8)
+#undef SPC_DQ_CASE
+  return SP_ERR_UNSUPPORTED;
+}
+
+}  // namespace spc

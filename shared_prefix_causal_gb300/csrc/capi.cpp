@@ -150,10 +150,14 @@ size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t Hq, in
   return delta + align_up(size_t(T) * size_t(Hq) * size_t(D) * sizeof(float));
 }
 
-int sp_tree_attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, const void *o,
-                     const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace,
-                     size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
-                     int32_t *d_status, void *stream) {
+}  // extern "C"
+
+namespace {
+
+int attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, const void *o,
+             const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
+             int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale, bool deterministic,
+             int32_t *d_status, void *stream) {
   if (!p) return SP_ERR_INVALID_ARG;
   if (int rc = check_heads(dtype, T, Hq, Hkv, D)) return rc;
   if (T != p->total_tokens) return SP_ERR_INVALID_ARG;
@@ -174,9 +178,31 @@ int sp_tree_attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void 
   if (dtype == SP_BF16) {
     float *dqacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                              align_up(size_t(T) * size_t(Hq) * sizeof(float)));
-    return spc::tc_bwd(plan_dev(*p), s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, d_status, stream);
+    return spc::tc_bwd(plan_dev(*p), s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, deterministic, d_status,
+                       stream);
   }
+  // the fp32 path computes dQ per query tile already (no atomics)
   return spc::simt_bwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_o, dq, dk, dv, delta, d_status, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sp_tree_attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, const void *o,
+                     const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace,
+                     size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
+                     int32_t *d_status, void *stream) {
+  return attn_bwd(p, dtype, q, k, v, o, lse, d_o, dq, dk, dv, workspace, workspace_bytes, T, Hq, Hkv, D,
+                  softmax_scale, false, d_status, stream);
+}
+
+int sp_tree_attn_bwd_deterministic(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v,
+                                   const void *o, const float *lse, const void *d_o, void *dq, void *dk, void *dv,
+                                   void *workspace, size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv,
+                                   int32_t D, float softmax_scale, int32_t *d_status, void *stream) {
+  return attn_bwd(p, dtype, q, k, v, o, lse, d_o, dq, dk, dv, workspace, workspace_bytes, T, Hq, Hkv, D,
+                  softmax_scale, true, d_status, stream);
 }
 
 int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_dim, const int32_t *idx, int32_t E,

@@ -71,10 +71,15 @@ int simt_bwd(const PlanDev &p, const AttnShape &s, int32_t dtype, const void *q,
 // Tensor-core kernels (sm_103a): bf16 input, tile_tokens * G == 128, kv_block == 128.
 int tc_fwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, void *o, float *lse,
            int32_t *d_status, void *stream);
-// delta: [Hq][T] fp32 scratch; dqacc: [T][Hq][D] fp32 scratch (zeroed inside).
+// delta: [Hq][T] fp32 scratch; dqacc: [T][Hq][D] fp32 scratch (zeroed inside;
+// unused when deterministic, which computes dQ per query tile with tc_dq).
 int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
-           int32_t *d_status, void *stream);
+           bool deterministic, int32_t *d_status, void *stream);
+// dQ of every query tile over its own key blocks, no atomics (attn_dq_sm103a.cu);
+// delta from the backward's preprocess.
+int tc_dq(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,
+          const void *d_o, void *dq, const float *delta, int32_t *d_status, void *stream);
 
 // edge_gather and its backward (edge_gather.cu).
 // Vocabulary head (lm_head_sm103a.cu): per-action log-probability of the

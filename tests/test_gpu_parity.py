@@ -39,14 +39,15 @@ def rel_l2(x, ref):
     return float(np.linalg.norm(x - ref) / nref)
 
 
-def run_gpu(w, dtype="bf16", tile_tokens=None, order=0, x=None, kv_block=128):
+def run_gpu(w, dtype="bf16", tile_tokens=None, order=0, x=None, kv_block=128, deterministic=False):
     x = W.draw_tensors(w, dtype) if x is None else x
     q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
     G = w.hq // w.hkv
     plan = spc.tree_plan(w.tree, tile_tokens or 128 // G, kv_block, order)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale, st)
-    dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, d_status=st)
+    dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, d_status=st,
+                                   deterministic=deterministic)
     torch.cuda.synchronize()
     assert st.item() == 0
     out = {n: t.float().cpu().numpy() for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
@@ -236,6 +237,53 @@ def test_long_bf16_sampled():
     x, out = run_gpu(w, "bf16")
     check_sampled(w, x, out, groups=[0], n_leaves=1, extra_rows=128)
     check_sums(w, x, out)
+
+
+# ------------------------------------------------------ deterministic backward
+
+def test_deterministic_bwd_tiny_and_degenerate_trees():
+    w = W.tiny()
+    x, out = run_gpu(w, "bf16", deterministic=True)
+    check_full(w, x, out, "bf16")
+    rng = np.random.default_rng(11)
+    trees = [W.tree_from_preorder([300], [-1]), W.tree_from_preorder([1] * 40, [-1] + list(range(39))),
+             W.random_small_tree(rng, max_segments=30, max_len=200)]
+    for tr in trees:
+        we = W.Workload("edge", "", tr, 8, 2, 128, 0.5, 9, None, None)
+        xe, oe = run_gpu(we, "bf16", deterministic=True)
+        check_full(we, xe, oe, "bf16")
+
+
+def test_deterministic_bwd_star_is_reproducible():
+    w = W.grpo_star()
+    x, out = run_gpu(w, "bf16", deterministic=True)
+    check_full(w, x, out, "bf16", groups=[0, w.hkv - 1])
+    check_sums(w, x, out)
+    _, out2 = run_gpu(w, "bf16", deterministic=True, x=x)
+    _, ref = run_gpu(w, "bf16", x=x)
+    for n in ("dq", "dk", "dv"):
+        assert np.array_equal(out[n], out2[n]), n  # bit-identical from run to run
+    for n in ("dk", "dv"):
+        assert np.array_equal(out[n], ref[n]), n  # dK, dV: the same kernel either way
+    # dQ: the two summation orders agree to within bf16 rounding
+    assert rel_l2(out["dq"], ref["dq"]) < 5e-3
+
+
+@pytest.mark.slow
+def test_deterministic_bwd_agent_sampled():
+    w = W.agent_tree()
+    x, out = run_gpu(w, "bf16", deterministic=True)
+    check_sampled(w, x, out, groups=[0, w.hkv - 1])
+    check_sums(w, x, out)
+    _, out2 = run_gpu(w, "bf16", deterministic=True, x=x)
+    assert np.array_equal(out["dq"], out2["dq"])
+
+
+@pytest.mark.slow
+def test_deterministic_bwd_long_sampled():
+    w = W.long_fragment()
+    x, out = run_gpu(w, "bf16", deterministic=True)
+    check_sampled(w, x, out, groups=[0], n_leaves=1, extra_rows=128)
 
 
 def test_sibling_isolation_bit_exact():
