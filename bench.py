@@ -48,10 +48,10 @@ TRAFFIC_SOURCES = {
     "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
 }
 MEASURED_TRAFFIC = {
-    "agent": {"fwd_tc_kernel": (814.13e6 + 510.82e6, "46ff7e4ca9802a8a"),
-              "bwd_tc_kernel": (13.45e9 + 6.80e9, "ad429f0c5f0c3095")},
-    "star": {"fwd_tc_kernel": (94.23e6 + 26.93e6, "46ff7e4ca9802a8a"),
-             "bwd_tc_kernel": (331.03e6 + 132.79e6, "ad429f0c5f0c3095")},
+    "agent": {"fwd_tc_kernel": (813.67e6 + 511.32e6, "5ebdf652e2c4eaed"),
+              "bwd_tc_kernel": (13.20e9 + 6.73e9, "af69ca8547df25bb")},
+    "star": {"fwd_tc_kernel": (94.39e6 + 27.56e6, "5ebdf652e2c4eaed"),
+             "bwd_tc_kernel": (331.91e6 + 132.75e6, "af69ca8547df25bb")},
 }
 
 
@@ -360,6 +360,8 @@ def run_gpu(args):
     mean_bwd = statistics.mean(bwd_ms)
     mean_fwd = statistics.mean(fwd_ms)
     e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 and not args.no_e2e else None
+    det = run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status, dev, f_bwd,
+                                p_burst)
     lm_head = run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust) \
         if gathered is not None and not args.no_lm_head else None
 
@@ -410,6 +412,7 @@ def run_gpu(args):
                                          else [LAUNCHES_PER_STEP["fwd"], LAUNCHES_PER_STEP["bwd"]]),
         "clocks": clk,
         "e2e": e2e,
+        "bwd_deterministic": det,
         "lm_head": lm_head,
     }
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
@@ -421,6 +424,28 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status, dev, f_bwd,
+                          p_burst):
+    """The backward with dQ formed per query tile (no atomics), timed like the step's backward."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        spc.sp_tree_attn_bwd_deterministic(plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            ms.append(e0.elapsed_time(e1))
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} in the deterministic backward")
+    t = statistics.median(ms)
+    tf = f_bwd / (t * 1e-3) / 1e12
+    return {"ms": round(t, 4), "useful_tflops": round(tf, 2), "frac_of_peak": round(tf / p_burst, 4) if p_burst else None,
+            "launches": 3}
 
 
 def run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust):
