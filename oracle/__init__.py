@@ -28,10 +28,11 @@ Modules: ``tree`` (validation, ancestry, brute-force visibility), ``plan``
 independently of the C++ planner), ``attention`` (leaf-unrolled forward and
 backward, plus the dense tree-mask route for tiny trees), ``gather``
 (sampled-edge selection and its adjoint), ``lm_head`` (log-probability of each
-sampled action through the vocabulary projection, and its backward).
+sampled action through the vocabulary projection, and its backward),
+``fragments`` (bounded fragment planning with repeated ancestors).
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 against brute force, library routines, finite differences or invariants; no
 function is "parity unpinned".
 """
-from . import tree, plan, attention, gather, lm_head  # noqa: F401
+from . import tree, plan, attention, gather, lm_head, fragments  # noqa: F401

@@ -478,3 +478,68 @@ def test_lm_head_weight_grad_rows_equals_the_full_backward():
     _, dw = LH.edge_logprob_backward(h, w, y, g)
     rows = np.array([y[0], 11, 0, y[3], 5])
     np.testing.assert_allclose(LH.weight_grad_rows(h, w, y, g, rows), dw[rows], rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------------------ bounded fragments
+
+def test_fragments_single_fragment_when_the_cap_is_large():
+    from oracle import fragments as OF
+    t = W.tiny()
+    frags = OF.plan_fragments(t.tree.seg_len, t.tree.parent, t.T)
+    assert len(frags) == 1 and all(o for _, o in frags[0])
+    assert OF.fragment_tokens(frags, t.tree.seg_len) == t.T
+
+
+def test_fragments_hand_example():
+    # root 64 -> children 32, 48 (-> grandchildren 16, 9), 17: the tiny tree, cap 130
+    from oracle import fragments as OF
+    lens = [64, 32, 48, 16, 9, 17]
+    par = [-1, 0, 0, 2, 2, 0]
+    frags = OF.plan_fragments(lens, par, 130)
+    # 64+32 = 96; +48 > 130 -> new fragment {0, 2}, 112; +16 = 128; +9 > 130 -> new {0, 2, 4} = 121;
+    # +17 > 130 -> new {0, 5} = 81
+    assert frags == [[(0, True), (1, True)], [(0, False), (2, True), (3, True)],
+                     [(0, False), (2, False), (4, True)], [(0, False), (5, True)]]
+    assert OF.fragment_tokens(frags, lens) == 96 + 128 + 121 + 81
+    OF.check_fragments(frags, lens, par, 130)
+
+
+def test_fragments_are_valid_on_random_trees_and_workloads():
+    from oracle import fragments as OF
+    rng = np.random.default_rng(3)
+    for _ in range(100):
+        t = W.random_small_tree(rng, max_segments=12, max_len=30)
+        longest_path = max(sum(int(t.seg_len[a]) for a in OT.ancestors(t.parent, s) + [s])
+                           for s in range(t.num_segments))
+        cap = int(rng.integers(longest_path, longest_path * 3 + 1))
+        frags = OF.plan_fragments(t.seg_len, t.parent, cap)
+        OF.check_fragments(frags, t.seg_len, t.parent, cap)
+        assert OF.fragment_tokens(frags, t.seg_len) >= int(t.seg_len.sum())
+    for name in ("agent", "long"):
+        w = W.get(name)
+        t = w.tree
+        cap = 2 * max(sum(int(t.seg_len[a]) for a in OT.ancestors(t.parent, s) + [s]) for s in range(t.num_segments))
+        frags = OF.plan_fragments(t.seg_len, t.parent, cap)
+        OF.check_fragments(frags, t.seg_len, t.parent, cap)
+        assert len(frags) > 1
+
+
+def test_fragments_checker_catches_broken_covers():
+    from oracle import fragments as OF
+    lens, par = [64, 32, 48, 16, 9, 17], [-1, 0, 0, 2, 2, 0]
+    good = OF.plan_fragments(lens, par, 130)
+    bad_owner = [list(f) for f in good]
+    bad_owner[1][0] = (0, True)  # the root owned twice
+    bad_closure = [[(0, True), (1, True)], [(2, True), (3, True)], [(0, False), (2, False), (4, True)],
+                   [(0, False), (5, True)]]
+    for bad in (bad_owner, bad_closure):
+        with pytest.raises(AssertionError):
+            OF.check_fragments(bad, lens, par, 130)
+    with pytest.raises(AssertionError):
+        OF.check_fragments(good, lens, par, 120)
+
+
+def test_fragments_reject_a_root_path_above_the_cap():
+    from oracle import fragments as OF
+    with pytest.raises(ValueError):
+        OF.plan_fragments([64, 32, 48, 16, 9, 17], [-1, 0, 0, 2, 2, 0], 127)
