@@ -57,7 +57,8 @@ typedef enum {
   SP_ERR_TIMEOUT = -6,      /* (device) a bounded wait gave up */
   SP_ERR_INDEX_RANGE = -7,  /* (device) an edge index outside [0, T) */
   SP_ERR_WORKSPACE = -8,    /* workspace missing or smaller than required */
-  SP_ERR_NOT_UPLOADED = -9  /* the plan has no device copy (call sp_plan_upload) */
+  SP_ERR_NOT_UPLOADED = -9, /* the plan has no device copy (call sp_plan_upload) */
+  SP_ERR_CAP = -10          /* a root path is longer than the fragment token cap */
 } sp_status;
 
 /* Bits a kernel ORs into *d_status. */
@@ -133,6 +134,48 @@ SP_API int sp_plan_upload(sp_plan *plan, void *stream);
 /* Frees the plan (host and device copies).  NULL is ignored.  The caller
  * must make sure no queued kernel still reads the plan. */
 SP_API void sp_plan_destroy(sp_plan *plan);
+
+/* ---------------------------------------------------- bounded fragments
+ * A tree too large for one step is split into fragments of at most
+ * max_tokens physical tokens.  The trainer "bounds fragments and may repeat
+ * ancestors across fragments to honor the memory bound", and every sampled
+ * action keeps exactly one loss owner (issue #7386, "Describe the solution
+ * you'd like", last paragraph; "Additional context": 3,744,651 physical
+ * tokens before fragment duplication, 3,919,929 after).  The pages give no
+ * algorithm; this one visits segments in preorder and adds each, with the
+ * ancestors the current fragment lacks, while the fragment stays within the
+ * cap, else it starts the next fragment from the segment's root path.  Every
+ * fragment is closed under "parent of" (each segment comes with its whole
+ * root path, so its attention is the same as in the whole tree); the fragment
+ * that takes a segment in its own visit owns it (its tokens' outputs and
+ * loss); re-added ancestors are context only. */
+typedef struct sp_fragments sp_fragments;
+
+/* Read-only view of a fragment plan (valid until sp_fragment_destroy).
+ * Fragment f consists of entries [offsets[f], offsets[f+1]) in preorder:
+ *   seg[i]           the segment in the input tree
+ *   owned[i]         1 if fragment f owns that segment, 0 if it is context
+ *   local_parent[i]  the parent as an entry index within fragment f (-1: root)
+ *   local_start[i]   the segment's first token in fragment f's packed buffer
+ * so (local_start, seg_len[seg], local_parent, depth[seg]) is fragment f's
+ * own sp_tree_desc; tokens[f] is its length. */
+typedef struct {
+  int32_t num_fragments, num_entries;
+  int64_t physical_tokens;  /* tokens of the input tree */
+  int64_t fragment_tokens;  /* sum of tokens[f] (>= physical_tokens; the ratio is the duplication) */
+  const int32_t *offsets;   /* [num_fragments + 1] */
+  const int32_t *tokens;    /* [num_fragments] */
+  const int32_t *seg, *owned, *local_parent, *local_start; /* [num_entries] */
+} sp_fragment_info;
+
+/* Plans the fragments of a validated tree with at most max_tokens tokens
+ * each (host only).  Errors: SP_ERR_INVALID_ARG (null, max_tokens < 1),
+ * SP_ERR_INVALID_TREE, SP_ERR_CAP (a root path longer than max_tokens). */
+SP_API int sp_fragment_plan(const sp_tree_desc *tree, int64_t max_tokens, sp_fragments **out);
+/* Fills *info.  Errors: SP_ERR_INVALID_ARG. */
+SP_API int sp_fragment_view(const sp_fragments *frag, sp_fragment_info *info);
+/* Frees the fragment plan; NULL is ignored. */
+SP_API void sp_fragment_destroy(sp_fragments *frag);
 
 /* tree_attn_fwd -- O and LSE of shared-prefix tree attention.
  *   q   [T][Hq][D], k and v [T][Hkv][D], o [T][Hq][D]: dtype (bf16 or fp32)

@@ -26,6 +26,7 @@ SP_F32 = 1
 SP_DEV_INDEX_RANGE = 1
 SP_DEV_TIMEOUT = 2
 SP_DEV_BAD_PLAN = 4
+SP_ERR_CAP = -10
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is not built; run `python shared_prefix_causal_gb300/build.py` "
@@ -48,6 +49,12 @@ class _PlanInfo(ctypes.Structure):
                 ("max_ranges_per_tile", _i32), ("tiles", _i32p), ("ranges", _i32p), ("bwd", _i32p)]
 
 
+class _FragInfo(ctypes.Structure):
+    _fields_ = [("num_fragments", _i32), ("num_entries", _i32), ("physical_tokens", ctypes.c_int64),
+                ("fragment_tokens", ctypes.c_int64), ("offsets", _i32p), ("tokens", _i32p), ("seg", _i32p),
+                ("owned", _i32p), ("local_parent", _i32p), ("local_start", _i32p)]
+
+
 def _sig(name, res, args):
     f = getattr(_lib, name)
     f.restype = res
@@ -65,6 +72,10 @@ _c_ws = _sig("sp_tree_attn_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32, _
 _c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_frag_plan = _sig("sp_fragment_plan", ctypes.c_int,
+                    [ctypes.POINTER(_TreeDesc), ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)])
+_c_frag_view = _sig("sp_fragment_view", ctypes.c_int, [_vp, ctypes.POINTER(_FragInfo)])
+_c_frag_destroy = _sig("sp_fragment_destroy", None, [_vp])
 _c_bwd_det = _sig("sp_tree_attn_bwd_deterministic", ctypes.c_int,
                   [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                    _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
@@ -88,7 +99,8 @@ EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
-            "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic")
+            "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic", "sp_fragment_plan", "sp_fragment_view",
+            "sp_fragment_destroy")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -323,6 +335,44 @@ def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
 
 # ------------------------------------------------------------ conveniences
 # Thin allocating wrappers over the entry points above (torch.empty only).
+
+def sp_fragment_plan(seg_start, seg_len, parent, depth, max_tokens: int) -> dict:
+    """Bounded fragments of a tree: the sp_fragment_view tables as numpy arrays (the handle is freed)."""
+    arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.int32)) for a in (seg_start, seg_len, parent, depth)]
+    n = int(arrs[0].shape[0])
+    total = int(arrs[1].astype(np.int64).sum()) if n else 0
+    desc = _TreeDesc(n, total, *[a.ctypes.data_as(_i32p) for a in arrs])
+    h = ctypes.c_void_p()
+    _check(_c_frag_plan(ctypes.byref(desc), int(max_tokens), ctypes.byref(h)), "sp_fragment_plan")
+    try:
+        info = _FragInfo()
+        _check(_c_frag_view(h, ctypes.byref(info)), "sp_fragment_view")
+        nf, ne = info.num_fragments, info.num_entries
+
+        def arr(p, k):
+            return np.ctypeslib.as_array(p, shape=(k,)).copy() if k else np.zeros(0, dtype=np.int32)
+
+        return {"num_fragments": nf, "physical_tokens": int(info.physical_tokens),
+                "fragment_tokens": int(info.fragment_tokens), "offsets": arr(info.offsets, nf + 1),
+                "tokens": arr(info.tokens, nf), "seg": arr(info.seg, ne), "owned": arr(info.owned, ne),
+                "local_parent": arr(info.local_parent, ne), "local_start": arr(info.local_start, ne)}
+    finally:
+        _c_frag_destroy(h)
+
+
+def fragment_plan(tree, max_tokens: int) -> dict:
+    """sp_fragment_plan for any object with seg_start/seg_len/parent/depth arrays."""
+    return sp_fragment_plan(tree.seg_start, tree.seg_len, tree.parent, tree.depth, max_tokens)
+
+
+def fragment_tree(frag: dict, f: int, tree):
+    """Fragment f's own packed tree: (seg_start, seg_len, parent, depth, segments, owned)."""
+    a, b = int(frag["offsets"][f]), int(frag["offsets"][f + 1])
+    segs = frag["seg"][a:b]
+    return (frag["local_start"][a:b].copy(), np.asarray(tree.seg_len)[segs].astype(np.int32),
+            frag["local_parent"][a:b].copy(), np.asarray(tree.depth)[segs].astype(np.int32), segs.copy(),
+            frag["owned"][a:b].copy())
+
 
 def tree_plan(tree, tile_tokens: int, kv_block: int = 128, order: int = 0, upload: bool = True) -> Plan:
     """Plan from any object with seg_start/seg_len/parent/depth arrays."""

@@ -297,6 +297,7 @@ const char *sp_status_string(int status) {
     case SP_ERR_INDEX_RANGE: return "edge index out of range";
     case SP_ERR_WORKSPACE: return "workspace missing or too small";
     case SP_ERR_NOT_UPLOADED: return "plan not uploaded to the device";
+    case SP_ERR_CAP: return "a root path is longer than the fragment token cap";
     default: return "unknown status";
   }
 }

@@ -34,6 +34,9 @@ struct sp_plan {
 
 namespace spc {
 
+// Tree checks of sp_tree_desc (plan.cpp): SP_OK or SP_ERR_INVALID_TREE.
+// Expects num_segments >= 0 and non-null arrays when num_segments > 0.
+int validate_tree(const sp_tree_desc &tree);
 // Plan builder (plan.cpp).  Returns SP_OK or SP_ERR_INVALID_TREE/ARG.
 int build_plan(const sp_tree_desc &tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
                sp_plan &plan);

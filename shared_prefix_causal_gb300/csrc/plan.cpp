@@ -29,7 +29,7 @@ void push_merged(std::vector<Interval> &v, Interval x) {
     v.push_back(x);
 }
 
-int validate(const sp_tree_desc &t) {
+int validate_impl(const sp_tree_desc &t) {
   const int n = t.num_segments;
   int64_t pos = 0;
   for (int s = 0; s < n; ++s) {
@@ -55,6 +55,8 @@ int validate(const sp_tree_desc &t) {
 
 }  // namespace
 
+int validate_tree(const sp_tree_desc &t) { return validate_impl(t); }
+
 int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int32_t order,
                sp_plan &plan) {
   if (tile_tokens <= 0 || kv_block <= 0 || (order != 0 && order != 1)) return SP_ERR_INVALID_ARG;
@@ -63,7 +65,7 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
       (!t.seg_start || !t.seg_len || !t.parent || !t.depth))
     return SP_ERR_INVALID_ARG;
   if ((t.num_segments == 0) != (t.total_tokens == 0)) return SP_ERR_INVALID_TREE;
-  if (int rc = validate(t)) return rc;
+  if (int rc = validate_impl(t)) return rc;
 
   const int n = t.num_segments;
   plan.tile_tokens = tile_tokens;

@@ -151,3 +151,65 @@ def test_bench_traffic_is_null_when_kernel_sources_change(monkeypatch):
     monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent",
                         {"bwd_tc_kernel": (7.0, bench.sources_digest("bwd_tc_kernel"))})
     assert bench.measured_traffic("agent", "bwd_tc_kernel") == 7
+
+
+# ------------------------------------------------------------ bounded fragments
+
+def _oracle_frag_tables(tree, cap):
+    from oracle import fragments as OF
+    frags = OF.plan_fragments(tree.seg_len, tree.parent, cap)
+    seg = [a for f in frags for a, _ in f]
+    owned = [int(o) for f in frags for _, o in f]
+    offsets = np.cumsum([0] + [len(f) for f in frags])
+    return frags, np.array(seg), np.array(owned), offsets
+
+
+def _longest_path(tree):
+    from oracle import tree as OT
+    return max(sum(int(tree.seg_len[a]) for a in OT.ancestors(tree.parent, s) + [s])
+               for s in range(tree.num_segments))
+
+
+@pytest.mark.parametrize("name", ["tiny", "star", "forest", "agent", "long"])
+def test_fragment_plan_bit_exact_vs_oracle(name):
+    w = W.get(name)
+    lp = _longest_path(w.tree)
+    for cap in (lp, 2 * lp, w.T):
+        got = spc.fragment_plan(w.tree, cap)
+        frags, seg, owned, offsets = _oracle_frag_tables(w.tree, cap)
+        assert got["num_fragments"] == len(frags)
+        assert np.array_equal(got["offsets"], offsets)
+        assert np.array_equal(got["seg"], seg) and np.array_equal(got["owned"], owned)
+        assert got["fragment_tokens"] == sum(int(w.tree.seg_len[a]) for a in seg)
+        assert got["physical_tokens"] == w.T
+
+
+def test_fragment_plan_random_trees_and_fragment_trees_are_valid():
+    rng = np.random.default_rng(21)
+    for _ in range(150):
+        t = W.random_small_tree(rng, max_segments=14, max_len=40)
+        lp = _longest_path(t)
+        cap = int(rng.integers(lp, 3 * lp + 1))
+        got = spc.fragment_plan(t, cap)
+        _, seg, owned, offsets = _oracle_frag_tables(t, cap)
+        assert np.array_equal(got["seg"], seg) and np.array_equal(got["owned"], owned)
+        assert np.array_equal(got["offsets"], offsets)
+        for f in range(got["num_fragments"]):
+            start, ln, par, dep, segs, own = spc.fragment_tree(got, f, t)
+            assert int(ln.sum()) == int(got["tokens"][f]) <= cap
+            # a valid packed tree of its own: the planner accepts it
+            spc.sp_tree_plan(start, ln, par, dep, 4, 16, 0)
+
+
+def test_fragment_plan_rejections():
+    w = W.get("tiny")
+    with pytest.raises(RuntimeError, match="fragment token cap"):
+        spc.fragment_plan(w.tree, _longest_path(w.tree) - 1)
+    with pytest.raises(RuntimeError):
+        spc.fragment_plan(w.tree, 0)
+    bad_parent = np.array(w.tree.parent).copy()
+    bad_parent[3] = 4  # parent after the child: not a preorder
+    with pytest.raises(RuntimeError):
+        spc.sp_fragment_plan(w.tree.seg_start, w.tree.seg_len, bad_parent, w.tree.depth, 1000)
+    empty = spc.sp_fragment_plan([], [], [], [], 10)
+    assert empty["num_fragments"] == 0 and empty["fragment_tokens"] == 0

@@ -399,3 +399,46 @@ def test_edge_gather_bwd_fp32_empty_and_bad_index():
     bad, st = _gather_bwd(grad[:2].cuda(), torch.tensor([1, 10], dtype=torch.int32).cuda(), 10)
     assert st == spc.SP_DEV_INDEX_RANGE
     assert torch.equal(bad.cpu()[1], grad[0]) and (bad.cpu()[[0, 2, 3]] == 0).all()
+
+
+# ------------------------------------------------------------ bounded fragments
+
+@pytest.mark.parametrize("name,cap_factor", [("star", 1.0), ("agent", 2.0)])
+def test_fragments_reproduce_the_whole_tree(name, cap_factor):
+    """Run every bounded fragment on its own (dO zeroed on tokens the fragment does not own) and map
+    back: owned tokens' outputs equal the whole tree's, and the gradients summed over fragments equal
+    the whole tree's -- repeated context ancestors receive exactly their owned descendants' share."""
+    from oracle import tree as OT
+    w = W.get(name)
+    t = w.tree
+    longest = max(sum(int(t.seg_len[a]) for a in OT.ancestors(t.parent, s) + [s]) for s in range(t.num_segments))
+    frag = spc.fragment_plan(t, int(cap_factor * longest))
+    assert frag["num_fragments"] >= 3
+    x = W.draw_tensors(w, "bf16")
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    G = w.hq // w.hkv
+    plan = spc.tree_plan(t, 128 // G)
+    o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale)
+    dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale)
+    o_f = torch.zeros_like(o, dtype=torch.float32)
+    dq_f = torch.zeros_like(q, dtype=torch.float32)
+    dk_f = torch.zeros_like(k, dtype=torch.float32)
+    dv_f = torch.zeros_like(v, dtype=torch.float32)
+    for f in range(frag["num_fragments"]):
+        start, ln, par, dep, segs, own = spc.fragment_tree(frag, f, t)
+        idx = torch.cat([torch.arange(int(t.seg_start[s]), int(t.seg_start[s]) + int(t.seg_len[s])) for s in segs])
+        owned_tok = torch.cat([torch.full((int(t.seg_len[s]),), bool(o_)) for s, o_ in zip(segs, own)]).cuda()
+        idx = idx.cuda()
+        p = spc.tree_plan(W.Tree(start, ln, par, dep), 128 // G)
+        qf, kf, vf = q[idx].contiguous(), k[idx].contiguous(), v[idx].contiguous()
+        dof = (do[idx] * owned_tok[:, None, None].to(do.dtype)).contiguous()
+        of, lf = spc.tree_attn_fwd(p, qf, kf, vf, w.softmax_scale)
+        dqf, dkf, dvf = spc.tree_attn_bwd(p, qf, kf, vf, of, lf, dof, w.softmax_scale)
+        o_f[idx[owned_tok]] = of[owned_tok].float()
+        dq_f[idx[owned_tok]] = dqf[owned_tok].float()
+        dk_f.index_add_(0, idx, dkf.float())
+        dv_f.index_add_(0, idx, dvf.float())
+    torch.cuda.synchronize()
+    assert rel_l2(o_f.cpu().numpy(), o.float().cpu().numpy()) < 1e-2
+    for got, ref in ((dq_f, dq), (dk_f, dk), (dv_f, dv)):
+        assert rel_l2(got.cpu().numpy(), ref.float().cpu().numpy()) < 2.5e-2
