@@ -413,6 +413,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": e2e,
         "bwd_deterministic": det,
+        "fragments": fragment_summary(spc, w, args.fragment_cap),
         "lm_head": lm_head,
     }
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
@@ -424,6 +425,19 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+
+
+def fragment_summary(spc, w, cap: int):
+    """Bounded fragments of the workload's tree (host planner): count and token duplication."""
+    t0 = time.perf_counter()
+    try:
+        f = spc.fragment_plan(w.tree, cap)
+    except RuntimeError as e:
+        return {"cap": cap, "error": str(e)}
+    ms = (time.perf_counter() - t0) * 1e3
+    return {"cap": cap, "fragments": f["num_fragments"], "physical_tokens": f["physical_tokens"],
+            "fragment_tokens": f["fragment_tokens"],
+            "duplication": round(f["fragment_tokens"] / max(1, f["physical_tokens"]), 4), "plan_ms": round(ms, 3)}
 
 
 def run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status, dev, f_bwd,
@@ -581,6 +595,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-lm-head", action="store_true", help="skip the vocabulary-head measurement")
     ap.add_argument("--lm-vocab", type=int, default=W.LM_HEAD_VOCAB, help="vocabulary size of the vocabulary head")
+    ap.add_argument("--fragment-cap", type=int, default=32768, help="token cap of the bounded-fragment summary")
     ap.add_argument("--cpu-flops", type=float, default=6e11, help="fp64 flop budget of the CPU-baseline sample")
     ap.add_argument("--ref-flops", type=float, default=1.2e11, help="fp64 flop budget per reference step")
     ap.add_argument("--_oracle-child", dest="oracle_child", default=None, help=argparse.SUPPRESS)
