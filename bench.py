@@ -87,6 +87,20 @@ def measured_traffic(config: str, kernel: str):
     return int(entry[0])
 
 
+def tile_efficiency(spc, plan, G: int, pairs: int) -> dict:
+    """Useful pairs over the pairs the kernels compute (full 128-key blocks of 128-row tiles
+    forward; 64-row query blocks against 128-key blocks backward), per query head."""
+    v = spc.sp_plan_view(plan)
+    tt = int(v["tile_tokens"])
+    fwd = 0
+    for _, q0, q1, rb, rc in v["tiles"].tolist():
+        nb = sum((e - a + 127) // 128 for a, e in v["ranges"][rb:rb + rc].tolist())
+        fwd += nb * 128 * tt
+    tpb = 64 // G
+    bwd = sum(((q1 - q0 + tpb - 1) // tpb) * tpb * 128 for _, _, _, q0, q1 in v["bwd"].tolist())
+    return {"fwd": round(pairs / max(fwd, 1), 4), "bwd": round(pairs / max(bwd, 1), 4)}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -109,7 +123,7 @@ def _peak_value(peaks, *keys):
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -117,6 +131,11 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.window = None
+
+    def mark(self, begin: float, end: float):
+        """Wall-clock bounds of the timed region: only samples inside it are kept."""
+        self.window = (begin, end)
 
     def start(self):
         try:
@@ -125,7 +144,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
 
@@ -139,17 +158,25 @@ class ClockSampler:
             self.proc.kill()
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    clk, cmax = float(parts[2]), float(parts[3])
                 except ValueError:
                     continue
-                for n, val in zip(names, parts[5:9]):
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    ts = None  # unparsable timestamp: keep the sample
+                if self.window and ts is not None and not (self.window[0] - 0.05 <= ts <= self.window[1] + 0.05):
+                    continue
+                sm.append(clk)
+                smax.append(cmax)
+                for n, val in zip(names, parts[6:10]):
                     if val.lower().startswith("active"):
                         reasons.add(n)
         os.unlink(self.path)
@@ -315,6 +342,8 @@ def run_gpu(args):
         if evs:
             evs[3].record(stream)
 
+    clocks = ClockSampler(dev.index)
+    clocks.start()  # running before the timed region: nvidia-smi takes a moment to start sampling
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -322,11 +351,10 @@ def run_gpu(args):
         raise RuntimeError(f"device status {status.item()} during warm-up")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    clocks = ClockSampler(dev.index)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
+    wall0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -334,6 +362,7 @@ def run_gpu(args):
         step(evs[i])
     stop.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark(wall0, time.time())
     clk = clocks.stop()
     if ws > 1:
         torch.distributed.barrier()
@@ -354,11 +383,22 @@ def run_gpu(args):
     peaks, peak_src = load_peaks()
     p_burst = _peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
     p_sust = _peak_value(peaks, "bf16_tflops_sustained") or p_burst
+    p_hbm = _peak_value(peaks, "hbm_gbs")
     med_fwd, med_bwd = statistics.median(fwd_ms), statistics.median(bwd_ms)
     fwd_tflops = f_fwd / (med_fwd * 1e-3) / 1e12
     bwd_tflops = f_bwd / (med_bwd * 1e-3) / 1e12
     mean_bwd = statistics.mean(bwd_ms)
     mean_fwd = statistics.mean(fwd_ms)
+    # one cold-L2 step: a 256 MiB scrub written just before it
+    l2_bytes = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0))
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cold_ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    scrub.fill_(1)
+    step(cold_ev)
+    torch.cuda.synchronize(dev)
+    del scrub
+    cold = {"fwd_ms": round(cold_ev[0].elapsed_time(cold_ev[1]), 4),
+            "bwd_ms": round(cold_ev[1].elapsed_time(cold_ev[2]), 4), "scrub_bytes": 256 << 20}
     e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 and not args.no_e2e else None
     det = run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status, dev, f_bwd,
                                 p_burst)
@@ -384,15 +424,23 @@ def run_gpu(args):
         "config": {"workload": w.description, "tokens": T, "segments": w.tree.num_segments,
                    "q_heads": w.hq, "kv_heads": w.hkv, "head_dim": D, "useful_pairs_per_head": pairs,
                    "tile_tokens": 128 // G, "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU",
-                   "l2": "inputs larger than L2 (Q and dO %d MiB each); no flush" % (q.numel() * 2 >> 20)},
+                   "l2": "inputs larger than L2 (%d MiB here; Q and dO %d MiB each); no flush between steps"
+                         % (l2_bytes >> 20, q.numel() * 2 >> 20)},
         "tokens_per_s": round(ws * T / (ms_step * 1e-3), 1),
+        "tokens_per_s_fwd": round(ws * T / (med_fwd * 1e-3), 1),
+        "tokens_per_s_bwd": round(ws * T / (med_bwd * 1e-3), 1),
+        "tile_efficiency": tile_efficiency(spc, plan, G, pairs),
+        "cold_l2": cold,
         "fwd": {"ms": round(med_fwd, 4), "useful_tflops": round(fwd_tflops, 2),
                 "frac_of_peak": round(fwd_tflops / p_burst, 4) if p_burst else None},
         "bwd": {"ms": round(med_bwd, 4), "useful_tflops": round(bwd_tflops, 2),
                 "frac_of_peak": round(bwd_tflops / p_burst, 4) if p_burst else None},
         "edge_gather": {"ms": round(statistics.median(gat_ms), 4),
                         "gbs": round(2 * gathered.numel() * 2 / (statistics.median(gat_ms) * 1e-3) / 1e9, 1)
-                        if gathered is not None and statistics.median(gat_ms) > 0 else None},
+                        if gathered is not None and statistics.median(gat_ms) > 0 else None,
+                        "frac_of_hbm_peak": round(2 * gathered.numel() * 2 / (statistics.median(gat_ms) * 1e-3)
+                                                  / 1e9 / p_hbm, 4)
+                        if gathered is not None and statistics.median(gat_ms) > 0 and p_hbm else None},
         "frac_of_bf16_peak": round(value / ws / p_burst, 4) if p_burst else None,
         "plan_ms": round(plan_ms, 3),
         "roofline": {

@@ -442,3 +442,22 @@ def test_fragments_reproduce_the_whole_tree(name, cap_factor):
     assert rel_l2(o_f.cpu().numpy(), o.float().cpu().numpy()) < 1e-2
     for got, ref in ((dq_f, dq), (dk_f, dk), (dv_f, dv)):
         assert rel_l2(got.cpu().numpy(), ref.float().cpu().numpy()) < 2.5e-2
+
+
+@pytest.mark.parametrize("name", ["tiny", "star"])
+def test_sibling_permutation_gpu(name):
+    """Laying the tree out with siblings in another order and mapping back changes nothing beyond
+    the config tolerances (the pages' result is a function of the tree, not of the sibling order)."""
+    from test_oracle import _permute_siblings
+    w = W.get(name)
+    x = W.draw_tensors(w, "bf16")
+    _, out = run_gpu(w, "bf16", x=x)
+    rng = np.random.default_rng(31)
+    nt, perm = _permute_siblings(w.tree, rng)
+    inv = torch.from_numpy(np.argsort(perm))
+    w2 = W.Workload(w.name, w.description, nt, w.hq, w.hkv, w.head_dim, w.tensor_scale, w.seed, None, None)
+    x2 = {n: x[n][inv].contiguous() for n in ("q", "k", "v", "do")}
+    _, out2 = run_gpu(w2, "bf16", x=x2)
+    for n, tol in (("o", 1e-2), ("dq", 2.5e-2), ("dk", 2.5e-2), ("dv", 2.5e-2)):
+        assert rel_l2(out2[n][perm], out[n]) < tol, n
+    assert np.abs(out2["lse"][:, perm] - out["lse"]).max() < 5e-3
