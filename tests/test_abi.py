@@ -213,3 +213,54 @@ def test_fragment_plan_rejections():
         spc.sp_fragment_plan(w.tree.seg_start, w.tree.seg_len, bad_parent, w.tree.depth, 1000)
     empty = spc.sp_fragment_plan([], [], [], [], 10)
     assert empty["num_fragments"] == 0 and empty["fragment_tokens"] == 0
+
+
+def test_vocab_head_gather_bwd_and_deterministic_argument_checks():
+    """Status codes for the newer entry points; every case fails (or returns) before device work."""
+    fake = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    lp = spc._c_lmh
+    ws = spc.sp_edge_logprob_workspace_bytes(300, 1000)
+    assert ws >= 8 * 300 * 4 + 4 * 300
+    ok = lambda **kw: dict(dict(dtype=0, h=fake, E=300, Hd=128, w=fake, V=1000, y=fake, lp=fake, lse=fake,  # noqa
+                                ws=fake, wsb=ws), **kw)
+    call = lambda a: lp(a["dtype"], a["h"], a["E"], a["Hd"], a["w"], a["V"], a["y"], a["lp"], a["lse"],  # noqa
+                        a["ws"], a["wsb"], None, None)
+    assert call(ok(dtype=7)) == -2
+    assert call(ok(dtype=1)) == -3                    # fp32 inputs: not supported here
+    assert call(ok(E=-1)) == -2 and call(ok(V=0)) == -2 and call(ok(Hd=0)) == -2
+    assert call(ok(Hd=12)) == -3                      # rows not a multiple of 16 bytes
+    assert call(ok(E=0)) == 0                         # no actions: nothing to do
+    assert call(ok(y=None)) == -2
+    assert call(ok(h=mis)) == -4
+    assert call(ok(wsb=ws - 1)) == -8
+    assert call(ok(ws=ctypes.c_void_p((1 << 20) + 16))) == -4  # workspace not 256-byte aligned
+    lb = spc._c_lmh_bwd
+    wsb = spc.sp_edge_logprob_bwd_workspace_bytes(300, 1000)
+    assert wsb >= 2 * 300 * 1000
+    bcall = lambda E=300, Hd=128, V=1000, dh=fake, dw=fake, b=wsb, h=fake: lb(  # noqa
+        0, h, E, Hd, fake, V, fake, fake, fake, dh, dw, fake, b, None, None)
+    assert bcall(V=1004) == -3                        # V % 8
+    assert bcall(dh=None, dw=None) == 0               # nothing requested
+    assert bcall(E=0, dw=None) == 0                   # no actions, no weight gradient requested
+    assert bcall(b=wsb - 1) == -8
+    assert bcall(h=mis) == -4
+    assert spc.sp_edge_logprob_bwd_workspace_bytes(-1, 8) == 0
+    gb = spc._c_gather_bwd
+    gws = spc.sp_edge_gather_bwd_workspace_bytes(186, 8)
+    assert gb(0, fake, 8, 256, fake, 0, fake, fake, gws, None, None) == 0       # T == 0
+    assert gb(0, fake, 8, 12, fake, 186, fake, fake, gws, None, None) == -3     # hidden_dim % 8
+    assert gb(0, fake, -1, 256, fake, 186, fake, fake, gws, None, None) == -2
+    assert gb(0, fake, 8, 256, fake, 186, fake, fake, gws - 1, None, None) == -8
+    assert gb(0, fake, 8, 256, fake, 186, mis, fake, gws, None, None) == -4
+    assert gb(5, fake, 8, 256, fake, 186, fake, fake, gws, None, None) == -3
+    t = W.tiny().tree
+    p = spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 64, 128, 0)
+    d = spc._c_bwd_det
+    assert d(p.handle, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, None, 0, 186, 2, 2, 64, 0.125,
+             None, None) == -8
+    assert d(p.handle, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 186, 2, 2, 64,
+             0.125, None, None) == -9
+    assert d(p.handle, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 186, 2, 2, 96,
+             0.125, None, None) == -3
+    assert "cap" in spc.sp_status_string(spc.SP_ERR_CAP)
