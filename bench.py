@@ -558,54 +558,92 @@ def run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust):
 
 
 def run_e2e(args, spc, w, x, dev, flops_per_step):
-    """Same metric through the public API from pinned host buffers: each step
-    plans and uploads the tree, copies the inputs in, runs forward, backward
-    and the gather, and copies dQ, dK, dV and the gathered rows out."""
+    """Same metric through the public API from pinned host buffers.  Every step
+    plans the tree and uploads the plan, copies that step's inputs in, runs
+    forward, backward and the gather, and copies dQ, dK, dV and the gathered
+    rows out.  Steps are pipelined the way a training loop would run them: two
+    device buffer sets, inputs copied on one stream and results on another
+    while the previous step computes (the copies of a step still precede and
+    follow its own compute)."""
     import torch
     G = w.hq // w.hkv
     host = {n: t.pin_memory() for n, t in x.items()}
     idx_h = torch.from_numpy(w.edge_idx).pin_memory() if w.edge_idx is not None else None
-    dvc = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    idx_d = torch.empty_like(idx_h, device=dev) if idx_h is not None else None
-    outs_h = {n: torch.empty_like(host[src]).pin_memory() for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
-    g_h = torch.empty((idx_h.shape[0], host["hidden"].shape[1]), dtype=torch.bfloat16).pin_memory() \
-        if idx_h is not None and "hidden" in host else None
+    nbuf = 2
+    sets = []
+    for _ in range(nbuf):
+        d = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+        d["idx"] = torch.empty_like(idx_h, device=dev) if idx_h is not None else None
+        d["ws"] = spc.bwd_workspace(d["q"])
+        d["o"] = torch.empty_like(d["q"])
+        d["lse"] = torch.empty((w.hq, w.T), dtype=torch.float32, device=dev)
+        d["dq"], d["dk"], d["dv"] = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+        d["g"] = torch.empty((idx_h.shape[0], host["hidden"].shape[1]), dtype=torch.bfloat16, device=dev) \
+            if idx_h is not None and "hidden" in host else None
+        d["out_h"] = {n: torch.empty_like(d[n], device="cpu").pin_memory() for n in ("dq", "dk", "dv")}
+        d["g_h"] = torch.empty_like(d["g"], device="cpu").pin_memory() if d["g"] is not None else None
+        sets.append(d)
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
         (idx_h.numel() * 4 if idx_h is not None else 0)
-    d2h = sum(t.numel() * t.element_size() for t in outs_h.values()) + \
-        (g_h.numel() * 2 if g_h is not None else 0)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0]["out_h"].values()) + \
+        (sets[0]["g_h"].numel() * 2 if sets[0]["g_h"] is not None else 0)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    ws_buf = spc.bwd_workspace(dvc["q"])
+    comp = torch.cuda.current_stream(dev)
+    s_in, s_out, s_plan = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev_comp = [torch.cuda.Event() for _ in range(nbuf)]   # compute of the set's last step done
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]    # results of the set's last step copied out
+    for b in range(nbuf):
+        ev_comp[b].record(comp)
+        ev_out[b].record(comp)
+    plans = []
 
-    def step():
-        plan = spc.tree_plan(w.tree, 128 // G, 128, 0)
-        for n in host:
-            dvc[n].copy_(host[n], non_blocking=True)
-        if idx_h is not None:
-            idx_d.copy_(idx_h, non_blocking=True)
-        q, k, v, do = dvc["q"], dvc["k"], dvc["v"], dvc["do"]
-        o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale, status)
-        dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, workspace=ws_buf,
-                                       d_status=status)
-        outs_h["dq"].copy_(dq, non_blocking=True)
-        outs_h["dk"].copy_(dk, non_blocking=True)
-        outs_h["dv"].copy_(dv, non_blocking=True)
-        if g_h is not None:
-            g_h.copy_(spc.edge_gather(dvc["hidden"], idx_d, status), non_blocking=True)
-        torch.cuda.synchronize(dev)
-        plan.close()
+    def step(i):
+        d = sets[i % nbuf]
+        b = i % nbuf
+        plan = spc.tree_plan(w.tree, 128 // G, 128, 0, upload=False)
+        spc.sp_plan_upload(plan, s_plan)  # its own stream: the upload's sync waits for the plan only
+        plans.append(plan)
+        s_in.wait_event(ev_comp[b])  # the set's inputs are free once its previous step has computed
+        with torch.cuda.stream(s_in):
+            for n in host:
+                d[n].copy_(host[n], non_blocking=True)
+            if idx_h is not None:
+                d["idx"].copy_(idx_h, non_blocking=True)
+        ev_in = torch.cuda.Event()
+        ev_in.record(s_in)
+        comp.wait_event(ev_in)
+        comp.wait_event(ev_out[b])  # the set's result buffers have been copied out
+        spc.sp_tree_attn_fwd(plan, d["q"], d["k"], d["v"], d["o"], d["lse"], w.softmax_scale, status)
+        spc.sp_tree_attn_bwd(plan, d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"], d["dv"],
+                             d["ws"], w.softmax_scale, status)
+        if d["g"] is not None:
+            spc.sp_edge_gather(d["hidden"], d["idx"], d["g"], status)
+        ev_comp[b].record(comp)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            for n in ("dq", "dk", "dv"):
+                d["out_h"][n].copy_(d[n], non_blocking=True)
+            if d["g"] is not None:
+                d["g_h"].copy_(d["g"], non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(max(1, args.warmup)):
-        step()
-    n = max(1, min(args.steps, 5))
+    for i in range(max(1, args.warmup)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    n = max(2, min(args.steps, 10))
     t0 = time.perf_counter()
-    for _ in range(n):
-        step()
+    for i in range(n):
+        step(i)
+    torch.cuda.synchronize(dev)
     el = (time.perf_counter() - t0) / n
+    for p_ in plans:
+        p_.close()
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the end-to-end run")
     return {"value": round(flops_per_step / el / 1e12, 3), "unit": UNIT, "ms_per_step": round(el * 1e3, 3),
             "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipelined": "2 buffer sets; inputs in on one stream, results out on another, next step's copies "
+                         "overlapping this step's compute",
             "includes": "tree_plan + plan upload + H2D of q,k,v,dO,hidden,idx + fwd + bwd + edge_gather + "
                         "D2H of dQ,dK,dV and gathered rows"}
 
