@@ -11,18 +11,21 @@
 // accumulators; nothing is scattered.  Per query block, FlashAttention-style
 // recomputation from the saved LSE:
 //   S^T  = K Q^T          dP^T = V dO^T                    (tensor cores)
-//   P^T  = exp(S^T - LSE) dS^T = P^T (dP^T - Delta)        (4 softmax warps)
+//   P^T  = exp(S^T - LSE) dS^T = P^T (dP^T - Delta)        (8 warps)
 //   dV  += P^T dO         dK  += dS^T Q                    (tensor cores)
-//   dQ^T = K^T dS^T  -> fp32 atomics into the dQ workspace (4 dQ warps)
-// dQ is formed transposed (M = head_dim) so it needs only 64 TMEM columns per
-// buffer: S^T, dP^T, two dQ^T buffers, dK and dV fill the 512 columns.
+//   dQ^T = K^T dS^T  -> fp32 atomics into the dQ workspace (4 of the 8 warps)
+// dQ is formed transposed (M = head_dim) so it needs only 64 TMEM columns:
+// S^T, dP^T, dQ^T, two P^T buffers, dK and dV fill the 512 columns.
 //
-// Roles: warps 0-3 softmax and the dK/dV epilogue (TMEM lane = key row),
-// warps 4-7 dQ readout (TMEM lane = head-dim index), warp 8 TMA producer
-// (Q, dO, and the per-column LSE / Delta staged by the whole warp), warp 9
-// the single-thread MMA issuer.  The MMA issue order is software pipelined:
-// S^T and dP^T of block j are issued before dV, dK and dQ^T of block j-1, so
-// the softmax of block j overlaps the second half of block j-1.
+// Roles: warps 0-7 form P^T and dS^T, warpgroup h taking query columns
+// [32h, 32h + 32) of every key row (TMEM lane = key row); warps 4-7 also read
+// dQ^T out (TMEM lane = head-dim index); in the epilogue warps 0-3 store dK
+// and warps 4-7 dV.  Warp 8: TMA producer (Q, dO, and the per-column LSE /
+// Delta staged by the whole warp); warp 9: the single-thread MMA issuer.  The
+// MMA issue order is software pipelined: S^T and dP^T of block j are issued
+// as soon as block j-1's S^T and dP^T have been read, before dV, dK and dQ^T
+// of block j-1, so the elementwise work of block j overlaps the second half of
+// block j-1.
 //
 // Companion kernels: bwd_pre (Delta = rowsum(dO * O) and zeroing the fp32 dQ
 // workspace) and dq_convert (scale and round dQ to bf16).
@@ -131,7 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
-      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1 || i == B_DQ_FREE) cnt = 128;
+      if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1) cnt = 256;  // warps 0-7, every thread
+      if (i == B_DQ_FREE) cnt = 128;                                       // warps 4-7
       mbar_init(ctl.bar(i), cnt);
     }
     *ctl.abort = 0;
@@ -282,126 +286,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(ctl.bar(B_FINAL));
       ctl.drain(B_FINAL, 0);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------- softmax + dK/dV epilogue
-    const int r = threadIdx.x;  // key row = TMEM lane
-    const uint32_t lane_base = uint32_t(32 * warp) << 16;
+  } else {
+    // ------------------------------ P^T, dS^T (+ dQ readout, dK/dV epilogue)
+    // Two warpgroups split each 64-query block by columns: group h (warps
+    // 4h..4h+3) handles query columns [32h, 32h + 32) of every key row (thread
+    // = key row = TMEM lane).  Both load their S^T and dP^T columns at once, so
+    // S_FREE (and the next block's S^T/dP^T products) follows right away.
+    // Group 1 also reads block j-1's dQ^T out of TMEM and adds it into the fp32
+    // workspace; in the epilogue group 0 stores dK and group 1 dV.
+    const int h = warp >> 2;
+    const int r = threadIdx.x & 127;  // key row = TMEM lane
+    const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
     const int key = k0 + r;
     const bool kvalid = key < k1;
     const float sl2 = s.scale * kLog2e;
     bool ok = true;
-    for (int j = 0; j < nq; ++j) {
-      const int st = j % kStages;
-      const int qt = q_of(j);
-      const float *stat = reinterpret_cast<const float *>(smem + L::STAGE + st * L::STAGE_BYTES + L::STAT_OFF);
-      if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j / kStages) & 1))) break;
-      if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
-      tc_fence_after();
-      const int pb = j & 1;
-      const uint32_t prow = sbase + L::PS + pb * L::PS_BYTES + r * 128;
-      const bool nomask = qt + tpb <= qe && qt >= k1 - 1;
-      const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
-      const int ql = qe - qt;   // tokens of this block inside the query run
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {  // 32 query columns at a time
-        uint32_t us[32], ud[32];
-        tmem_ld32x2(tmem + lane_base + T_S + 32 * h, tmem + lane_base + T_DP + 32 * h, us, ud);
-        if (h == 1) {
-          tc_fence_before();
-          mbar_arrive(ctl.bar(B_S_FREE));
-        }
-        // this half's -LSE (log2) and -Delta, as float4 shared loads
-        float nl2[32], ndl[32];
-        const float4 *st4 = reinterpret_cast<const float4 *>(stat);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const float4 a = st4[8 * h + q4], b = st4[16 + 8 * h + q4];
-          nl2[4 * q4] = a.x, nl2[4 * q4 + 1] = a.y, nl2[4 * q4 + 2] = a.z, nl2[4 * q4 + 3] = a.w;
-          ndl[4 * q4] = b.x, ndl[4 * q4 + 1] = b.y, ndl[4 * q4 + 2] = b.z, ndl[4 * q4 + 3] = b.w;
-        }
-        // phases: exponents (masked to -inf), all exp2 back to back, products;
-        // paired fp32 instructions where the columns need no test
-        float pv[32], dsv[32];
-        if (nomask && kvalid) {  // two loops: a per-column test inside one loop is far slower
-#pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            ffma2(pv[i], pv[i + 1], __uint_as_float(us[i]), __uint_as_float(us[i + 1]), sl2, sl2, nl2[i],
-                  nl2[i + 1]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 32 * h + i;
-            const bool vis = kvalid && c / G < ql && kq <= c / G;
-            pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, nl2[i]) : -INFINITY;
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float t0, t1;
-          fadd2(t0, t1, __uint_as_float(ud[i]), __uint_as_float(ud[i + 1]), ndl[i], ndl[i + 1]);
-          fmul2(dsv[i], dsv[i + 1], pv[i], pv[i + 1], t0, t1);
-        }
-        if (h == 0 && !(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;  // block j-2's MMAs done
-        {  // P^T: 32 query columns as 16 bf16 pairs into this row's TMEM lane
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
-          tmem_st16(tmem + lane_base + T_P + 32 * pb + 16 * h, pk);
-        }
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {  // dS^T: K-major, 128-byte swizzle
-          const int u8 = 4 * h + u4;
-          const float *y = dsv + 8 * u4;
-          const uint32_t off = (u8 ^ (r & 7)) << 4;
-          st_shared_v4(prow + off, pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
-                       pack_bf16(y[6], y[7]));
-        }
-      }
-      if (!ok) break;
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(ctl.bar(B_P_FULL + pb));
-    }
-    if (ok && ctl.wait_warp(B_FINAL, 0)) {
-      tc_fence_after();
-      const float sc = s.scale;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // 0: dK (scaled), 1: dV
-        __nv_bfloat16 *dst = (half == 0 ? dk : dv) + (size_t(key) * s.Hkv + g) * D;
-        const float mul = half == 0 ? sc : 1.f;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(tmem + lane_base + T_DK + half * D + 32 * c, u);
-          if (kvalid) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(u[i]) * mul, __uint_as_float(u[i + 1]) * mul);
-              w.y = pack_bf16(__uint_as_float(u[i + 2]) * mul, __uint_as_float(u[i + 3]) * mul);
-              w.z = pack_bf16(__uint_as_float(u[i + 4]) * mul, __uint_as_float(u[i + 5]) * mul);
-              w.w = pack_bf16(__uint_as_float(u[i + 6]) * mul, __uint_as_float(u[i + 7]) * mul);
-              *reinterpret_cast<uint4 *>(dst + 32 * c + i) = w;
-            }
-          }
-        }
-      }
-    }
-  } else if constexpr (kDQ) {
-    // ------------------------------------------------------- dQ readout
-    const int d = 32 * (warp - 4) + lane;  // TMEM lane = head-dim index
-    const uint32_t lane_base = uint32_t(32 * (warp - 4)) << 16;
-    for (int j = 0; j < nq; ++j) {
-      const int qt = q_of(j);
-      if (!ctl.wait_warp(B_DQ_FULL, j & 1)) break;
+    // dQ^T of block m: TMEM lane d = head-dim index, 64 query columns; one
+    // fp32 atomic add per (column, d) into the workspace row of that query
+    auto dq_readout = [&](int m) -> bool {
+      const int qt = q_of(m);
+      if (!ctl.wait_warp(B_DQ_FULL, m & 1)) return false;
       tc_fence_after();
       uint32_t u0[32], u1[32];
       tmem_ld32x2(tmem + lane_base + T_DQ, tmem + lane_base + T_DQ + 32, u0, u1);
       tc_fence_before();
       mbar_arrive(ctl.bar(B_DQ_FREE));
+      const int d = r;
       if (d < D) {
         // query row c is token qt + c / G, head g * G + c % G
         float *base = dqacc + (size_t(qt) * Hq + g * G) * D + d;
@@ -420,6 +330,104 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 32; c < 64; ++c)
             if (c / G < ql) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u1[c - 32]));
+        }
+      }
+      return true;
+    };
+    for (int j = 0; j < nq; ++j) {
+      const int st = j % kStages;
+      const int qt = q_of(j);
+      const float *stat = reinterpret_cast<const float *>(smem + L::STAGE + st * L::STAGE_BYTES + L::STAT_OFF);
+      if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j / kStages) & 1))) break;
+      if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
+      tc_fence_after();
+      const int pb = j & 1;
+      const uint32_t prow = sbase + L::PS + pb * L::PS_BYTES + r * 128;
+      const bool nomask = qt + tpb <= qe && qt >= k1 - 1;
+      const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
+      const int ql = qe - qt;   // tokens of this block inside the query run
+      uint32_t us[32], ud[32];
+      tmem_ld32x2(tmem + lane_base + T_S + 32 * h, tmem + lane_base + T_DP + 32 * h, us, ud);
+      tc_fence_before();
+      mbar_arrive(ctl.bar(B_S_FREE));
+      // this group's -LSE (log2) and -Delta, as float4 shared loads
+      float nl2[32], ndl[32];
+      const float4 *st4 = reinterpret_cast<const float4 *>(stat);
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 a = st4[8 * h + q4], b = st4[16 + 8 * h + q4];
+        nl2[4 * q4] = a.x, nl2[4 * q4 + 1] = a.y, nl2[4 * q4 + 2] = a.z, nl2[4 * q4 + 3] = a.w;
+        ndl[4 * q4] = b.x, ndl[4 * q4 + 1] = b.y, ndl[4 * q4 + 2] = b.z, ndl[4 * q4 + 3] = b.w;
+      }
+      // phases: exponents (masked to -inf), all exp2 back to back, products;
+      // paired fp32 instructions where the columns need no test
+      float pv[32], dsv[32];
+      if (nomask && kvalid) {  // two loops: a per-column test inside one loop is far slower
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+          ffma2(pv[i], pv[i + 1], __uint_as_float(us[i]), __uint_as_float(us[i + 1]), sl2, sl2, nl2[i],
+                nl2[i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 32 * h + i;
+          const bool vis = kvalid && c / G < ql && kq <= c / G;
+          pv[i] = vis ? fmaf(__uint_as_float(us[i]), sl2, nl2[i]) : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        float t0, t1;
+        fadd2(t0, t1, __uint_as_float(ud[i]), __uint_as_float(ud[i + 1]), ndl[i], ndl[i + 1]);
+        fmul2(dsv[i], dsv[i + 1], pv[i], pv[i + 1], t0, t1);
+      }
+      if (!(ok = ctl.wait_warp(B_P_FREE + pb, ((j >> 1) & 1) ^ 1))) break;  // block j-2's MMAs done
+      {  // P^T: this group's 32 query columns as 16 bf16 pairs into this row's TMEM lane
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(pv[2 * i], pv[2 * i + 1]);
+        tmem_st16(tmem + lane_base + T_P + 32 * pb + 16 * h, pk);
+      }
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {  // dS^T: K-major, 128-byte swizzle
+        const int u8 = 4 * h + u4;
+        const float *y = dsv + 8 * u4;
+        const uint32_t off = (u8 ^ (r & 7)) << 4;
+        st_shared_v4(prow + off, pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]),
+                     pack_bf16(y[6], y[7]));
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ctl.bar(B_P_FULL + pb));
+      if constexpr (kDQ) {
+        if (h == 1 && j >= 1 && !(ok = dq_readout(j - 1))) break;
+      }
+    }
+    if constexpr (kDQ) {
+      if (ok && h == 1 && nq >= 1) ok = dq_readout(nq - 1);
+    }
+    if (ok && ctl.wait_warp(B_FINAL, 0)) {
+      tc_fence_after();
+      // group 0: dK (scaled); group 1: dV
+      __nv_bfloat16 *dst = (h == 0 ? dk : dv) + (size_t(key) * s.Hkv + g) * D;
+      const float mul = h == 0 ? s.scale : 1.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem + lane_base + T_DK + h * D + 32 * c, u);
+        if (kvalid) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(u[i]) * mul, __uint_as_float(u[i + 1]) * mul);
+            w.y = pack_bf16(__uint_as_float(u[i + 2]) * mul, __uint_as_float(u[i + 3]) * mul);
+            w.z = pack_bf16(__uint_as_float(u[i + 4]) * mul, __uint_as_float(u[i + 5]) * mul);
+            w.w = pack_bf16(__uint_as_float(u[i + 6]) * mul, __uint_as_float(u[i + 7]) * mul);
+            *reinterpret_cast<uint4 *>(dst + 32 * c + i) = w;
+          }
         }
       }
     }
