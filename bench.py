@@ -48,10 +48,10 @@ TRAFFIC_SOURCES = {
     "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
 }
 MEASURED_TRAFFIC = {
-    "agent": {"fwd_tc_kernel": (813.67e6 + 511.32e6, "5ebdf652e2c4eaed"),
-              "bwd_tc_kernel": (13.20e9 + 6.73e9, "af69ca8547df25bb")},
-    "star": {"fwd_tc_kernel": (94.39e6 + 27.56e6, "5ebdf652e2c4eaed"),
-             "bwd_tc_kernel": (331.91e6 + 132.75e6, "af69ca8547df25bb")},
+    "agent": {"fwd_tc_kernel": (813.75e6 + 510.94e6, "068960eb1a442da3"),
+              "bwd_tc_kernel": (16.64e9 + 8.42e9, "01d9ed31dcd02ef2")},
+    "star": {"fwd_tc_kernel": (94.39e6 + 27.93e6, "068960eb1a442da3"),
+             "bwd_tc_kernel": (333.02e6 + 131.47e6, "01d9ed31dcd02ef2")},
 }
 
 
