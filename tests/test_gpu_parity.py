@@ -461,3 +461,18 @@ def test_sibling_permutation_gpu(name):
     for n, tol in (("o", 1e-2), ("dq", 2.5e-2), ("dk", 2.5e-2), ("dv", 2.5e-2)):
         assert rel_l2(out2[n][perm], out[n]) < tol, n
     assert np.abs(out2["lse"][:, perm] - out["lse"]).max() < 5e-3
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 2, 128), (4, 2, 64), (8, 1, 64), (2, 2, 128)])
+def test_gqa_and_head_dim_sweep(hq, hkv, d):
+    """Every GQA ratio and head_dim the kernels instantiate, default and deterministic backward."""
+    rng = np.random.default_rng(hq * 100 + hkv * 10 + d)
+    tr = W.random_small_tree(rng, max_segments=20, max_len=300)
+    w = W.Workload("sweep", "", tr, hq, hkv, d, 0.5, 17, None, None)
+    x = W.draw_tensors(w, "bf16")
+    _, out = run_gpu(w, "bf16", x=x)
+    check_full(w, x, out, "bf16")
+    _, out_det = run_gpu(w, "bf16", x=x, deterministic=True)
+    check_full(w, x, out_det, "bf16")
+    for n in ("dk", "dv"):
+        assert np.array_equal(out[n], out_det[n]), n
