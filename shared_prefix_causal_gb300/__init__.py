@@ -374,6 +374,20 @@ def fragment_tree(frag: dict, f: int, tree):
             frag["owned"][a:b].copy())
 
 
+def fragment_tokens(frag: dict, f: int, tree):
+    """(token index [n], owned [n] bool) of fragment f: row i of the fragment's packed buffer is row
+    token_index[i] of the whole tree's; owned marks the tokens whose outputs and loss this fragment owns."""
+    a, b = int(frag["offsets"][f]), int(frag["offsets"][f + 1])
+    idx, own = [], []
+    for s_, o_ in zip(frag["seg"][a:b], frag["owned"][a:b]):
+        start, n = int(tree.seg_start[s_]), int(tree.seg_len[s_])
+        idx.append(np.arange(start, start + n, dtype=np.int64))
+        own.append(np.full(n, bool(o_)))
+    if not idx:
+        return np.zeros(0, dtype=np.int64), np.zeros(0, dtype=bool)
+    return np.concatenate(idx), np.concatenate(own)
+
+
 def tree_plan(tree, tile_tokens: int, kv_block: int = 128, order: int = 0, upload: bool = True) -> Plan:
     """Plan from any object with seg_start/seg_len/parent/depth arrays."""
     p = sp_tree_plan(tree.seg_start, tree.seg_len, tree.parent, tree.depth, tile_tokens, kv_block, order)

@@ -264,3 +264,18 @@ def test_vocab_head_gather_bwd_and_deterministic_argument_checks():
     assert d(p.handle, 0, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake, 1 << 30, 186, 2, 2, 96,
              0.125, None, None) == -3
     assert "cap" in spc.sp_status_string(spc.SP_ERR_CAP)
+
+
+def test_fragment_tokens_index_the_whole_tree():
+    w = W.get("star")
+    frag = spc.fragment_plan(w.tree, 3034)
+    owned_total = np.zeros(w.T, dtype=np.int64)
+    for f in range(frag["num_fragments"]):
+        idx, own = spc.fragment_tokens(frag, f, w.tree)
+        assert len(idx) == int(frag["tokens"][f]) and len(set(idx.tolist())) == len(idx)
+        start, ln, par, dep, segs, _ = spc.fragment_tree(frag, f, w.tree)
+        # the fragment's packed layout maps segment by segment onto the tree's tokens
+        for s_, st_ in zip(segs, start):
+            assert idx[st_] == int(w.tree.seg_start[s_])
+        np.add.at(owned_total, idx[own], 1)
+    assert (owned_total == 1).all()  # every token owned exactly once

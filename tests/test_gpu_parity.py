@@ -426,9 +426,8 @@ def test_fragments_reproduce_the_whole_tree(name, cap_factor):
     dv_f = torch.zeros_like(v, dtype=torch.float32)
     for f in range(frag["num_fragments"]):
         start, ln, par, dep, segs, own = spc.fragment_tree(frag, f, t)
-        idx = torch.cat([torch.arange(int(t.seg_start[s]), int(t.seg_start[s]) + int(t.seg_len[s])) for s in segs])
-        owned_tok = torch.cat([torch.full((int(t.seg_len[s]),), bool(o_)) for s, o_ in zip(segs, own)]).cuda()
-        idx = idx.cuda()
+        idx_np, owned_np = spc.fragment_tokens(frag, f, t)
+        idx, owned_tok = torch.from_numpy(idx_np).cuda(), torch.from_numpy(owned_np).cuda()
         p = spc.tree_plan(W.Tree(start, ln, par, dep), 128 // G)
         qf, kf, vf = q[idx].contiguous(), k[idx].contiguous(), v[idx].contiguous()
         dof = (do[idx] * owned_tok[:, None, None].to(do.dtype)).contiguous()
