@@ -590,6 +590,7 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     comp = torch.cuda.current_stream(dev)
     s_in, s_out, s_plan = (torch.cuda.Stream(device=dev) for _ in range(3))
+    plan_buf = [None] * nbuf  # per buffer set: the device buffer its steps' plans are uploaded into
     ev_comp = [torch.cuda.Event() for _ in range(nbuf)]   # compute of the set's last step done
     ev_out = [torch.cuda.Event() for _ in range(nbuf)]    # results of the set's last step copied out
     for b in range(nbuf):
@@ -601,7 +602,16 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         d = sets[i % nbuf]
         b = i % nbuf
         plan = spc.tree_plan(w.tree, 128 // G, 128, 0, upload=False)
-        spc.sp_plan_upload(plan, s_plan)  # its own stream: the upload's sync waits for the plan only
+        need = spc.sp_plan_device_bytes(plan)
+        if plan_buf[b] is None or plan_buf[b].numel() < need:
+            plan_buf[b] = torch.empty(2 * need, dtype=torch.uint8, device=dev)
+        # the set's buffer is free once its previous step (two back) has computed; the upload goes on an
+        # idle stream of its own (a copy from pageable host memory queued behind busy work would stall)
+        ev_comp[b].synchronize()
+        spc.sp_plan_upload_to(plan, plan_buf[b], s_plan)
+        ev_plan = torch.cuda.Event()
+        ev_plan.record(s_plan)
+        comp.wait_event(ev_plan)
         plans.append(plan)
         s_in.wait_event(ev_comp[b])  # the set's inputs are free once its previous step has computed
         with torch.cuda.stream(s_in):
@@ -643,7 +653,7 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
     return {"value": round(flops_per_step / el / 1e12, 3), "unit": UNIT, "ms_per_step": round(el * 1e3, 3),
             "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "pipelined": "2 buffer sets; inputs in on one stream, results out on another, next step's copies "
-                         "overlapping this step's compute",
+                         "overlapping this step's compute; each step's plan uploaded into a reused device buffer",
             "includes": "tree_plan + plan upload + H2D of q,k,v,dO,hidden,idx + fwd + bwd + edge_gather + "
                         "D2H of dQ,dK,dV and gathered rows"}
 

@@ -131,8 +131,25 @@ SP_API int sp_plan_view(const sp_plan *plan, sp_plan_info *info);
  * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA. */
 SP_API int sp_plan_upload(sp_plan *plan, void *stream);
 
-/* Frees the plan (host and device copies).  NULL is ignored.  The caller
- * must make sure no queued kernel still reads the plan. */
+/* Bytes of device memory the plan's tables take (for sp_plan_upload_to);
+ * 0 for a NULL plan. */
+SP_API size_t sp_plan_device_bytes(sp_plan *plan);
+
+/* sp_plan_upload into caller-owned device memory: no allocation and no
+ * synchronisation.  The tables are copied on `stream` (the host copies are
+ * staged before the call returns), so kernels launched on the same stream
+ * afterwards see them; the caller keeps the buffer alive, and unmodified,
+ * while any kernel using the plan may run, and frees it (sp_plan_destroy
+ * does not).  A training loop can plan every step without device
+ * allocations.  Repeat calls, or a call after sp_plan_upload, are no-ops.
+ *   device_buffer  256-byte aligned, at least sp_plan_device_bytes(plan) bytes.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_ALIGNMENT, SP_ERR_WORKSPACE (too small),
+ * SP_ERR_CUDA. */
+SP_API int sp_plan_upload_to(sp_plan *plan, void *device_buffer, size_t buffer_bytes, void *stream);
+
+/* Frees the plan (host copies, and the device copy if sp_plan_upload made
+ * it).  NULL is ignored.  The caller must make sure no queued kernel still
+ * reads the plan. */
 SP_API void sp_plan_destroy(sp_plan *plan);
 
 /* ---------------------------------------------------- bounded fragments

@@ -72,6 +72,8 @@ _c_ws = _sig("sp_tree_attn_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32, _
 _c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_plan_bytes = _sig("sp_plan_device_bytes", ctypes.c_size_t, [_vp])
+_c_plan_upload_to = _sig("sp_plan_upload_to", ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp])
 _c_frag_plan = _sig("sp_fragment_plan", ctypes.c_int,
                     [ctypes.POINTER(_TreeDesc), ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)])
 _c_frag_view = _sig("sp_fragment_view", ctypes.c_int, [_vp, ctypes.POINTER(_FragInfo)])
@@ -100,7 +102,7 @@ EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
             "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic", "sp_fragment_plan", "sp_fragment_view",
-            "sp_fragment_destroy")
+            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -184,6 +186,17 @@ def _stream(stream):
 
 def sp_plan_upload(plan: Plan, stream=None):
     _check(_c_plan_upload(plan.handle, _stream(stream)), "sp_plan_upload")
+
+
+def sp_plan_device_bytes(plan: Plan) -> int:
+    return int(_c_plan_bytes(plan.handle))
+
+
+def sp_plan_upload_to(plan: Plan, buffer, stream=None):
+    """Upload the plan into a caller-owned device buffer (a CUDA uint8 tensor kept alive by the caller)."""
+    _need_cuda(buffer)
+    _check(_c_plan_upload_to(plan.handle, _ptr(buffer), buffer.numel() * buffer.element_size(), _stream(stream)),
+           "sp_plan_upload_to")
 
 
 def _ptr(t):

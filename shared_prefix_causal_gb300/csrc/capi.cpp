@@ -78,35 +78,46 @@ int sp_plan_view(const sp_plan *p, sp_plan_info *info) {
   return SP_OK;
 }
 
-int sp_plan_upload(sp_plan *p, void *stream) {
-  if (!p) return SP_ERR_INVALID_ARG;
-  if (p->d_tiles) return SP_OK;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+}  // extern "C"
+
+namespace {
+
+// Derived device tables (forward pairs, backward launch order), built once.
+int prepare_device_tables(sp_plan *p) {
+  if (!p->pairs.empty() || p->tiles.empty()) return SP_OK;
   try {
     spc::build_pairs(*p, 128);
     spc::build_bwd_schedule(*p);
   } catch (...) {
     return SP_ERR_INVALID_ARG;
   }
-  const size_t bt = p->tiles.size() * 4, br = p->ranges.size() * 4, bb = p->bwd.size() * 4;
-  const size_t bp = p->pairs.size() * 4, bk = p->pblk.size() * 4;
-  const size_t total = align_up(bt) + align_up(br) + align_up(bb) + align_up(bp) + align_up(bk) + 256;
-  char *base = nullptr;
-  if (cudaMalloc(&base, total) != cudaSuccess) return SP_ERR_CUDA;
+  return SP_OK;
+}
+
+struct DeviceLayout {
+  size_t bt, br, bb, bp, bk, total;
+};
+
+DeviceLayout device_layout(const sp_plan &p) {
+  DeviceLayout l{p.tiles.size() * 4, p.ranges.size() * 4, p.bwd.size() * 4, p.pairs.size() * 4,
+                 p.pblk.size() * 4, 0};
+  l.total = align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp) + align_up(l.bk) + 256;
+  return l;
+}
+
+// Copies the tables into base (256-byte aligned) on stream st and points the plan at them.
+int copy_tables(sp_plan *p, char *base, const DeviceLayout &l, cudaStream_t st) {
   int32_t *dt = reinterpret_cast<int32_t *>(base);
-  int32_t *dr = reinterpret_cast<int32_t *>(base + align_up(bt));
-  int32_t *db = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br));
-  int32_t *dp = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br) + align_up(bb));
-  int32_t *dk = reinterpret_cast<int32_t *>(base + align_up(bt) + align_up(br) + align_up(bb) + align_up(bp));
-  if ((bt && cudaMemcpyAsync(dt, p->tiles.data(), bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      (br && cudaMemcpyAsync(dr, p->ranges.data(), br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      (bb && cudaMemcpyAsync(db, p->bwd_sched.data(), bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      (bp && cudaMemcpyAsync(dp, p->pairs.data(), bp, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      (bk && cudaMemcpyAsync(dk, p->pblk.data(), bk, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      cudaStreamSynchronize(st) != cudaSuccess) {
-    cudaFree(base);
+  int32_t *dr = reinterpret_cast<int32_t *>(base + align_up(l.bt));
+  int32_t *db = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br));
+  int32_t *dp = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br) + align_up(l.bb));
+  int32_t *dk = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp));
+  if ((l.bt && cudaMemcpyAsync(dt, p->tiles.data(), l.bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.br && cudaMemcpyAsync(dr, p->ranges.data(), l.br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.bb && cudaMemcpyAsync(db, p->bwd_sched.data(), l.bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.bp && cudaMemcpyAsync(dp, p->pairs.data(), l.bp, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.bk && cudaMemcpyAsync(dk, p->pblk.data(), l.bk, cudaMemcpyHostToDevice, st) != cudaSuccess))
     return SP_ERR_CUDA;
-  }
   p->d_tiles = dt;
   p->d_ranges = dr;
   p->d_bwd = db;
@@ -116,9 +127,50 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   return SP_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int sp_plan_upload(sp_plan *p, void *stream) {
+  if (!p) return SP_ERR_INVALID_ARG;
+  if (p->d_tiles) return SP_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (int rc = prepare_device_tables(p)) return rc;
+  const DeviceLayout l = device_layout(*p);
+  char *base = nullptr;
+  if (cudaMalloc(&base, l.total) != cudaSuccess) return SP_ERR_CUDA;
+  if (copy_tables(p, base, l, st) != SP_OK || cudaStreamSynchronize(st) != cudaSuccess) {
+    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = nullptr;
+    cudaFree(base);
+    return SP_ERR_CUDA;
+  }
+  p->owns_device = true;
+  return SP_OK;
+}
+
+size_t sp_plan_device_bytes(sp_plan *p) {
+  if (!p || prepare_device_tables(p) != SP_OK) return 0;
+  return device_layout(*p).total;
+}
+
+int sp_plan_upload_to(sp_plan *p, void *device_buffer, size_t buffer_bytes, void *stream) {
+  if (!p || !device_buffer) return SP_ERR_INVALID_ARG;
+  if (p->d_tiles) return SP_OK;
+  if (reinterpret_cast<uintptr_t>(device_buffer) & 255u) return SP_ERR_ALIGNMENT;
+  if (int rc = prepare_device_tables(p)) return rc;
+  const DeviceLayout l = device_layout(*p);
+  if (buffer_bytes < l.total) return SP_ERR_WORKSPACE;
+  if (int rc = copy_tables(p, static_cast<char *>(device_buffer), l, static_cast<cudaStream_t>(stream))) {
+    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = nullptr;
+    return rc;
+  }
+  p->owns_device = false;
+  return SP_OK;
+}
+
 void sp_plan_destroy(sp_plan *p) {
   if (!p) return;
-  if (p->d_tiles) cudaFree(p->d_tiles);
+  if (p->d_tiles && p->owns_device) cudaFree(p->d_tiles);
   delete p;
 }
 

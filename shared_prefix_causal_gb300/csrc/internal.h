@@ -26,6 +26,7 @@ struct sp_plan {
   // device copies (owned), valid after sp_plan_upload
   int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr, *d_pairs = nullptr, *d_pblk = nullptr;
   int device = -1;
+  bool owns_device = false;  // the device tables were allocated by sp_plan_upload
   int32_t n_tiles() const { return int32_t(tiles.size() / 5); }
   int32_t n_ranges() const { return int32_t(ranges.size() / 2); }
   int32_t n_bwd() const { return int32_t(bwd.size() / 5); }

@@ -279,3 +279,16 @@ def test_fragment_tokens_index_the_whole_tree():
             assert idx[st_] == int(w.tree.seg_start[s_])
         np.add.at(owned_total, idx[own], 1)
     assert (owned_total == 1).all()  # every token owned exactly once
+
+
+def test_plan_upload_to_checks():
+    t = W.tiny().tree
+    p = spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 64, 128, 0)
+    n = spc.sp_plan_device_bytes(p)
+    assert n > 0 and n % 256 == 0
+    assert spc._c_plan_bytes(None) == 0
+    fake = ctypes.c_void_p(1 << 20)
+    assert spc._c_plan_upload_to(p.handle, None, n, None) == -2
+    assert spc._c_plan_upload_to(None, fake, n, None) == -2
+    assert spc._c_plan_upload_to(p.handle, ctypes.c_void_p((1 << 20) + 16), n, None) == -4
+    assert spc._c_plan_upload_to(p.handle, fake, n - 1, None) == -8

@@ -475,3 +475,24 @@ def test_gqa_and_head_dim_sweep(hq, hkv, d):
     check_full(w, x, out_det, "bf16")
     for n in ("dk", "dv"):
         assert np.array_equal(out[n], out_det[n]), n
+
+
+def test_plan_uploaded_into_a_caller_buffer_gives_identical_results():
+    w = W.get("star")
+    x = W.draw_tensors(w, "bf16")
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    G = w.hq // w.hkv
+    ref = spc.tree_plan(w.tree, 128 // G)
+    p = spc.tree_plan(w.tree, 128 // G, upload=False)
+    buf = torch.empty(spc.sp_plan_device_bytes(p), dtype=torch.uint8, device="cuda")
+    spc.sp_plan_upload_to(p, buf)
+    outs = []
+    for plan in (ref, p):
+        o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale)
+        dq, dk, dv = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, deterministic=True)
+        outs.append([t.cpu() for t in (o, lse, dq, dk, dv)])
+    torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    p.close()  # the caller's buffer is not freed by the plan
+    assert buf.is_cuda and buf.numel() > 0
