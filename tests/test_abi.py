@@ -292,3 +292,42 @@ def test_plan_upload_to_checks():
     assert spc._c_plan_upload_to(None, fake, n, None) == -2
     assert spc._c_plan_upload_to(p.handle, ctypes.c_void_p((1 << 20) + 16), n, None) == -4
     assert spc._c_plan_upload_to(p.handle, fake, n - 1, None) == -8
+
+
+# ------------------------------------------------------------ bench host helpers
+
+def _golden_value(key):
+    import os
+    path = os.path.join(os.path.dirname(__file__), "golden", "tiny_plan.txt")
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 2 and parts[0] == key:
+            return int(parts[1])
+    raise KeyError(key)
+
+
+def test_bench_useful_pairs_matches_the_hand_derived_count():
+    import bench
+    assert bench.useful_pairs(W.get("tiny").tree) == _golden_value("pairs")
+
+
+def test_bench_tile_efficiency_by_hand_on_a_single_segment():
+    """One 300-token segment, G = 4 (32-token tiles, 16-token backward blocks): computed pairs by hand."""
+    import bench
+    t = W.tree_from_preorder([300], [-1])
+    p = spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 32, 128, 0)
+    pairs = 300 * 301 // 2
+    # forward: tile k covers tokens [32k, min(32k+32, 300)) and reads keys [0, q_end) in 128-key blocks
+    fwd = sum(((min(32 * k + 32, 300) + 127) // 128) * 128 * 32 for k in range(10))
+    # backward: key block [128b, ...) walks queries [128b, 300) in 16-token blocks of 128 keys
+    bwd = sum(((300 - 128 * b + 15) // 16) * 16 * 128 for b in range(3))
+    eff = bench.tile_efficiency(spc, p, 4, pairs)
+    assert eff == {"fwd": round(pairs / fwd, 4), "bwd": round(pairs / bwd, 4)}
+
+
+def test_bench_fragment_summary():
+    import bench
+    out = bench.fragment_summary(spc, W.get("tiny"), 130)
+    assert out["fragments"] == 4 and out["fragment_tokens"] == 426 and out["physical_tokens"] == 186
+    assert out["duplication"] == round(426 / 186, 4)
+    assert "error" in bench.fragment_summary(spc, W.get("tiny"), 10)
