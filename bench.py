@@ -40,18 +40,18 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 3, "gather": 1}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each tensor-core kernel,
 # from one single-pass ncu capture of this bench on a GB300 (profiles/dram_traffic_agent_tree_64k.md),
-# keyed by workload, with a digest of the sources that define the kernel and its schedule: a
-# figure whose sources have changed since the capture is reported as null.
+# keyed by workload, with a digest of the code (comments stripped) that defines the kernel and its
+# schedule: a figure whose code has changed since the capture is reported as null.
 CSRC = os.path.join(ROOT, "shared_prefix_causal_gb300", "csrc")
 TRAFFIC_SOURCES = {
     "fwd_tc_kernel": ("attn_fwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
     "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
 }
 MEASURED_TRAFFIC = {
-    "agent": {"fwd_tc_kernel": (813.75e6 + 510.94e6, "068960eb1a442da3"),
-              "bwd_tc_kernel": (16.64e9 + 8.42e9, "01d9ed31dcd02ef2")},
-    "star": {"fwd_tc_kernel": (94.39e6 + 27.93e6, "068960eb1a442da3"),
-             "bwd_tc_kernel": (333.02e6 + 131.47e6, "01d9ed31dcd02ef2")},
+    "agent": {"fwd_tc_kernel": (813.75e6 + 510.94e6, "b87f4ad41bb9668b"),
+              "bwd_tc_kernel": (16.64e9 + 8.42e9, "740fd55f1556b1c3")},
+    "star": {"fwd_tc_kernel": (94.39e6 + 27.93e6, "b87f4ad41bb9668b"),
+             "bwd_tc_kernel": (333.02e6 + 131.47e6, "740fd55f1556b1c3")},
 }
 
 
@@ -70,12 +70,20 @@ def useful_pairs(tree) -> int:
     return total
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments, blank lines or trailing blanks (comments do not change a kernel)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def sources_digest(kernel: str) -> str:
     import hashlib
     m = hashlib.sha256()
     for f in TRAFFIC_SOURCES[kernel]:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
+            m.update(_code_only(fh.read()).encode())
     return m.hexdigest()[:16]
 
 

@@ -106,9 +106,9 @@ typedef struct {
 } sp_plan_info;
 
 /* tree_plan -- validate the tree and build the per-query-tile ancestor
- * KV-range lists (issue #7386, third bullet: attention "for each query run
- * against only its ancestor path"; PR #7387, "Summary": "causal attention over
- * each query segment's ancestors").
+ * KV-range lists (issue #7386, "Describe the solution you'd like", third
+ * bullet: every query run attends to its own ancestor path and nothing else;
+ * PR #7387, "Summary": a query segment attends causally over its ancestors).
  *   tile_tokens  query tokens per tile (> 0); a tile never crosses a segment
  *                end.  The bf16 kernels need tile_tokens * G == 128; the fp32
  *                kernels need tile_tokens * G <= 128.
@@ -154,9 +154,9 @@ SP_API void sp_plan_destroy(sp_plan *plan);
 
 /* ---------------------------------------------------- bounded fragments
  * A tree too large for one step is split into fragments of at most
- * max_tokens physical tokens.  The trainer "bounds fragments and may repeat
- * ancestors across fragments to honor the memory bound", and every sampled
- * action keeps exactly one loss owner (issue #7386, "Describe the solution
+ * max_tokens physical tokens.  The trainer keeps every fragment under a memory
+ * bound, repeating ancestors in several fragments where it has to, and every
+ * sampled action keeps exactly one loss owner (issue #7386, "Describe the solution
  * you'd like", last paragraph; "Additional context": 3,744,651 physical
  * tokens before fragment duplication, 3,919,929 after).  The pages give no
  * algorithm; this one visits segments in preorder and adds each, with the
@@ -213,8 +213,8 @@ SP_API size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t
 /* tree_attn_bwd -- dQ, dK, dV of L = sum_i <O_i, dO_i> through the tree
  * attention (FlashAttention-style: S and P are recomputed from q, k and lse).
  * Every child branch's contribution to a shared prefix's dK/dV is summed into
- * that prefix ("Backward accumulates branch contributions into the shared
- * prefix", #7914 introduction).
+ * that prefix (#7914, introduction: the backward sums the branches'
+ * contributions into the prefix they share).
  *   q, k, v, o, lse, d_o: as in / out of tree_attn_fwd (d_o like o)
  *   dq [T][Hq][D], dk and dv [T][Hkv][D]: outputs in dtype, fully overwritten
  *   workspace: device scratch of at least

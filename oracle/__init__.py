@@ -10,16 +10,17 @@ Sources (three web pages about one Megatron-LM feature):
 
 * "[ENHANCEMENT] Shared-prefix training with context parallelism for exact
   agent trajectories" (issue #7386) -- "Describe the solution you'd like"
-  (DFS segments with parent/depth metadata; attention of each query run
-  against only its ancestor path; only sampled-edge sources projected, one
-  loss owner per sampled action) and "Describe alternatives you've
+  (DFS segments with parent/depth metadata; every query run attends to its
+  own ancestor path only; only the sampled-edge sources are projected, and
+  each sampled action has a single loss owner) and "Describe alternatives you've
   considered" (independent exact-call sequences are the correctness
   reference).
 * "feat(hybrid): add opt-in shared-prefix attention and Mamba execution"
-  (#7914) -- introduction (prompt K/V reused, each suffix causally isolated,
-  backward accumulates branch contributions into the shared prefix).
+  (#7914) -- introduction (the prompt's K/V is reused, each suffix is
+  causally isolated, the backward sums the branches' contributions into
+  their shared prefix).
 * "TreePackedSeqParams" draft (PR #7387) -- "Summary" (DFS segments, ancestor
-  relationships, causal attention over each query segment's ancestors,
+  relationships, each query segment attending causally over its ancestors,
   edge-source selection before the vocabulary projection, rejection of
   unsupported input).
 

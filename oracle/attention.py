@@ -9,13 +9,13 @@ softmax attention on it and maps every row back to its physical token; a
 prefix token that lies on several paths must come out the same on all of them
 (checked).
 
-Backward.  #7914 (introduction) says backward "accumulates branch
-contributions into the shared prefix".  The loss of the tree is
+Backward.  #7914 (introduction): the backward sums every branch's
+contribution into the prefix the branches share.  The loss of the tree is
 ``L = sum_i <O_i, dO_i>`` over physical tokens.  In the unrolled sequences
 each physical token's upstream gradient dO is handed to exactly one copy --
 the first root-to-leaf path in DFS order that contains it -- and all other
-copies get zero; this is the pages' "one loss owner per sampled action"
-(issue #7386, "Describe the solution you'd like", fifth bullet, and
+copies get zero; this is the pages' rule that each sampled action has a
+single loss owner (issue #7386, "Describe the solution you'd like", fifth bullet, and
 "Additional context") applied to the upstream gradient, and it is the only
 assignment for which the unrolled sum equals dL of the tree.  Per path the
 gradient is the textbook one (dV = P^T dO, dP = dO V^T, D = rowsum(dO*O),

@@ -2,9 +2,9 @@
 
 "[ENHANCEMENT] Shared-prefix training with context parallelism for exact
 agent trajectories" (issue #7386), "Describe the solution you'd like" (third
-and last paragraphs): the trainer bounds fragments to a memory limit and may
-repeat ancestors across fragments to honour it, and every sampled action keeps
-exactly one loss owner ("Additional context": 3,744,651 physical tokens before
+and last paragraphs): the trainer keeps fragments under a memory limit, with
+ancestors repeated in several fragments where needed, and every sampled action
+keeps exactly one loss owner ("Additional context": 3,744,651 physical tokens before
 fragment duplication, 3,919,929 after).  The pages give no algorithm; the
 reading implemented here, in plain Python:
 

@@ -1,9 +1,8 @@
 """Independent planner for the per-query-tile ancestor KV ranges (oracle).
 
-Issue #7386 ("Describe the solution you'd like", third bullet) computes
-attention "for each query run against only its ancestor path"; PR #7387
-("Summary", second bullet) runs "causal attention over each query segment's
-ancestors".  A plan lists, for every query tile, the key ranges that tile
+Issue #7386 ("Describe the solution you'd like", third bullet): each query
+run attends to its ancestor path only; PR #7387 ("Summary", second bullet): a
+query segment attends causally over its ancestors.  A plan lists, for every query tile, the key ranges that tile
 reads: the ancestor segments' tokens (fully visible) and the own segment up to
 the tile's end (causal).  The pages fix no tile size or order; the canonical
 form below is this library's, and the C++ planner must reproduce it bit for

@@ -5,12 +5,12 @@ A tree is four int arrays over segments in DFS preorder: ``seg_start``,
 the solution you'd like", first bullet) and PR #7387 ("Summary", first bullet)
 describe this metadata as DFS-linearized segments with parent/depth
 (ancestor) information.  Reading taken: "DFS-linearized" is preorder, the one
-DFS order in which every ancestor precedes its descendants, which "causal
-attention over each query segment's ancestors" (PR #7387, "Summary") needs.
+DFS order in which every ancestor precedes its descendants, which a query
+segment attending causally over its ancestors (PR #7387, "Summary") needs.
 
-Rejection of malformed input before any work follows #7914 ("unsupported
-layouts and training modes fail before execution") and PR #7387 ("Reject
-unsupported ...").
+Rejection of malformed input before any work follows #7914 (introduction:
+unsupported layouts and modes are refused before anything runs) and PR #7387
+("Summary": unsupported input is rejected).
 """
 from __future__ import annotations
 

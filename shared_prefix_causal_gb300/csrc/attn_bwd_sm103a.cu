@@ -1,7 +1,7 @@
 // Tree attention backward on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
-// The backward "accumulates branch contributions into the shared prefix"
-// (#7914, "feat(hybrid): add opt-in shared-prefix attention and Mamba
+// The backward sums every branch's contribution into the prefix the branches
+// share (#7914, "feat(hybrid): add opt-in shared-prefix attention and Mamba
 // execution", introduction).  In preorder, the queries that can see a key are
 // exactly the key's own later tokens and every token of its segment's
 // subtree: one contiguous run [kv_start, subtree end).  So each CTA owns one

@@ -2,8 +2,8 @@
 // its own ancestor key ranges ("[ENHANCEMENT] Shared-prefix training with
 // context parallelism for exact agent trajectories", issue #7386, "Describe
 // the solution you'd like": each query run attends to its ancestor path; PR
-// #7387 "TreePackedSeqParams", "Summary": causal attention over each query
-// segment's ancestors) and accumulates
+// #7387 "TreePackedSeqParams", "Summary": a query segment attends causally
+// over its ancestors) and accumulates
 //
 //   dQ = scale * sum_keys dS K,   dS = P o (dP - Delta),  P = exp(scale Q K^T - LSE),  dP = dO V^T
 //

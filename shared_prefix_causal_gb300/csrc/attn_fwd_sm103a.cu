@@ -2,9 +2,9 @@
 //
 // What it computes: for every query token, softmax attention over the keys of
 // its ancestor segments (all visible) and of its own segment up to itself
-// (causal), i.e. "causal attention over each query segment's ancestors"
-// (PR #7387 "TreePackedSeqParams", "Summary"; issue #7386, "Describe the
-// solution you'd like": each query run attends only to its ancestor path).
+// (causal): each query segment attends causally over its ancestors (PR #7387
+// "TreePackedSeqParams", "Summary"; issue #7386, "Describe the solution
+// you'd like": each query run attends only to its ancestor path).
 // Outputs O (bf16) and the natural-log LSE (fp32) kept for the backward.
 //
 // One CTA per (pair of query tiles, KV head).  A tile is 128 rows = (128 / G)

@@ -2,13 +2,13 @@
 //
 // Same plan walk as the tensor-core path: a query tile reads the key ranges
 // of its ancestors (fully visible) and its own segment up to the tile end
-// (causal), per "causal attention over each query segment's ancestors"
-// (PR #7387 "TreePackedSeqParams", "Summary").  The backward is split in two
+// (causal), as PR #7387 "TreePackedSeqParams", "Summary" has a query segment
+// attend over its ancestors.  The backward is split in two
 // deterministic kernels: dQ walks the same forward ranges; dK/dV walks, for
 // each block of keys, the one contiguous run of queries that can see it (the
 // key's segment and its whole subtree, which preorder places right after it),
-// so every branch's contribution is summed into the shared prefix ("Backward
-// accumulates branch contributions into the shared prefix", #7914).
+// so every branch's contribution is summed into the shared prefix (#7914,
+// introduction).
 //
 // Work decomposition: a CTA of 256 threads owns 64 rows (query rows of a
 // tile for the forward and dQ, keys of a block for dK/dV) and steps over the

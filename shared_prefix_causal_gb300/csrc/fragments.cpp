@@ -1,8 +1,8 @@
 // Bounded fragment planning ("[ENHANCEMENT] Shared-prefix training with
 // context parallelism for exact agent trajectories", issue #7386, "Describe
-// the solution you'd like": the trainer bounds fragments and may repeat
-// ancestors across fragments to honour the memory bound; every sampled action
-// keeps one loss owner).  The pages give no algorithm.  This one visits the
+// the solution you'd like": the trainer keeps fragments within a memory bound,
+// repeating ancestors in several fragments where it has to; every sampled
+// action keeps one loss owner).  The pages give no algorithm.  This one visits the
 // segments in preorder and adds each, with whichever of its ancestors the
 // current fragment lacks, while the fragment stays within the cap; otherwise
 // the fragment is closed and the next starts from the segment's root path.

@@ -2,7 +2,7 @@
 // the sampled token ("[ENHANCEMENT] Shared-prefix training with context
 // parallelism for exact agent trajectories", issue #7386, "Describe the
 // solution you'd like", fifth bullet: only sampled-edge source states are
-// projected, one loss owner per sampled action; "TreePackedSeqParams" draft,
+// projected, a single loss owner for each sampled action; "TreePackedSeqParams" draft,
 // PR #7387, "Summary": edge-source selection before the vocabulary projection).
 //
 //   logits[e][v] = <h[e], W[v]>    (h: [E][Hd], W: [V][Hd], bf16; fp32 accumulation)

@@ -1,9 +1,9 @@
 // Host planner: tree validation and the per-query-tile ancestor KV-range
 // lists ("[ENHANCEMENT] Shared-prefix training with context parallelism for
 // exact agent trajectories", issue #7386, "Describe the solution you'd like":
-// attention for each query run against only its ancestor path; PR #7387
-// "TreePackedSeqParams", "Summary": causal attention over each query
-// segment's ancestors).
+// every query run attends to its ancestor path only; PR #7387
+// "TreePackedSeqParams", "Summary": a query segment attends causally over its
+// ancestors).
 //
 // One preorder pass with an explicit root-path stack validates the tree and
 // builds, per segment, the merged token intervals of its root path; a reverse
