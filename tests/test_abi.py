@@ -68,6 +68,22 @@ def test_plan_matches_tiny_golden_file():
     assert [tuple(map(int, b)) for b in got["bwd"]] == gold["bwd"]
 
 
+def test_plan_order1_matches_tiny_golden_file():
+    from tests.test_oracle import _read_golden
+    got = _plan_tables(W.tiny().tree, 32, 32, 1)
+    assert [tuple(map(int, r[:3])) for r in got["tiles"]] == _read_golden()["order1"]
+
+
+def test_plan_matches_the_hand_worked_forest():
+    from tests.test_oracle import FOREST_HAND as f
+    p = spc.sp_tree_plan(f["seg_start"], f["seg_len"], f["parent"], f["depth"], 32, 32, 0)
+    got = spc.sp_plan_view(p)
+    tiles = [(int(s), int(a), int(b), [tuple(map(int, got["ranges"][r])) for r in range(rb, rb + rc)])
+             for s, a, b, rb, rc in got["tiles"]]
+    assert tiles == f["tiles"]
+    assert [tuple(map(int, b)) for b in got["bwd"]] == f["bwd"]
+
+
 def _desc(t):
     return [np.asarray(getattr(t, k)).copy() for k in ("seg_start", "seg_len", "parent", "depth")]
 

@@ -48,6 +48,7 @@ def test_validate_accepts_generated_configs():
 @pytest.mark.parametrize("mutate,msg", [
     (lambda a: a["seg_len"].__setitem__(2, 0), "empty"),
     (lambda a: a["seg_start"].__setitem__(3, 100), "start"),
+    (lambda a: a["seg_start"].__setitem__(3, 150), "gap"),
     (lambda a: a["parent"].__setitem__(1, 3), "parent"),
     (lambda a: a["parent"].__setitem__(0, 0), "root"),
     (lambda a: a["depth"].__setitem__(3, 1), "depth"),
@@ -59,6 +60,13 @@ def test_validate_rejects(mutate, msg):
     mutate(a)
     with pytest.raises(OT.InvalidTree):
         OT.validate(a["seg_start"], a["seg_len"], a["parent"], a["depth"], t.total_tokens)
+
+
+def test_validate_rejects_an_empty_segment_even_when_the_packing_is_consistent():
+    # the tiny tree with leaf segment 4 emptied and every later start moved back to stay packed
+    with pytest.raises(OT.InvalidTree):
+        OT.validate([0, 64, 96, 144, 160, 160], [64, 32, 48, 16, 0, 17], [-1, 0, 0, 2, 2, 0],
+                    [0, 1, 1, 2, 2, 1], 177)
 
 
 def test_visibility_pairs_and_naive_tokens_match_hand_count():
@@ -73,7 +81,7 @@ def test_visibility_pairs_and_naive_tokens_match_hand_count():
 # ---------------------------------------------------------------- plan checks
 
 def _read_golden():
-    tiles, bwd, out = [], [], {}
+    tiles, bwd, order1, out = [], [], [], {}
     with open(os.path.join(GOLDEN, "tiny_plan.txt")) as f:
         for line in f:
             line = line.split("#")[0].strip()
@@ -86,10 +94,12 @@ def _read_golden():
                 tiles.append((s, q0, q1, list(zip(r[0::2], r[1::2]))))
             elif line.startswith("bwd "):
                 bwd.append(tuple(map(int, line[4:].split())))
+            elif line.startswith("order1 "):
+                order1.append(tuple(map(int, line[7:].split())))
             else:
                 k, v = line.split()
                 out[k] = int(v)
-    out["tiles"], out["bwd"] = tiles, bwd
+    out["tiles"], out["bwd"], out["order1"] = tiles, bwd, order1
     return out
 
 
@@ -103,6 +113,47 @@ def test_plan_matches_hand_derived_golden():
     assert [tuple(map(int, b)) for b in bwd] == gold["bwd"]
     # r_begin is the running count of ranges in schedule order
     assert list(tiles[:, 3]) == list(np.cumsum([0] + [len(x[3]) for x in gold["tiles"]])[:-1])
+
+
+def test_plan_order1_matches_hand_derived_golden():
+    gold = _read_golden()
+    t = W.tiny().tree
+    tiles, _, _ = OP.build(*_tree_args(t), tile_tokens=32, kv_block=32, order=1)
+    assert [tuple(map(int, r[:3])) for r in tiles] == gold["order1"]
+
+
+# Two trees: root 0 [0,40) with children 1 [40,60) and 2 [60,80); root 3 [80,110) with child 4
+# [110,120).  Tiles of 32 tokens in order 0, worked by hand: the first tree's tiles, then the
+# second's; each tile's ranges are its ancestors' tokens and its own segment up to the tile end.
+FOREST_HAND = {
+    "seg_start": [0, 40, 60, 80, 110], "seg_len": [40, 20, 20, 30, 10], "parent": [-1, 0, 0, -1, 3],
+    "depth": [0, 1, 1, 0, 1],
+    "tiles": [(0, 0, 32, [(0, 32)]), (0, 32, 40, [(0, 40)]), (1, 40, 60, [(0, 60)]),
+              (2, 60, 80, [(0, 40), (60, 80)]), (3, 80, 110, [(80, 110)]), (4, 110, 120, [(80, 120)])],
+    # kv_block 32: (seg, kv_start, kv_end, q_begin, q_end), most queries first, ties by kv_start
+    "bwd": [(0, 0, 32, 0, 80), (0, 32, 40, 32, 80), (3, 80, 110, 80, 120), (1, 40, 60, 40, 60),
+            (2, 60, 80, 60, 80), (4, 110, 120, 110, 120)],
+}
+
+
+def test_plan_forest_keeps_each_tree_together_by_hand():
+    f = FOREST_HAND
+    tiles, ranges, bwd = OP.build(f["seg_start"], f["seg_len"], f["parent"], tile_tokens=32, kv_block=32,
+                                  order=0)
+    got = [(int(s), int(q0), int(q1), [tuple(map(int, ranges[r])) for r in range(rb, rb + rc)])
+           for s, q0, q1, rb, rc in tiles]
+    assert got == f["tiles"]
+    assert [tuple(map(int, b)) for b in bwd] == f["bwd"]
+
+
+def test_plan_order0_groups_tiles_by_tree_on_the_forest_workload():
+    t = W.grpo_forest().tree
+    tiles, _, _ = OP.build(*_tree_args(t), tile_tokens=32, kv_block=128, order=0)
+    root = np.empty(t.num_segments, dtype=np.int64)
+    for s in range(t.num_segments):
+        root[s] = s if t.parent[s] == -1 else root[t.parent[s]]
+    seq = root[tiles[:, 0]]
+    assert (np.diff(seq) >= 0).all() and len(np.unique(seq)) == int((np.asarray(t.parent) == -1).sum()) > 1
 
 
 @pytest.mark.parametrize("seed", range(200))
@@ -352,6 +403,9 @@ def test_edge_gather_oracle():
         OG.edge_gather(h, [6])
     with pytest.raises(IndexError):
         OG.edge_gather(h, [-1])
+    for bad in ([6], [-1], [0, -1]):
+        with pytest.raises(IndexError):
+            OG.edge_gather_backward(np.ones((len(bad), 2)), bad, 6)
 
 
 def test_subtree_key_grads_equal_full_backward():
@@ -466,9 +520,10 @@ def test_lm_head_backward_vanishes_when_all_vocabulary_rows_are_equal():
 def test_lm_head_rejects_labels_outside_the_vocabulary():
     from oracle import lm_head as LH
     h, w, y = _lmh_case()
-    y[0] = w.shape[0]
-    with pytest.raises(IndexError):
-        LH.edge_logprob(h, w, y)
+    for bad in (w.shape[0], -1):
+        y[0] = bad
+        with pytest.raises(IndexError):
+            LH.edge_logprob(h, w, y)
 
 
 def test_lm_head_weight_grad_rows_equals_the_full_backward():
@@ -537,6 +592,14 @@ def test_fragments_checker_catches_broken_covers():
             OF.check_fragments(bad, lens, par, 130)
     with pytest.raises(AssertionError):
         OF.check_fragments(good, lens, par, 120)
+
+
+def test_fragments_accept_a_root_path_exactly_at_the_cap():
+    from oracle import fragments as OF
+    lens, par = [64, 32, 48, 16, 9, 17], [-1, 0, 0, 2, 2, 0]
+    frags = OF.plan_fragments(lens, par, 128)  # 64 + 48 + 16: the longest root path
+    OF.check_fragments(frags, lens, par, 128)
+    assert [(3, True)] == [x for f in frags for x in f if x[0] == 3]
 
 
 def test_fragments_reject_a_root_path_above_the_cap():
