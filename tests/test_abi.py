@@ -96,6 +96,8 @@ def _desc(t):
     lambda a: a[3].__setitem__(3, 1),                       # wrong depth
     lambda a: (a[2].__setitem__(5, 1), a[3].__setitem__(5, 2)),  # not preorder
     lambda a: a[2].__setitem__(4, -2),                      # parent below -1
+    lambda a: a[0].__setitem__(3, 150),                     # a true gap (start after the previous end)
+    lambda a: (a[1].__setitem__(4, 0), a[0].__setitem__(5, 160)),  # empty segment, packing consistent
 ])
 def test_plan_rejects_invalid_tree(mutate):
     a = _desc(W.tiny().tree)
