@@ -349,3 +349,41 @@ def test_bench_fragment_summary():
     assert out["fragments"] == 4 and out["fragment_tokens"] == 426 and out["physical_tokens"] == 186
     assert out["duplication"] == round(426 / 186, 4)
     assert "error" in bench.fragment_summary(spc, W.get("tiny"), 10)
+
+
+def test_bench_clock_sampler_keeps_only_the_timed_window(tmp_path):
+    """nvidia-smi lines (timestamp first) outside the timed region are dropped; throttle reasons are
+    collected from the kept lines only; the median SM clock is over the kept lines."""
+    import datetime
+    import bench
+
+    def line(t, sm, reasons=("Not Active",) * 4):
+        ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return ", ".join([ts, "0", str(sm), "2070", "900.00", "0x0000000000000000", *reasons]) + "\n"
+
+    t0 = 1_800_000_000.0
+    csv = tmp_path / "clocks.csv"
+    csv.write_text(line(t0 - 2.0, 800, ("Active", "Not Active", "Not Active", "Not Active"))  # before
+                   + line(t0 + 0.1, 2070) + line(t0 + 0.2, 2055)
+                   + line(t0 + 0.3, 2040, ("Not Active", "Not Active", "Not Active", "Active"))
+                   + "garbage line\n"
+                   + line(t0 + 5.0, 1000, ("Not Active", "Active", "Not Active", "Not Active")))  # after
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    cs = bench.ClockSampler(0)
+    cs.proc, cs.path = FakeProc(), str(csv)
+    cs.mark(t0, t0 + 0.4)
+    got = cs.stop()
+    assert got == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+    assert not csv.exists()
+
+
+def test_bench_clock_sampler_without_nvidia_smi_reports_nothing():
+    import bench
+    assert bench.ClockSampler(0).stop() is None
