@@ -201,6 +201,8 @@ SP_API void sp_fragment_destroy(sp_fragments *frag);
  *   D in {64, 128}; G = Hq / Hkv in {1, 2, 4, 8}; T == plan total_tokens.
  * bf16 runs on the tensor cores (fp32 accumulation and softmax, P rounded to
  * bf16 for the P*V product); fp32 runs a full-fp32 SIMT kernel.
+ * The current device must be the one the plan was uploaded on (its tables
+ * live there); otherwise SP_ERR_INVALID_ARG and nothing is launched.
  * Errors: SP_ERR_INVALID_ARG, SP_ERR_UNSUPPORTED, SP_ERR_ALIGNMENT,
  * SP_ERR_NOT_UPLOADED, SP_ERR_CUDA; device: SP_DEV_TIMEOUT, SP_DEV_BAD_PLAN. */
 SP_API int sp_tree_attn_fwd(const sp_plan *plan, int32_t dtype, const void *q, const void *k,

@@ -175,13 +175,20 @@ def sp_plan_view(plan: Plan) -> dict:
     }
 
 
-def _stream(stream):
+def _stream(stream, device=None):
+    """The stream argument as a cudaStream_t: None means the current stream of ``device``."""
     import torch
     if stream is None:
-        return _vp(torch.cuda.current_stream().cuda_stream)
+        return _vp(torch.cuda.current_stream(device).cuda_stream)
     if isinstance(stream, int):
         return _vp(stream)
     return _vp(stream.cuda_stream)
+
+
+def _on(t):
+    """Makes tensor t's GPU current for one call: the library launches on the current device."""
+    import torch
+    return torch.cuda.device(t.device)
 
 
 def sp_plan_upload(plan: Plan, stream=None):
@@ -195,8 +202,9 @@ def sp_plan_device_bytes(plan: Plan) -> int:
 def sp_plan_upload_to(plan: Plan, buffer, stream=None):
     """Upload the plan into a caller-owned device buffer (a CUDA uint8 tensor kept alive by the caller)."""
     _need_cuda(buffer)
-    _check(_c_plan_upload_to(plan.handle, _ptr(buffer), buffer.numel() * buffer.element_size(), _stream(stream)),
-           "sp_plan_upload_to")
+    with _on(buffer):
+        _check(_c_plan_upload_to(plan.handle, _ptr(buffer), buffer.numel() * buffer.element_size(),
+                                 _stream(stream, buffer.device)), "sp_plan_upload_to")
 
 
 def _ptr(t):
@@ -225,8 +233,9 @@ def sp_tree_attn_fwd(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status
     if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) or tuple(o.shape) != (T, Hq, D) \
             or tuple(lse.shape) != (Hq, T) or o.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
         raise ValueError("shape or dtype mismatch")
-    _check(_c_fwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, D,
-                  float(softmax_scale), _ptr(d_status), _stream(stream)), "sp_tree_attn_fwd")
+    with _on(q):
+        _check(_c_fwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, D,
+                      float(softmax_scale), _ptr(d_status), _stream(stream, q.device)), "sp_tree_attn_fwd")
 
 
 def sp_tree_attn_bwd_workspace_bytes(dtype: int, T: int, Hq: int, D: int) -> int:
@@ -244,9 +253,10 @@ def sp_tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, so
             raise ValueError("shape or dtype mismatch")
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     fn, name = _fn or (_c_bwd, "sp_tree_attn_bwd")
-    _check(fn(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
-              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D, float(softmax_scale),
-              _ptr(d_status), _stream(stream)), name)
+    with _on(q):
+        _check(fn(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D, float(softmax_scale),
+                  _ptr(d_status), _stream(stream, q.device)), name)
 
 
 def sp_tree_attn_bwd_deterministic(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale: float,
@@ -266,9 +276,10 @@ def sp_tree_attn_bwd_noalloc(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, softm
                    (dk, (T, Hkv, D)), (dv, (T, Hkv, D))):
         if tuple(t.shape) != shp or t.dtype != q.dtype:
             raise ValueError("shape or dtype mismatch")
-    _check(_c_bwd_noalloc(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
-                          _ptr(dq), _ptr(dk), _ptr(dv), T, Hq, Hkv, D, float(softmax_scale), _ptr(d_status),
-                          _stream(stream)), "sp_tree_attn_bwd_noalloc")
+    with _on(q):
+        _check(_c_bwd_noalloc(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                              _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), T, Hq, Hkv, D, float(softmax_scale),
+                              _ptr(d_status), _stream(stream, q.device)), "sp_tree_attn_bwd_noalloc")
 
 
 def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
@@ -280,8 +291,9 @@ def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
     E = idx.shape[0]
     if tuple(out.shape) != (E, Hd) or out.dtype != hidden.dtype:
         raise ValueError("shape or dtype mismatch")
-    _check(_c_gather(_dtype_code(hidden), _ptr(hidden), T, Hd, _ptr(idx), E, _ptr(out), _ptr(d_status),
-                     _stream(stream)), "sp_edge_gather")
+    with _on(hidden):
+        _check(_c_gather(_dtype_code(hidden), _ptr(hidden), T, Hd, _ptr(idx), E, _ptr(out), _ptr(d_status),
+                         _stream(stream, hidden.device)), "sp_edge_gather")
 
 
 def sp_edge_gather_bwd_workspace_bytes(T: int, E: int) -> int:
@@ -298,8 +310,10 @@ def sp_edge_gather_bwd(grad_out, idx, grad_hidden, workspace, d_status=None, str
     if tuple(grad_hidden.shape) != (T, Hd) or grad_hidden.dtype != grad_out.dtype or idx.shape[0] != E:
         raise ValueError("shape or dtype mismatch")
     ws = workspace.numel() * workspace.element_size()
-    _check(_c_gather_bwd(_dtype_code(grad_out), _ptr(grad_out), E, Hd, _ptr(idx), T, _ptr(grad_hidden),
-                         _ptr(workspace), ws, _ptr(d_status), _stream(stream)), "sp_edge_gather_bwd")
+    with _on(grad_hidden):
+        _check(_c_gather_bwd(_dtype_code(grad_out), _ptr(grad_out), E, Hd, _ptr(idx), T, _ptr(grad_hidden),
+                             _ptr(workspace), ws, _ptr(d_status), _stream(stream, grad_hidden.device)),
+               "sp_edge_gather_bwd")
 
 
 def sp_edge_logprob_workspace_bytes(E: int, V: int) -> int:
@@ -316,8 +330,10 @@ def sp_edge_logprob(hidden_sel, weight, labels, logprob, lse, workspace, d_statu
     if weight.shape[1] != Hd or labels.shape[0] != E or logprob.shape[0] != E or lse.shape[0] != E:
         raise ValueError("shape mismatch")
     ws = workspace.numel() * workspace.element_size()
-    _check(_c_lmh(_dtype_code(hidden_sel), _ptr(hidden_sel), E, Hd, _ptr(weight), V, _ptr(labels), _ptr(logprob),
-                  _ptr(lse), _ptr(workspace), ws, _ptr(d_status), _stream(stream)), "sp_edge_logprob")
+    with _on(weight):
+        _check(_c_lmh(_dtype_code(hidden_sel), _ptr(hidden_sel), E, Hd, _ptr(weight), V, _ptr(labels),
+                      _ptr(logprob), _ptr(lse), _ptr(workspace), ws, _ptr(d_status), _stream(stream, weight.device)),
+               "sp_edge_logprob")
 
 
 def sp_edge_logprob_bwd_workspace_bytes(E: int, V: int) -> int:
@@ -336,14 +352,17 @@ def sp_edge_logprob_bwd(hidden_sel, weight, labels, lse, grad_logprob, d_hidden_
     if labels.dtype != torch.int32 or lse.dtype != torch.float32 or grad_logprob.dtype != torch.float32:
         raise ValueError("labels int32, lse and grad_logprob float32")
     ws = workspace.numel() * workspace.element_size()
-    _check(_c_lmh_bwd(_dtype_code(hidden_sel), _ptr(hidden_sel), E, Hd, _ptr(weight), V, _ptr(labels), _ptr(lse),
-                      _ptr(grad_logprob), _ptr(d_hidden_sel), _ptr(d_weight), _ptr(workspace), ws, _ptr(d_status),
-                      _stream(stream)), "sp_edge_logprob_bwd")
+    with _on(weight):
+        _check(_c_lmh_bwd(_dtype_code(hidden_sel), _ptr(hidden_sel), E, Hd, _ptr(weight), V, _ptr(labels),
+                          _ptr(lse), _ptr(grad_logprob), _ptr(d_hidden_sel), _ptr(d_weight), _ptr(workspace), ws,
+                          _ptr(d_status), _stream(stream, weight.device)), "sp_edge_logprob_bwd")
 
 
 def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
     _need_cuda(d_status)
-    _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream)), "sp_debug_wait_timeout")
+    with _on(d_status):
+        _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream, d_status.device)),
+               "sp_debug_wait_timeout")
 
 
 # ------------------------------------------------------------ conveniences

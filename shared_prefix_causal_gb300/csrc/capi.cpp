@@ -37,6 +37,13 @@ spc::PlanDev plan_dev(const sp_plan &p) {
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
+// A plan's device tables live on the GPU that was current when it was uploaded;
+// kernels launched on another GPU must not read them.
+bool on_plan_device(const sp_plan &p) {
+  int dev = -1;
+  return cudaGetDevice(&dev) == cudaSuccess && dev == p.device;
+}
+
 }  // namespace
 
 extern "C" {
@@ -186,6 +193,7 @@ int sp_tree_attn_fwd(const sp_plan *p, int32_t dtype, const void *q, const void 
     return SP_ERR_ALIGNMENT;
   if (!(softmax_scale > 0.f)) return SP_ERR_INVALID_ARG;
   if (!p->d_tiles) return SP_ERR_NOT_UPLOADED;
+  if (!on_plan_device(*p)) return SP_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
   if (int rc = check_tiling(*p, dtype, G)) return rc;
   const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
@@ -223,6 +231,7 @@ int attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, cons
   if (!workspace || workspace_bytes < need) return SP_ERR_WORKSPACE;
   if (!aligned16(workspace)) return SP_ERR_ALIGNMENT;
   if (!p->d_tiles) return SP_ERR_NOT_UPLOADED;
+  if (!on_plan_device(*p)) return SP_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
   if (int rc = check_tiling(*p, dtype, G)) return rc;
   const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
