@@ -186,7 +186,9 @@ typedef struct {
 } sp_fragment_info;
 
 /* Plans the fragments of a validated tree with at most max_tokens tokens
- * each (host only).  Errors: SP_ERR_INVALID_ARG (null, max_tokens < 1),
+ * each (host only).  *out receives a library-owned handle (NULL on error),
+ * freed with sp_fragment_destroy; the tree's arrays are only read during the
+ * call.  Errors: SP_ERR_INVALID_ARG (null, max_tokens < 1),
  * SP_ERR_INVALID_TREE, SP_ERR_CAP (a root path longer than max_tokens). */
 SP_API int sp_fragment_plan(const sp_tree_desc *tree, int64_t max_tokens, sp_fragments **out);
 /* Fills *info.  Errors: SP_ERR_INVALID_ARG. */
@@ -194,7 +196,12 @@ SP_API int sp_fragment_view(const sp_fragments *frag, sp_fragment_info *info);
 /* Frees the fragment plan; NULL is ignored. */
 SP_API void sp_fragment_destroy(sp_fragments *frag);
 
-/* tree_attn_fwd -- O and LSE of shared-prefix tree attention.
+/* tree_attn_fwd -- O and LSE of shared-prefix tree attention.  Query token i
+ * attends causally inside its own segment and fully to the tokens of every
+ * ancestor segment (issue #7386, "Describe the solution you'd like", third
+ * bullet; PR #7387, "Summary", second bullet); the prompt's K/V is read once
+ * for all its branches and each branch is isolated from its siblings (#7914,
+ * introduction).
  *   q   [T][Hq][D], k and v [T][Hkv][D], o [T][Hq][D]: dtype (bf16 or fp32)
  *   lse [Hq][T] fp32: natural-log sum of exp(softmax_scale * q.k) over the
  *       visible keys (the softmax normaliser, kept for the backward pass)
@@ -209,7 +216,9 @@ SP_API int sp_tree_attn_fwd(const sp_plan *plan, int32_t dtype, const void *q, c
                      const void *v, void *o, float *lse, int32_t T, int32_t Hq, int32_t Hkv,
                      int32_t D, float softmax_scale, int32_t *d_status, void *stream);
 
-/* Bytes of device workspace sp_tree_attn_bwd needs for these sizes. */
+/* Bytes of device workspace sp_tree_attn_bwd needs for these sizes:
+ * 4 * T * Hq (Delta), plus 4 * T * Hq * D (the fp32 dQ accumulator) for bf16,
+ * each rounded up to 256.  0 for T <= 0 or a non-positive size. */
 SP_API size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t Hq, int32_t D);
 
 /* tree_attn_bwd -- dQ, dK, dV of L = sum_i <O_i, dO_i> through the tree
@@ -230,7 +239,7 @@ SP_API int sp_tree_attn_bwd(const sp_plan *plan, int32_t dtype, const void *q, c
                      void *stream);
 
 /* Bytes of device workspace sp_edge_gather_bwd needs (per-token counts and
- * offsets, one int per edge). */
+ * offsets, one int per edge).  0 for a negative size. */
 SP_API size_t sp_edge_gather_bwd_workspace_bytes(int32_t T, int32_t E);
 
 /* edge_gather backward -- grad_hidden[t][:] = sum of grad_out[e][:] over the
@@ -251,7 +260,8 @@ SP_API int sp_edge_gather_bwd(int32_t dtype, const void *grad_out, int32_t E, in
                               size_t workspace_bytes, int32_t *d_status, void *stream);
 
 /* Bytes of device workspace sp_edge_logprob needs: 8 * E * ceil(V / 256)
- * (per-tile row maxima and sums) + 4 * E (label logits), each 256-aligned. */
+ * (per-tile row maxima and sums) + 4 * E (label logits), each 256-aligned.
+ * 0 for E < 0 or V < 1. */
 SP_API size_t sp_edge_logprob_workspace_bytes(int32_t E, int32_t V);
 
 /* Vocabulary head over the sampled-edge states -- the log-probability that
@@ -275,7 +285,8 @@ SP_API int sp_edge_logprob(int32_t dtype, const void *hidden_sel, int32_t E, int
                            int32_t V, const int32_t *labels, float *logprob, float *lse, void *workspace,
                            size_t workspace_bytes, int32_t *d_status, void *stream);
 
-/* Bytes of device workspace sp_edge_logprob_bwd needs: 2 * E * V (bf16 dlogits). */
+/* Bytes of device workspace sp_edge_logprob_bwd needs: 2 * E * V (bf16
+ * dlogits).  0 for E < 0 or V < 1. */
 SP_API size_t sp_edge_logprob_bwd_workspace_bytes(int32_t E, int32_t V);
 
 /* Backward of sp_edge_logprob for upstream gradients grad_logprob[e] =

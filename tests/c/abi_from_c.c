@@ -47,6 +47,9 @@ int main(void) {
   if (sp_plan_view(NULL, NULL) != SP_ERR_INVALID_ARG) return fail("null view");
   sp_plan_destroy(NULL);
   sp_fragment_destroy(NULL);
+  tree.total_tokens = (int32_t)(total + 1); /* lengths no longer add up to the token count */
+  if (sp_tree_plan(&tree, tile, kvb, order, &p) != SP_ERR_INVALID_TREE || p != NULL) return fail("wrong total");
+  tree.total_tokens = (int32_t)total;
   for (int code = 0; code >= -10; --code) {
     const char *msg = sp_status_string(code);
     if (!msg || !msg[0]) return fail("empty status string");
