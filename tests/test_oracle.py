@@ -213,6 +213,22 @@ def test_single_segment_equals_library_causal_attention():
         np.testing.assert_allclose(ours, ref.numpy(), rtol=0, atol=1e-11)
 
 
+def test_large_scores_stay_finite_and_match_the_library():
+    """Scores of several hundred (far beyond exp's range in fp64) through both routes and the backward."""
+    rng = np.random.default_rng(18)
+    q, k, v, do = _rand(rng, 60, 2, 1, 16, scale=30.0)
+    ref = _sdpa_causal(q, k, v, 0.25)
+    mask = np.tril(np.ones((60, 60), dtype=bool))
+    assert np.abs(0.25 * np.einsum("id,jd->ij", q[:, 0], k[:, 0])).max() > 800
+    O, L = A.tree_forward(q, k, v, [0], [60], [-1], 0.25)
+    O2, L2, _ = A.dense_forward(q, k, v, mask, 0.25)
+    for o, l in ((O, L), (O2, L2)):
+        assert np.isfinite(o).all() and np.isfinite(l).all()
+        np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-10)
+    for g in A.tree_backward(q, k, v, do, [0], [60], [-1], 0.25) + A.dense_backward(q, k, v, do, mask, 0.25):
+        assert np.isfinite(g).all()
+
+
 def test_star_with_one_child_equals_causal_on_concatenation():
     rng = np.random.default_rng(8)
     q, k, v, _ = _rand(rng, 50, 2, 2, 8)

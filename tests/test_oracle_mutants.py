@@ -89,6 +89,19 @@ MUTANTS = [
      "dense dK keeps only the last query head of a group"),
     ("attention", "if int(idx[p]) not in seen", "if True", "subtree key gradients count shared rows twice"),
     ("attention", "kmax = int(r[-1]) + 1", "kmax = int(r[-1])", "last visible key cut off"),
+    ("attention", "m = S.max(axis=1)\n        P = np.exp(S - m[:, None])", "m = S.max(axis=1) * 0\n        P = np.exp(S - m[:, None])",
+     "softmax without the max shift (overflows on large scores)"),
+    ("attention", "m = S.max(axis=1)\n        E = np.exp(S - m[:, None])", "m = S.max(axis=1) * 0\n        E = np.exp(S - m[:, None])",
+     "dense softmax without the max shift"),
+    ("attention", "O[:, h] = P[h] @ v[:, h // G]", "O[:, h] = P[h] @ v[:, h % k.shape[1]]", "dense route maps heads modulo"),
+    ("attention", "LSE[hs, idx[new]] = r[\"LSE\"][:, new]", "LSE[hs, idx[new]] = r[\"LSE\"][::-1][:, new]",
+     "LSE rows of a group's heads swapped"),
+    ("attention", "dQ[idx[own], hs] += r[\"dQ\"]", "dQ[idx[own], hs] += r[\"dQ\"][:, ::-1]", "dQ heads of a group swapped"),
+    ("attention", "dV[:, g] += P[h].T @ do[:, h]", "dV[:, g] += P[h] @ do[:, h]", "dense dV with P untransposed"),
+    ("plan", "raw.sort(key=lambda r: r[0])", "raw.sort(key=lambda r: r[0], reverse=True)", "tile order reversed"),
+    ("plan", "tiles.append((s, q0, q1, len(ranges), len(rng)))", "tiles.append((s, q0, q1, len(ranges), len(rng) - 1))",
+     "range count drops the causal range"),
+    ("gather", "return hidden[idx]", "return hidden[np.sort(idx)]", "gather rows sorted by source"),
     # gather
     ("gather", "if idx.size and (idx.min() < 0 or idx.max() >= T):", "if idx.size and (idx.min() < -1 or idx.max() >= T):",
      "gather accepts index -1 (NumPy would read the last row)"),
@@ -121,6 +134,15 @@ MUTANTS = [
     ("fragments", "assert int(parent[a]) in present", "assert int(parent[a]) >= -1",
      "checker does not check ancestor closure"),
 ]
+
+
+# Not planted, because they cannot change any result (equivalent mistakes):
+# descendants returned in stack order (only their maximum end and their set are
+# used); fragment entries left unsorted, or root paths taken leaf first (a
+# fragment's insertion order is already preorder: an ancestor missing from the
+# current fragment precedes its first segment and so lies on that segment's root
+# path); an index bound of T or a label bound of V (NumPy's own indexing raises
+# there); a self-parent accepted by the parent check (the depth check refuses it).
 
 
 def _cases(fn, limit=12):
