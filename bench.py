@@ -671,7 +671,9 @@ def run_reference(args):
     if rank != 0:
         return
     w = W.get(args.config)
-    r = run_oracle_sample(w, args.ref_flops, reps=args.warmup + args.steps)
+    reps = args.warmup + args.steps
+    # the whole run stays within its budget: with many steps each step's sample shrinks
+    r = run_oracle_sample(w, min(args.ref_flops, args.ref_total_flops / max(1, reps)), reps=reps)
     times = r["times"][args.warmup:]
     total = sum(times)
     value = r["useful_flops"] * len(times) / total / 1e12
@@ -702,6 +704,8 @@ def main():
     ap.add_argument("--fragment-cap", type=int, default=32768, help="token cap of the bounded-fragment summary")
     ap.add_argument("--cpu-flops", type=float, default=6e11, help="fp64 flop budget of the CPU-baseline sample")
     ap.add_argument("--ref-flops", type=float, default=1.2e11, help="fp64 flop budget per reference step")
+    ap.add_argument("--ref-total-flops", type=float, default=4e12,
+                    help="fp64 flop budget of the whole reference run (warm-up and timed steps together)")
     ap.add_argument("--_oracle-child", dest="oracle_child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child:
