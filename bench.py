@@ -39,7 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernels the library launches per call (fwd; bwd = preprocess, main, dQ; gather)
 LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 3, "gather": 1}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each tensor-core kernel,
-# from one single-pass ncu capture of this bench on a GB300 (profiles/dram_traffic_agent_tree_64k.md),
+# from one single-pass ncu capture of this bench on a GB300 (one launch of the kernel, warm-up step 2),
 # keyed by workload, with a digest of the code (comments stripped) that defines the kernel and its
 # schedule: a figure whose code has changed since the capture is reported as null.
 CSRC = os.path.join(ROOT, "shared_prefix_causal_gb300", "csrc")
