@@ -109,8 +109,8 @@ def tile_efficiency(spc, plan, G: int, pairs: int) -> dict:
     return {"fwd": round(pairs / max(fwd, 1), 4), "bwd": round(pairs / max(bwd, 1), 4)}
 
 
-def load_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def load_peaks(path=None):
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             with open(path) as f:
@@ -121,11 +121,40 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _peak_value(peaks, *keys):
-    for k in keys:
-        if k in peaks and isinstance(peaks[k], (int, float)):
-            return float(peaks[k])
+def _number(x):
+    """A plain number, or one held under value/median/mean of a small record."""
+    if isinstance(x, (int, float)) and not isinstance(x, bool):
+        return float(x)
+    if isinstance(x, dict):
+        for k in ("value", "median", "mean"):
+            if isinstance(x.get(k), (int, float)) and not isinstance(x.get(k), bool):
+                return float(x[k])
     return None
+
+
+def _peak_value(peaks, *keys):
+    """The first of ``keys`` found with a number, at the top level of ``peaks`` or one level down."""
+    if not isinstance(peaks, dict):
+        return None
+    for k in keys:
+        for d in [peaks] + [v for v in peaks.values() if isinstance(v, dict)]:
+            if k in d and _number(d[k]) is not None:
+                return _number(d[k])
+    return None
+
+
+PEAK_KEYS = {"burst": ("bf16_tflops", "bf16_tflops_burst"), "sustained": ("bf16_tflops_sustained",),
+             "hbm": ("hbm_gbs",)}
+
+
+def resolve_peaks(peaks, source):
+    """{name: (value, "measured" | "fallback")}: the measured figure where the file has a positive one,
+    else the fallback figure."""
+    out = {}
+    for name, keys in PEAK_KEYS.items():
+        v = _peak_value(peaks, *keys) if source == "measured" else None
+        out[name] = (v, "measured") if v is not None and v > 0 else (_peak_value(FALLBACK_PEAKS, *keys), "fallback")
+    return out
 
 
 class ClockSampler:
@@ -388,10 +417,8 @@ def run_gpu(args):
     f_bwd = 10.0 * D * w.hq * pairs
     ms_step = total_ms / args.steps
     value = job_throughput(f_fwd + f_bwd, ws, ms_step) / 1e12
-    peaks, peak_src = load_peaks()
-    p_burst = _peak_value(peaks, "bf16_tflops", "bf16_tflops_burst")
-    p_sust = _peak_value(peaks, "bf16_tflops_sustained") or p_burst
-    p_hbm = _peak_value(peaks, "hbm_gbs")
+    pk = resolve_peaks(*load_peaks())
+    (p_burst, src_burst), (p_sust, src_sust), (p_hbm, _) = pk["burst"], pk["sustained"], pk["hbm"]
     med_fwd, med_bwd = statistics.median(fwd_ms), statistics.median(bwd_ms)
     fwd_tflops = f_fwd / (med_fwd * 1e-3) / 1e12
     bwd_tflops = f_bwd / (med_bwd * 1e-3) / 1e12
@@ -457,13 +484,13 @@ def run_gpu(args):
             "peak": p_sust, "unit": "TFLOP/s",
             "frac": round(f_bwd / (mean_bwd * 1e-3) / 1e12 / p_sust, 4) if p_sust else None,
             "traffic": measured_traffic(args.config, "bwd_tc_kernel"), "traffic_kernel": "bwd_tc_kernel",
-            "algorithmic_bytes": algo_bwd, "peak_source": f"bf16 sustained, {peak_src}"},
+            "algorithmic_bytes": algo_bwd, "peak_source": f"bf16 sustained, {src_sust}"},
         "roofline_fwd": {
             "kernel": "tree_attn_fwd", "bound": "tensor",
             "achieved": round(f_fwd / (mean_fwd * 1e-3) / 1e12, 2), "peak": p_burst, "unit": "TFLOP/s",
             "frac": round(f_fwd / (mean_fwd * 1e-3) / 1e12 / p_burst, 4) if p_burst else None,
             "traffic": measured_traffic(args.config, "fwd_tc_kernel"), "traffic_kernel": "fwd_tc_kernel",
-            "algorithmic_bytes": algo_fwd, "peak_source": f"bf16 burst, {peak_src}"},
+            "algorithmic_bytes": algo_fwd, "peak_source": f"bf16 burst, {src_burst}"},
         "gpu_launches": args.steps * sum(LAUNCHES_PER_STEP.values() if hidden is not None
                                          else [LAUNCHES_PER_STEP["fwd"], LAUNCHES_PER_STEP["bwd"]]),
         "clocks": clk,

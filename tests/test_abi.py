@@ -387,3 +387,22 @@ def test_bench_clock_sampler_keeps_only_the_timed_window(tmp_path):
 def test_bench_clock_sampler_without_nvidia_smi_reports_nothing():
     import bench
     assert bench.ClockSampler(0).stop() is None
+
+
+@pytest.mark.parametrize("content,want", [
+    ({"hbm_gbs": 7000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1750.0},
+     {"burst": (2000.0, "measured"), "sustained": (1750.0, "measured"), "hbm": (7000.0, "measured")}),
+    ({"gb300": {"hbm_gbs": {"value": 7100}, "bf16_tflops": {"median": 1980.5}}, "clocks": {"sm_mhz": 2070}},
+     {"burst": (1980.5, "measured"), "sustained": (1700.0, "fallback"), "hbm": (7100.0, "measured")}),
+    ({"bf16_tflops": None, "hbm_gbs": "n/a"},
+     {"burst": (1900.0, "fallback"), "sustained": (1700.0, "fallback"), "hbm": (6800.0, "fallback")}),
+    ("not json", {"burst": (1900.0, "fallback"), "sustained": (1700.0, "fallback"), "hbm": (6800.0, "fallback")}),
+    (None, {"burst": (1900.0, "fallback"), "sustained": (1700.0, "fallback"), "hbm": (6800.0, "fallback")}),
+])
+def test_bench_peaks_from_the_measured_file_else_the_fallback(tmp_path, content, want):
+    import json
+    import bench
+    path = tmp_path / "peaks.json"
+    if content is not None:
+        path.write_text(content if isinstance(content, str) else json.dumps(content))
+    assert bench.resolve_peaks(*bench.load_peaks(str(path))) == want
