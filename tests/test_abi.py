@@ -158,6 +158,28 @@ def test_attention_argument_checks_fail_before_device_work():
     assert g(0, ctypes.c_void_p((1 << 20) + 2), 186, 256, fake, 4, fake, None, None) == -4
 
 
+def test_zero_sized_calls_are_no_ops_before_any_device_work():
+    """An empty tree (T = 0), no actions (E = 0) or no requested outputs return SP_OK at once:
+    nothing is read, written or launched, so null pointers are fine and no GPU is needed."""
+    e = np.zeros(0, dtype=np.int32)
+    p = spc.sp_tree_plan(e, e, e, e, 32, 128, 0)  # never uploaded
+    n9 = [None] * 9
+    for dtype in (spc.SP_BF16, spc.SP_F32):
+        assert spc._c_fwd(p.handle, dtype, *n9[:5], 0, 32, 8, 128, 0.1, None, None) == 0
+        for fn in (spc._c_bwd, spc._c_bwd_det):
+            assert fn(p.handle, dtype, *n9, None, 0, 0, 32, 8, 128, 0.1, None, None) == 0
+        assert spc._c_bwd_noalloc(p.handle, dtype, *n9, 0, 32, 8, 128, 0.1, None, None) == 0
+        assert spc._c_gather_bwd(dtype, None, 0, 256, None, 0, None, None, 0, None, None) == 0
+    assert spc._c_lmh(spc.SP_BF16, None, 0, 64, None, 96, None, None, None, None, 0, None, None) == 0
+    # backward with neither gradient requested
+    assert spc._c_lmh_bwd(spc.SP_BF16, None, 5, 64, None, 96, None, None, None, None, None, None, 0, None,
+                          None) == 0
+    # a non-empty plan still refuses T = 0
+    t = W.tiny().tree
+    q = spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 64, 128, 0)
+    assert spc._c_fwd(q.handle, spc.SP_BF16, *n9[:5], 0, 2, 2, 64, 0.1, None, None) == -2
+
+
 def test_bench_traffic_is_null_when_kernel_sources_change(monkeypatch):
     import bench
     assert bench.measured_traffic("tiny", "bwd_tc_kernel") is None  # never captured
