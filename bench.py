@@ -41,17 +41,19 @@ LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 3, "gather": 1}
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each tensor-core kernel,
 # from one single-pass ncu capture of this bench on a GB300 (one launch of the kernel, warm-up step 2),
 # keyed by workload, with a digest of the code (comments stripped) that defines the kernel and its
-# schedule: a figure whose code has changed since the capture is reported as null.
+# schedule: a figure whose code has changed since the capture is reported as null.  "file:function"
+# takes one function of a file: the planner's schedule builders decide the launch order, while the
+# canonical plan they start from is fixed bit for bit by the planner's tests.
 CSRC = os.path.join(ROOT, "shared_prefix_causal_gb300", "csrc")
 TRAFFIC_SOURCES = {
-    "fwd_tc_kernel": ("attn_fwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
-    "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp"),
+    "fwd_tc_kernel": ("attn_fwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_pairs"),
+    "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_bwd_schedule"),
 }
 MEASURED_TRAFFIC = {
-    "agent": {"fwd_tc_kernel": (813.75e6 + 510.94e6, "b87f4ad41bb9668b"),
-              "bwd_tc_kernel": (16.64e9 + 8.42e9, "740fd55f1556b1c3")},
-    "star": {"fwd_tc_kernel": (94.39e6 + 27.93e6, "b87f4ad41bb9668b"),
-             "bwd_tc_kernel": (333.02e6 + 131.47e6, "740fd55f1556b1c3")},
+    "agent": {"fwd_tc_kernel": (813.75e6 + 510.94e6, "cb788fccbf1250a9"),
+              "bwd_tc_kernel": (16.64e9 + 8.42e9, "1c4afdf5b4242bb4")},
+    "star": {"fwd_tc_kernel": (94.39e6 + 27.93e6, "cb788fccbf1250a9"),
+             "bwd_tc_kernel": (333.02e6 + 131.47e6, "1c4afdf5b4242bb4")},
 }
 
 
@@ -78,12 +80,27 @@ def _code_only(text: str) -> str:
     return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
 
 
+def _function_text(code: str, name: str) -> str:
+    """The definition of function ``name`` (signature line to closing brace) in comment-free code."""
+    import re
+    m = re.search(r"^[^\n;{}]*\b" + re.escape(name) + r"\s*\([^;{]*\)\s*\{", code, flags=re.M)
+    if m is None:
+        raise KeyError(name)
+    depth, i = 1, m.end()
+    while depth:
+        depth += {"{": 1, "}": -1}.get(code[i], 0)
+        i += 1
+    return code[m.start():i]
+
+
 def sources_digest(kernel: str) -> str:
     import hashlib
     m = hashlib.sha256()
     for f in TRAFFIC_SOURCES[kernel]:
-        with open(os.path.join(CSRC, f), encoding="utf-8") as fh:
-            m.update(_code_only(fh.read()).encode())
+        path, _, func = f.partition(":")
+        with open(os.path.join(CSRC, path), encoding="utf-8") as fh:
+            code = _code_only(fh.read())
+        m.update((_function_text(code, func) if func else code).encode())
     return m.hexdigest()[:16]
 
 
