@@ -75,70 +75,91 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
   plan.num_segments = n;
 
   // Root-path intervals per segment (inclusive of the segment itself), built
-  // from the parent's list; root id per segment; subtree ends.
-  std::vector<std::vector<Interval>> path(n);
-  std::vector<int32_t> root(n), send(n);
+  // from the parent's list and kept in one pool; the token count of each
+  // segment's strict ancestors; root id per segment; subtree ends.
+  std::vector<Interval> pool;
+  std::vector<int32_t> path_off(size_t(n) + 1, 0), root(n), send(n);
+  std::vector<int64_t> anc_tokens(n, 0);
   for (int s = 0; s < n; ++s) {
     const int32_t p = t.parent[s];
-    if (p >= 0) path[s] = path[p];
+    path_off[s] = int32_t(pool.size());
+    if (p >= 0) {
+      pool.insert(pool.end(), pool.begin() + path_off[p], pool.begin() + path_off[p + 1]);
+      anc_tokens[s] = anc_tokens[p] + t.seg_len[p];
+    }
+    std::vector<Interval> tail(pool.begin() + path_off[s], pool.end());
+    pool.resize(path_off[s]);
+    push_merged(tail, {t.seg_start[s], t.seg_start[s] + t.seg_len[s]});
+    pool.insert(pool.end(), tail.begin(), tail.end());
+    path_off[s + 1] = int32_t(pool.size());
     root[s] = p < 0 ? s : root[p];
-    push_merged(path[s], {t.seg_start[s], t.seg_start[s] + t.seg_len[s]});
     send[s] = t.seg_start[s] + t.seg_len[s];
   }
   for (int s = n - 1; s >= 0; --s)
     if (t.parent[s] >= 0) send[t.parent[s]] = std::max(send[t.parent[s]], send[s]);
 
+  // A tile reads its parent's root path, then its own segment up to the
+  // tile's end (merged into the last interval when they touch).
   struct Tile {
     int32_t seg, k, q0, q1;
     int64_t kv_total;
-    std::vector<Interval> r;
   };
+  size_t n_tiles = 0, n_ranges = 0;
+  for (int s = 0; s < n; ++s) {
+    const size_t c = size_t((int64_t(t.seg_len[s]) + tile_tokens - 1) / tile_tokens);
+    n_tiles += c;
+    n_ranges += c * size_t(1 + (t.parent[s] >= 0 ? path_off[t.parent[s] + 1] - path_off[t.parent[s]] : 0));
+  }
   std::vector<Tile> tiles;
+  tiles.reserve(n_tiles);
   for (int s = 0; s < n; ++s) {
     const int32_t a0 = t.seg_start[s], a1 = a0 + t.seg_len[s];
-    const int32_t p = t.parent[s];
     int32_t k = 0;
     for (int32_t q0 = a0; q0 < a1; q0 += tile_tokens, ++k) {
-      Tile x;
-      x.seg = s;
-      x.k = k;
-      x.q0 = q0;
-      x.q1 = std::min(a1, q0 + tile_tokens);
-      if (p >= 0) x.r = path[p];
-      push_merged(x.r, {a0, x.q1});
-      x.kv_total = 0;
-      for (auto &iv : x.r) x.kv_total += iv.second - iv.first;
-      tiles.push_back(std::move(x));
+      const int32_t q1 = std::min(a1, q0 + tile_tokens);
+      tiles.push_back({s, k, q0, q1, anc_tokens[s] + (q1 - a0)});
     }
   }
-  std::vector<int32_t> perm(tiles.size());
-  std::iota(perm.begin(), perm.end(), 0);
-  if (order == 0) {
-    std::sort(perm.begin(), perm.end(), [&](int32_t a, int32_t b) {
-      const Tile &x = tiles[a], &y = tiles[b];
-      const int32_t px = t.parent[x.seg], py = t.parent[y.seg];
-      if (root[x.seg] != root[y.seg]) return root[x.seg] < root[y.seg];
-      if (px != py) return px < py;
-      if (x.k != y.k) return x.k < y.k;
-      return x.seg < y.seg;
-    });
-  } else {
-    std::sort(perm.begin(), perm.end(), [&](int32_t a, int32_t b) {
-      const Tile &x = tiles[a], &y = tiles[b];
-      if (x.kv_total != y.kv_total) return x.kv_total > y.kv_total;
-      if (x.seg != y.seg) return x.seg < y.seg;
-      return x.k < y.k;
-    });
+  // Sort keys as two integers compared in order; every field is non-negative
+  // and below 2^31, so each pair of fields packs into one int64 without
+  // changing the order.  Order 0: (root, parent + 1) then (tile index,
+  // segment); order 1: (-kv_total) then (segment, tile index).
+  struct Key {
+    int64_t a, b;
+    int32_t tile;
+  };
+  std::vector<Key> keys(tiles.size());
+  for (size_t i = 0; i < tiles.size(); ++i) {
+    const Tile &x = tiles[i];
+    if (order == 0)
+      keys[i] = {(int64_t(root[x.seg]) << 32) | int64_t(t.parent[x.seg] + 1), (int64_t(x.k) << 32) | x.seg,
+                 int32_t(i)};
+    else
+      keys[i] = {-x.kv_total, (int64_t(x.seg) << 32) | x.k, int32_t(i)};
   }
+  std::sort(keys.begin(), keys.end(), [](const Key &x, const Key &y) { return x.a != y.a ? x.a < y.a : x.b < y.b; });
   plan.tiles.clear();
   plan.ranges.clear();
+  plan.tiles.reserve(5 * tiles.size());
+  plan.ranges.reserve(2 * n_ranges);
   plan.max_ranges_per_tile = 0;
-  for (int32_t i : perm) {
-    const Tile &x = tiles[i];
+  for (const Key &key : keys) {
+    const Tile &x = tiles[key.tile];
+    const int32_t p = t.parent[x.seg], a0 = t.seg_start[x.seg];
     const int32_t rb = int32_t(plan.ranges.size() / 2);
-    const int32_t rc = int32_t(x.r.size());
-    plan.tiles.insert(plan.tiles.end(), {x.seg, x.q0, x.q1, rb, rc});
-    for (auto &iv : x.r) plan.ranges.insert(plan.ranges.end(), {iv.first, iv.second});
+    if (p >= 0)
+      for (int32_t j = path_off[p]; j < path_off[p + 1]; ++j) {
+        plan.ranges.push_back(pool[j].first);
+        plan.ranges.push_back(pool[j].second);
+      }
+    if (!plan.ranges.empty() && int32_t(plan.ranges.size() / 2) > rb && plan.ranges.back() == a0) {
+      plan.ranges.back() = x.q1;
+    } else {
+      plan.ranges.push_back(a0);
+      plan.ranges.push_back(x.q1);
+    }
+    const int32_t rc = int32_t(plan.ranges.size() / 2) - rb;
+    for (int32_t v : {x.seg, x.q0, x.q1, rb, rc}) plan.tiles.push_back(v);
     plan.max_ranges_per_tile = std::max(plan.max_ranges_per_tile, rc);
   }
 

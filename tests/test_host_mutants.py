@@ -43,21 +43,28 @@ MUTANTS = [
      "closed parents accepted"),
     ("plan.cpp", "send[t.parent[s]] = std::max(send[t.parent[s]], send[s]);", "send[t.parent[s]] = send[s];",
      "subtree end from the first child only"),
-    ("plan.cpp", "x.q1 = std::min(a1, q0 + tile_tokens);", "x.q1 = q0 + tile_tokens;",
+    ("plan.cpp", "const int32_t q1 = std::min(a1, q0 + tile_tokens);", "const int32_t q1 = q0 + tile_tokens;",
      "tiles cross the segment end"),
-    ("plan.cpp", "if (x.k != y.k) return x.k < y.k;", "if (x.k != y.k) return x.k > y.k;",
-     "order 0 by descending tile index"),
-    ("plan.cpp", "if (root[x.seg] != root[y.seg]) return root[x.seg] < root[y.seg];", "",
+    ("plan.cpp", "(int64_t(x.k) << 32) | x.seg,", "(int64_t(x.seg) << 32) | x.k,",
+     "order 0 by segment before tile index (siblings not interleaved)"),
+    ("plan.cpp", "{(int64_t(root[x.seg]) << 32) | int64_t(t.parent[x.seg] + 1),", "{int64_t(t.parent[x.seg] + 1),",
      "order 0 ignores the tree a tile belongs to"),
-    ("plan.cpp", "if (x.kv_total != y.kv_total) return x.kv_total > y.kv_total;",
-     "if (x.kv_total != y.kv_total) return x.kv_total < y.kv_total;", "order 1 shortest first"),
+    ("plan.cpp", "keys[i] = {-x.kv_total,", "keys[i] = {x.kv_total,", "order 1 shortest first"),
+    ("plan.cpp", "return x.a != y.a ? x.a < y.a : x.b < y.b;", "return x.a < y.a;", "ties of the first key left unordered"),
     ("plan.cpp", "if (cx != cy) return cx > cy;", "if (cx != cy) return cx < cy;", "backward table ascending"),
     ("plan.cpp", "blocks.push_back({s, k0, std::min(a1, k0 + kv_block), k0, send[s]});",
      "blocks.push_back({s, k0, std::min(a1, k0 + kv_block), a0, send[s]});",
      "block queries from the segment start"),
     ("plan.cpp", "const int32_t rb = int32_t(plan.ranges.size() / 2);",
      "const int32_t rb = int32_t(plan.ranges.size() / 2) - 1;", "range begin off by one"),
-    ("plan.cpp", "push_merged(x.r, {a0, x.q1});", "push_merged(x.r, {a0, a1});", "own range to the segment end"),
+    ("plan.cpp", "      plan.ranges.back() = x.q1;\n    } else {\n      plan.ranges.push_back(a0);\n"
+     "      plan.ranges.push_back(x.q1);",
+     "      plan.ranges.back() = a0 + t.seg_len[x.seg];\n    } else {\n      plan.ranges.push_back(a0);\n"
+     "      plan.ranges.push_back(a0 + t.seg_len[x.seg]);", "own range to the segment end"),
+    ("plan.cpp", "int32_t(plan.ranges.size() / 2) > rb && plan.ranges.back() == a0",
+     "int32_t(plan.ranges.size() / 2) > rb && false", "own range not merged into a touching parent range"),
+    ("plan.cpp", "anc_tokens[s] = anc_tokens[p] + t.seg_len[p];", "anc_tokens[s] = t.seg_len[p];",
+     "longest-first key counts the parent only"),
     ("fragments.cpp", "if (!cur_seg.empty() && cur_tokens + extra > cap) {",
      "if (!cur_seg.empty() && cur_tokens + extra >= cap) {", "a fragment never fills the cap exactly"),
     ("fragments.cpp", "      emit();\n      extra = path_tokens;", "      emit();",
