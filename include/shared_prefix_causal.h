@@ -117,8 +117,8 @@ typedef struct {
  *                (shared ancestor K/V stays in L2); 1: longest KV walk first.
  *   *out         receives the new plan (NULL on error).
  * Errors: SP_ERR_INVALID_ARG (null pointers, bad sizes), SP_ERR_INVALID_TREE
- * (checks listed in sp_tree_desc; issue #7914: unsupported layouts "fail
- * before execution"). */
+ * (checks listed in sp_tree_desc; #7914, introduction: unsupported layouts
+ * are refused before anything runs). */
 SP_API int sp_tree_plan(const sp_tree_desc *tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
                  sp_plan **out);
 
