@@ -1,0 +1,98 @@
+"""Precision study for FP8 variants of the attention products (CPU only).
+
+The forward's tolerance is 1e-2 relative L2 on O against fp64.  This study
+emulates the rounding of the tensor-core forward on one root-to-leaf call of
+the GRPO star workload: bf16 operands, fp32 scores and softmax, P rounded to
+bf16 for P V, fp32 accumulation, O rounded to bf16.  Then it replaces operands
+with e4m3 (torch's own float8_e4m3fn rounding) to see which products could move
+to FP8 within that tolerance.  Every variant is compared with the oracle's
+plain causal attention in fp64.
+
+Findings pinned here:
+  * the current precision sits well inside the bound;
+  * P in e4m3 alone exceeds it about two-fold, with or without per-32-key
+    block scales.  e4m3 keeps 3 mantissa bits, so range scaling cannot help;
+  * Q and K in e4m3 stay inside it, with little margin.
+So an FP8 P V product cannot meet the forward's tolerance, and an FP8 Q K^T
+product would leave almost none of it.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as A
+from oracle import tree as OT
+
+
+def _e4m3(x, scale):
+    t = torch.from_numpy(np.asarray(x / scale, dtype=np.float32)).to(torch.float8_e4m3fn)
+    return t.float().numpy().astype(np.float64) * scale
+
+
+def _bf16(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+def _f32(x):
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def _p_block_e4m3(P, block=32):
+    out = np.empty_like(P)
+    for j in range(0, P.shape[1], block):
+        blk = P[:, j:j + block]
+        sc = 2.0 ** np.ceil(np.log2(np.maximum(blk.max(1, keepdims=True), 1e-30) / 448))
+        out[:, j:j + block] = _e4m3(blk, sc)
+    return out
+
+
+def _emulated_forward(q, k, v, scale, qk8=False, p8=None):
+    n = q.shape[0]
+    if qk8:
+        q, k = _e4m3(q, np.abs(q).max() / 448), _e4m3(k, np.abs(k).max() / 448)
+    S = _f32(scale * (q @ k.T))
+    S[np.triu_indices(n, 1)] = -np.inf
+    P = _f32(np.exp(S - S.max(1, keepdims=True)))
+    l = P.sum(1, keepdims=True)
+    if p8 == "row":
+        Pq = _e4m3(P, 1.0 / 256)  # P in [0, 1], scaled into e4m3's range
+    elif p8 == "block":
+        Pq = _p_block_e4m3(P)
+    else:
+        Pq = _bf16(P)
+    return _bf16(_f32(Pq @ v) / l)
+
+
+@pytest.fixture(scope="module")
+def case():
+    w = W.grpo_star()
+    x = W.draw_tensors(w, "bf16")
+    t = w.tree
+    idx = OT.path_tokens(t.seg_start, t.seg_len, t.parent, OT.leaves(t.parent)[0])
+    q = x["q"][idx, 0].double().numpy()
+    k = x["k"][idx, 0].double().numpy()
+    v = x["v"][idx, 0].double().numpy()
+    ref, _ = A.causal_rows(q, k, v, np.arange(len(idx)), w.softmax_scale)
+    return q, k, v, w.softmax_scale, ref
+
+
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / np.linalg.norm(b))
+
+
+def test_current_precision_is_well_inside_the_forward_tolerance(case):
+    q, k, v, scale, ref = case
+    assert _rel(_emulated_forward(q, k, v, scale), ref) < 4e-3
+
+
+@pytest.mark.parametrize("p8", ["row", "block"])
+def test_e4m3_p_exceeds_the_forward_tolerance(case, p8):
+    q, k, v, scale, ref = case
+    assert _rel(_emulated_forward(q, k, v, scale, p8=p8), ref) > 1.5e-2
+
+
+def test_e4m3_q_and_k_stay_inside_it_with_little_margin(case):
+    q, k, v, scale, ref = case
+    err = _rel(_emulated_forward(q, k, v, scale, qk8=True), ref)
+    assert 5e-3 < err < 1e-2
