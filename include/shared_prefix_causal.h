@@ -128,8 +128,8 @@ SP_API int sp_plan_view(const sp_plan *plan, sp_plan_info *info);
 /* Copies the plan tables to device memory owned by the plan (a cudaMalloc on
  * the current device and an async copy on `stream`).  Must precede the first
  * attention call with this plan; repeat calls are no-ops.  The first upload
- * (this call or sp_plan_upload_to) builds the device tables inside the plan, so
- * one thread must make it; after that the plan is read-only and any number of
+ * (this call or sp_plan_upload_to), or sp_plan_device_bytes, builds the device
+ * tables inside the plan, so one thread must make those calls; after that the plan is read-only and any number of
  * calls on any streams of that device may use it at once.
  * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA. */
 SP_API int sp_plan_upload(sp_plan *plan, void *stream);
