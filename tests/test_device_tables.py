@@ -1,0 +1,141 @@
+"""The tables the kernels read, checked on the CPU.
+
+At upload the library builds, from the canonical plan, the forward's work
+list and the backward's launch order:
+  * pairs [n][4] = {tile_a, tile_b or -1, first entry, entry count}: tiles
+    2i and 2i+1 of the schedule share one CTA;
+  * pblk [m][4] = {kb, end_a or 0, end_b or 0, causal bits}: the pair's
+    128-key blocks merged by start.  Tile t reads keys [kb, min(kb + 128,
+    end_t)) of an entry whose end_t is non-zero, and only keys j <= its query
+    i when bit t is set;
+  * bwd_sched: the backward table's rows in launch order (latest run end
+    first, longest run first within a run end), with the runs' sum and maximum.
+These checks hold the tables to that reading, to the forward kernel's own
+validity test, and to the canonical plan.  The tables come from the host-only
+build of the planner (no CUDA).
+"""
+import shutil
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+from host_planner import Host, build_host_library, original_objects
+
+pytestmark = pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+BLOCK = 128
+
+
+def _merge(ivs):
+    out = []
+    for a, b in sorted(ivs):
+        if out and out[-1][1] == a:
+            out[-1] = (out[-1][0], b)
+        else:
+            out.append((a, b))
+    return out
+
+
+def check_device_tables(T, d):
+    """Raises AssertionError where the tables break the kernels' reading of them."""
+    tiles, ranges, pairs, pblk = d["tiles"], d["ranges"], d["pairs"], d["pblk"]
+    nt = len(tiles)
+    assert len(pairs) == (nt + 1) // 2
+    begin = 0
+    for i, (ta, tb, b0, cnt) in enumerate(pairs):
+        assert (ta, tb) == (2 * i, 2 * i + 1 if 2 * i + 1 < nt else -1)
+        assert b0 == begin and cnt >= 1
+        begin += cnt
+    assert begin == len(pblk)
+    # the forward kernel's own test of each entry (tile b absent: end_b must be 0)
+    tb_of = np.repeat(pairs[:, 1], pairs[:, 3]) if len(pairs) else np.zeros(0, np.int32)
+    kb, ea, eb = pblk[:, 0], pblk[:, 1], pblk[:, 2]
+    assert ((0 <= kb) & (kb < T) & (ea <= T) & (eb <= T) & ((ea > kb) | (eb > kb))).all()
+    assert (((ea == 0) | (ea > kb)) & ((eb == 0) | (eb > kb)) & ((tb_of >= 0) | (eb == 0))).all()
+    assert ((tiles[:, 1] >= 0) & (tiles[:, 1] < tiles[:, 2]) & (tiles[:, 2] <= T)).all()
+    for ta, tb, b0, cnt in pairs:
+        ent = pblk[b0:b0 + cnt]
+        assert (np.diff(ent[:, 0]) > 0).all(), "entries not merged by block start"
+        for x, t in ((0, ta), (1, tb)):
+            if t < 0:
+                assert not (ent[:, 3] & 2).any()
+                continue
+            _, _, _, rb, rc = tiles[t]
+            want = [tuple(map(int, ranges[r])) for r in range(rb, rb + rc)]
+            last = want[-1]
+            end = ent[:, 1 + x]
+            causal = ((ent[:, 3] >> x) & 1).astype(bool)
+            assert not causal[end == 0].any()
+            sel = end > 0
+            k0 = ent[sel, 0].astype(np.int64)
+            k1 = np.minimum(k0 + BLOCK, end[sel])
+            assert (causal[sel] == ((k0 >= last[0]) & (k1 <= last[1]))).all(), "causal flag off the own range"
+            assert (k1[:-1] <= k0[1:]).all(), "a key read twice"
+            cut = np.nonzero(k1[:-1] != k0[1:])[0]  # merged runs of the covered blocks
+            got = list(zip(np.r_[k0[:1], k0[cut + 1]].tolist(), np.r_[k1[cut], k1[-1:]].tolist()))
+            assert got == _merge(want), "blocks do not cover the tile's ranges exactly"
+    bwd, sched = d["bwd"], d["bwd_sched"]
+    assert sorted(map(tuple, sched.tolist())) == sorted(map(tuple, bwd.tolist()))
+    runs = sched[:, 4] - sched[:, 3]
+    assert (np.diff(sched[:, 4]) <= 0).all(), "run ends not latest first"
+    for i in range(len(sched) - 1):
+        if sched[i, 4] == sched[i + 1, 4]:
+            assert runs[i] >= runs[i + 1], "runs of one end not longest first"
+            if runs[i] == runs[i + 1]:
+                assert sched[i, 1] < sched[i + 1, 1], "ties not in canonical order"
+    assert d["run_sum"] == int(runs.sum()) and d["run_max"] == (int(runs.max()) if len(runs) else 0)
+
+
+@pytest.fixture(scope="module")
+def host(tmp_path_factory):
+    d = tmp_path_factory.mktemp("device_tables")
+    return build_host_library(original_objects(d), d / "lib")
+
+
+def _tables(host, t, tile, order=0):
+    d = host.device_tables(t.seg_start, t.seg_len, t.parent, t.depth, tile, BLOCK, order)
+    assert not isinstance(d, int), f"refused ({d})"
+    return d
+
+
+@pytest.mark.parametrize("name", ["tiny", "star", "agent", "forest", "long"])
+@pytest.mark.parametrize("order", [0, 1])
+def test_workload_tables(host, name, order):
+    w = W.get(name)
+    check_device_tables(w.T, _tables(host, w.tree, 128 // (w.hq // w.hkv), order))
+
+
+def test_random_tree_tables(host):
+    rng = np.random.default_rng(8)
+    for _ in range(80):
+        t = W.random_small_tree(rng, max_segments=12, max_len=400)
+        check_device_tables(t.total_tokens, _tables(host, t, int(rng.choice([16, 32, 64, 128])),
+                                                     int(rng.integers(0, 2))))
+
+
+def test_single_tile_and_empty_plans(host):
+    one = W.tree_from_preorder([40], [-1])
+    d = _tables(host, one, 128)
+    assert d["pairs"].tolist() == [[0, -1, 0, 1]] and d["pblk"].tolist() == [[0, 40, 0, 1]]
+    check_device_tables(40, d)
+    empty = host.device_tables([], [], [], [], 128, BLOCK, 0)
+    assert len(empty["pairs"]) == 0 and len(empty["bwd_sched"]) == 0 and empty["run_max"] == 0
+
+
+def test_the_checks_catch_broken_tables(host):
+    t = W.tiny().tree
+    good = _tables(host, t, 32)
+    check_device_tables(t.total_tokens, good)
+    breaks = [
+        lambda d: d["pblk"].__setitem__((0, 3), d["pblk"][0, 3] ^ 1),        # a causal bit flipped
+        lambda d: d["pblk"].__setitem__((0, 1), d["pblk"][0, 1] - 1),        # a block end cut short
+        lambda d: d["pairs"].__setitem__((0, 3), d["pairs"][0, 3] - 1),      # an entry dropped from a pair
+        lambda d: d["bwd_sched"].__setitem__(slice(None), d["bwd_sched"][::-1].copy()),  # launch order reversed
+        lambda d: d.__setitem__("run_max", d["run_max"] + 1),
+    ]
+    for brk in breaks:
+        bad = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in good.items()}
+        brk(bad)
+        with pytest.raises(AssertionError):
+            check_device_tables(t.total_tokens, bad)

@@ -1,17 +1,15 @@
 """The planner tests catch planted mistakes in the library's host C++.
 
 Each case plants one plausible mistake in a copy of ``plan.cpp`` (tree
-validation, tiling, range merging, ordering, the backward table) or
+validation, tiling, range merging, ordering, the backward table, the forward
+pairs and the backward launch order built at upload) or
 ``fragments.cpp`` (the bounded fragment planner).  The copy is built with g++
 into a small host-only library, together with ``tests/c/planner_shim.cpp``.
 The case then runs the checks the planner's parity tests make (hand-derived
 plans, the oracle's planner and fragment planner on random trees, accepted and
 refused trees) and expects at least one to fail.  No GPU, no CUDA.
 """
-import ctypes
-import os
 import shutil
-import subprocess
 
 import numpy as np
 import pytest
@@ -21,9 +19,8 @@ from oracle import fragments as OF
 from oracle import plan as OP
 from oracle import tree as OT
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-CSRC = os.path.join(ROOT, "shared_prefix_causal_gb300", "csrc")
-SHIM = os.path.join(ROOT, "tests", "c", "planner_shim.cpp")
+from host_planner import build_host_library, original_objects
+
 
 pytestmark = pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
 
@@ -65,6 +62,22 @@ MUTANTS = [
      "int32_t(plan.ranges.size() / 2) > rb && false", "own range not merged into a touching parent range"),
     ("plan.cpp", "anc_tokens[s] = anc_tokens[p] + t.seg_len[p];", "anc_tokens[s] = t.seg_len[p];",
      "longest-first key counts the parent only"),
+    ("plan.cpp", "out.push_back({kb, e, r == tl[4] - 1});", "out.push_back({kb, e, r == 0});",
+     "forward blocks flagged causal on the first range"),
+    ("plan.cpp", "for (int32_t kb = a; kb < e; kb += block_keys)", "for (int32_t kb = a; kb < e; kb += block_keys / 2)",
+     "forward blocks overlap"),
+    ("plan.cpp", "const int32_t tb = t + 1 < nt ? t + 1 : -1;", "const int32_t tb = t + 1 < nt ? t + 1 : t;",
+     "an odd last tile paired with itself"),
+    ("plan.cpp", "(i < ba.size() && ba[i].kb < bb[j].kb)", "(i < ba.size() && ba[i].kb <= bb[j].kb)",
+     "blocks of both tiles at one start not merged"),
+    ("plan.cpp", "flags = (ba[i].causal ? 1 : 0) | (bb[j].causal ? 2 : 0);", "flags = ba[i].causal ? 1 : 0;",
+     "merged blocks lose the second tile's causal bit"),
+    ("plan.cpp", "return b[5 * x + 4] > b[5 * y + 4];", "return b[5 * x + 4] < b[5 * y + 4];",
+     "backward launch order by earliest run end"),
+    ("plan.cpp", "    return len(x) > len(y);", "    return len(x) < len(y);", "backward runs of one end shortest first"),
+    ("plan.cpp", "plan.bwd_run_max = std::max(plan.bwd_run_max, len(i));", "plan.bwd_run_max = len(i);",
+     "longest backward run mis-counted"),
+    ("plan.cpp", "plan.bwd_run_sum += len(i);", "plan.bwd_run_sum = len(i);", "backward run sum mis-counted"),
     ("fragments.cpp", "if (!cur_seg.empty() && cur_tokens + extra > cap) {",
      "if (!cur_seg.empty() && cur_tokens + extra >= cap) {", "a fragment never fills the cap exactly"),
     ("fragments.cpp", "      emit();\n      extra = path_tokens;", "      emit();",
@@ -80,93 +93,6 @@ MUTANTS = [
     ("fragments.cpp", "      local[s] = -1;\n      in_cur[s] = 0;", "      local[s] = -1;",
      "segments of a closed fragment still counted as present"),
 ]
-
-
-class _Desc(ctypes.Structure):
-    _fields_ = [("num_segments", ctypes.c_int32), ("total_tokens", ctypes.c_int32)] + \
-               [(n, ctypes.POINTER(ctypes.c_int32)) for n in ("seg_start", "seg_len", "parent", "depth")]
-
-
-class _FragInfo(ctypes.Structure):
-    _fields_ = [("num_fragments", ctypes.c_int32), ("num_entries", ctypes.c_int32),
-                ("physical_tokens", ctypes.c_int64), ("fragment_tokens", ctypes.c_int64)] + \
-               [(n, ctypes.POINTER(ctypes.c_int32)) for n in ("offsets", "tokens", "seg", "owned", "local_parent",
-                                                              "local_start")]
-
-
-class Host:
-    """ctypes view of one host-only build."""
-
-    def __init__(self, path):
-        self.lib = ctypes.CDLL(path)
-        self.lib.shim_plan.restype = ctypes.c_void_p
-        self.lib.shim_plan.argtypes = [ctypes.POINTER(_Desc), ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                       ctypes.POINTER(ctypes.c_int32)]
-        self.lib.shim_rows.restype = ctypes.c_int32
-        self.lib.shim_rows.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.POINTER(ctypes.c_int32))]
-        self.lib.shim_free.argtypes = [ctypes.c_void_p]
-        self.lib.sp_fragment_plan.argtypes = [ctypes.POINTER(_Desc), ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)]
-        self.lib.sp_fragment_view.argtypes = [ctypes.c_void_p, ctypes.POINTER(_FragInfo)]
-        self.lib.sp_fragment_destroy.argtypes = [ctypes.c_void_p]
-
-    @staticmethod
-    def _desc(st, ln, par, dep, total=None):
-        arrs = [np.ascontiguousarray(np.asarray(a, dtype=np.int32)) for a in (st, ln, par, dep)]
-        total = int(arrs[1].sum()) if total is None else total
-        return _Desc(len(arrs[0]), total, *[a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) for a in arrs]), arrs
-
-    def plan(self, st, ln, par, dep, tile, kvb, order, total=None):
-        d, keep = self._desc(st, ln, par, dep, total)
-        rc = ctypes.c_int32()
-        h = self.lib.shim_plan(ctypes.byref(d), tile, kvb, order, ctypes.byref(rc))
-        if rc.value:
-            return rc.value
-        out = []
-        for which, w in ((0, 5), (1, 2), (2, 5)):
-            ptr = ctypes.POINTER(ctypes.c_int32)()
-            n = self.lib.shim_rows(h, which, ctypes.byref(ptr))
-            out.append(np.ctypeslib.as_array(ptr, shape=(n * w,)).reshape(n, w).copy() if n else
-                       np.zeros((0, w), dtype=np.int32))
-        self.lib.shim_free(h)
-        return tuple(out)
-
-    def fragments(self, st, ln, par, dep, cap):
-        d, keep = self._desc(st, ln, par, dep)
-        h = ctypes.c_void_p()
-        rc = self.lib.sp_fragment_plan(ctypes.byref(d), cap, ctypes.byref(h))
-        if rc:
-            return rc
-        info = _FragInfo()
-        assert self.lib.sp_fragment_view(h, ctypes.byref(info)) == 0
-        get = lambda p, n: np.ctypeslib.as_array(p, shape=(n,)).copy() if n else np.zeros(0, np.int32)  # noqa: E731
-        ne, nf = info.num_entries, info.num_fragments
-        out = {k: get(getattr(info, k), ne) for k in ("seg", "owned", "local_parent", "local_start")}
-        out["offsets"], out["tokens"] = get(info.offsets, nf + 1), get(info.tokens, nf)
-        self.lib.sp_fragment_destroy(h)
-        return out
-
-
-_CXX = ["g++", "-std=c++17", "-O0", "-fPIC", "-fvisibility=hidden", "-I", CSRC]
-
-
-def _compile(src, obj):
-    subprocess.run(_CXX + ["-c", str(src), "-o", str(obj)], check=True, capture_output=True, text=True)
-    return str(obj)
-
-
-def _build(objs, d, mutant=None):
-    """A host-only library: the original objects, with the mutated file (if any) recompiled."""
-    d.mkdir()
-    parts = dict(objs)
-    if mutant:
-        f, old, new = mutant[:3]
-        text = open(os.path.join(CSRC, f), encoding="utf-8").read()
-        assert text.count(old) == 1, f"{f}: the planted text must occur exactly once: {old!r}"
-        (d / f).write_text(text.replace(old, new))
-        parts[f] = _compile(d / f, d / (f + ".o"))
-    out = str(d / "libhost.so")
-    subprocess.run(["g++", "-shared", *parts.values(), "-o", out], check=True, capture_output=True, text=True)
-    return Host(out)
 
 
 def _expected_fragment_tables(t, frags):
@@ -197,6 +123,12 @@ def _battery(host):
         @staticmethod
         def plan(*a, **k):
             r = host.plan(*a, **k)
+            assert not isinstance(r, int), f"a valid tree was refused (status {r})"
+            return r
+
+        @staticmethod
+        def device_tables(*a):
+            r = host.device_tables(*a)
             assert not isinstance(r, int), f"a valid tree was refused (status {r})"
             return r
 
@@ -236,6 +168,13 @@ def _battery(host):
     for a, total in bad:
         assert host.plan(*a, 32, 32, 0, total=total) == -1
     assert host.fragments(*args, 127) == -10
+    # the tables the kernels read, as the first upload builds them
+    from test_device_tables import check_device_tables
+    for name in ("tiny", "star"):
+        w = W.get(name)
+        wt = w.tree
+        check_device_tables(w.T, Ok.device_tables(wt.seg_start, wt.seg_len, wt.parent, wt.depth,
+                                                  128 // (w.hq // w.hkv), 128, 0))
     rng = np.random.default_rng(5)
     for _ in range(40):
         r = W.random_small_tree(rng, max_segments=12, max_len=30)
@@ -254,19 +193,17 @@ def _battery(host):
 @pytest.fixture(scope="module")
 def objects(tmp_path_factory):
     d = tmp_path_factory.mktemp("host_mutants")
-    objs = {f: _compile(os.path.join(CSRC, f), d / (f + ".o")) for f in ("plan.cpp", "fragments.cpp")}
-    objs["shim"] = _compile(SHIM, d / "shim.o")
-    return d, objs
+    return d, original_objects(d)
 
 
 def test_unmutated_host_code_passes_the_battery(objects):
     d, objs = objects
-    _battery(_build(objs, d / "original"))
+    _battery(build_host_library(objs, d / "original"))
 
 
 @pytest.mark.parametrize("mutant", MUTANTS, ids=[f"{m[0]}: {m[3]}" for m in MUTANTS])
 def test_planted_host_mistake_is_caught(objects, mutant):
     d, objs = objects
-    host = _build(objs, d / f"m{MUTANTS.index(mutant)}", mutant)
+    host = build_host_library(objs, d / f"m{MUTANTS.index(mutant)}", mutant)
     with pytest.raises(AssertionError):
         _battery(host)
