@@ -34,6 +34,7 @@ sampled action through the vocabulary projection, and its backward),
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
 against brute force, library routines, finite differences or invariants; no
-function is "parity unpinned".
+function is "parity unpinned".  ``tests/test_oracle_mutants.py`` plants
+mistakes in a copy of this package and checks that some pin fails for each.
 """
 from . import tree, plan, attention, gather, lm_head, fragments  # noqa: F401
