@@ -118,7 +118,9 @@ typedef struct {
  *   *out         receives the new plan (NULL on error).
  * Errors: SP_ERR_INVALID_ARG (null pointers, bad sizes), SP_ERR_INVALID_TREE
  * (checks listed in sp_tree_desc; #7914, introduction: unsupported layouts
- * are refused before anything runs). */
+ * are refused before anything runs), SP_ERR_UNSUPPORTED (the plan would hold
+ * more than 2^30 root-path intervals or tile ranges: its tables are indexed
+ * in int32; only very deep trees whose paths do not merge come near this). */
 SP_API int sp_tree_plan(const sp_tree_desc *tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
                  sp_plan **out);
 

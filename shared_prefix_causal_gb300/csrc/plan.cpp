@@ -22,12 +22,9 @@ namespace {
 
 using Interval = std::pair<int32_t, int32_t>;
 
-void push_merged(std::vector<Interval> &v, Interval x) {
-  if (!v.empty() && v.back().second == x.first)
-    v.back().second = x.second;
-  else
-    v.push_back(x);
-}
+// Largest number of root-path intervals, or of tile ranges, a plan may hold
+// (its tables are indexed in int32).
+constexpr int64_t kMaxEntries = int64_t(1) << 30;
 
 int validate_impl(const sp_tree_desc &t) {
   const int n = t.num_segments;
@@ -74,26 +71,43 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
   plan.total_tokens = t.total_tokens;
   plan.num_segments = n;
 
-  // Root-path intervals per segment (inclusive of the segment itself), built
-  // from the parent's list and kept in one pool; the token count of each
-  // segment's strict ancestors; root id per segment; subtree ends.
+  // Intervals of each segment's root path: the parent's, then the segment
+  // itself, merged into the parent's last interval when it starts where that
+  // one ends (a first child, placed right after its parent).  A tile's ranges
+  // are its segment's root path cut at the tile's end, so they number the
+  // same.  Both totals are counted first: the plan's tables are indexed in
+  // int32, and a tree whose tables would pass kMaxEntries entries (possible
+  // for deep trees whose paths do not merge) is refused before anything is
+  // allocated.
+  std::vector<int32_t> path_len(n);
+  std::vector<char> merges(n);
+  int64_t pool_total = 0, range_total = 0;
+  for (int s = 0; s < n; ++s) {
+    const int32_t p = t.parent[s];
+    merges[s] = p >= 0 && t.seg_start[p] + t.seg_len[p] == t.seg_start[s];
+    path_len[s] = (p >= 0 ? path_len[p] : 0) + (merges[s] ? 0 : 1);
+    pool_total += path_len[s];
+    range_total += (int64_t(t.seg_len[s]) + tile_tokens - 1) / tile_tokens * path_len[s];
+  }
+  if (pool_total > kMaxEntries || range_total > kMaxEntries) return SP_ERR_UNSUPPORTED;
   std::vector<Interval> pool;
+  pool.reserve(size_t(pool_total));
   std::vector<int32_t> path_off(size_t(n) + 1, 0), root(n), send(n);
   std::vector<int64_t> anc_tokens(n, 0);
   for (int s = 0; s < n; ++s) {
-    const int32_t p = t.parent[s];
+    const int32_t p = t.parent[s], a0 = t.seg_start[s], a1 = a0 + t.seg_len[s];
     path_off[s] = int32_t(pool.size());
     if (p >= 0) {
       pool.insert(pool.end(), pool.begin() + path_off[p], pool.begin() + path_off[p + 1]);
       anc_tokens[s] = anc_tokens[p] + t.seg_len[p];
     }
-    std::vector<Interval> tail(pool.begin() + path_off[s], pool.end());
-    pool.resize(path_off[s]);
-    push_merged(tail, {t.seg_start[s], t.seg_start[s] + t.seg_len[s]});
-    pool.insert(pool.end(), tail.begin(), tail.end());
+    if (merges[s])
+      pool.back().second = a1;
+    else
+      pool.push_back({a0, a1});
     path_off[s + 1] = int32_t(pool.size());
     root[s] = p < 0 ? s : root[p];
-    send[s] = t.seg_start[s] + t.seg_len[s];
+    send[s] = a1;
   }
   for (int s = n - 1; s >= 0; --s)
     if (t.parent[s] >= 0) send[t.parent[s]] = std::max(send[t.parent[s]], send[s]);
@@ -104,12 +118,8 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
     int32_t seg, k, q0, q1;
     int64_t kv_total;
   };
-  size_t n_tiles = 0, n_ranges = 0;
-  for (int s = 0; s < n; ++s) {
-    const size_t c = size_t((int64_t(t.seg_len[s]) + tile_tokens - 1) / tile_tokens);
-    n_tiles += c;
-    n_ranges += c * size_t(1 + (t.parent[s] >= 0 ? path_off[t.parent[s] + 1] - path_off[t.parent[s]] : 0));
-  }
+  size_t n_tiles = 0;
+  for (int s = 0; s < n; ++s) n_tiles += size_t((int64_t(t.seg_len[s]) + tile_tokens - 1) / tile_tokens);
   std::vector<Tile> tiles;
   tiles.reserve(n_tiles);
   for (int s = 0; s < n; ++s) {
@@ -141,7 +151,7 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
   plan.tiles.clear();
   plan.ranges.clear();
   plan.tiles.reserve(5 * tiles.size());
-  plan.ranges.reserve(2 * n_ranges);
+  plan.ranges.reserve(2 * size_t(range_total));
   plan.max_ranges_per_tile = 0;
   for (const Key &key : keys) {
     const Tile &x = tiles[key.tile];

@@ -107,6 +107,33 @@ def test_plan_rejects_invalid_tree(mutate):
     assert e.value.code == -1
 
 
+def _comb(levels):
+    """A chain whose next node is each node's second child (after a one-token leaf): no root path
+    merges, so the plan's interval tables grow with the square of the depth."""
+    lens, pars, chain = [], [], -1
+    for _ in range(levels):
+        node = len(lens)
+        lens.append(1)
+        pars.append(chain)
+        lens.append(1)
+        pars.append(node)  # the leaf, first child of the node
+        chain = node
+    return W.tree_from_preorder(lens, pars)
+
+
+def test_plan_refuses_trees_whose_tables_overflow_int32_indexing():
+    t = _comb(33000)  # about 1.09e9 root-path intervals, over the 2^30 limit
+    with pytest.raises(spc.SPError) as e:
+        spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 128, 128, 0)
+    assert e.value.code == -3
+    small = _comb(300)
+    got = _plan_tables(small, 128, 128, 0)
+    want = OP.build(small.seg_start, small.seg_len, small.parent, 128, 128, 0)
+    for a, b in zip((got["tiles"], got["ranges"], got["bwd"]), want):
+        assert np.array_equal(a, b)
+    assert got["max_ranges_per_tile"] == 300
+
+
 def test_plan_rejects_bad_arguments():
     a = _desc(W.tiny().tree)
     for tt, kb, order in ((0, 128, 0), (32, 0, 0), (32, 128, 2)):

@@ -26,7 +26,10 @@ pytestmark = pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
 
 # (file, text in it, replacement, what the mistake is)
 MUTANTS = [
-    ("plan.cpp", "if (!v.empty() && v.back().second == x.first)", "if (false)", "touching ranges not merged"),
+    ("plan.cpp", "merges[s] = p >= 0 && t.seg_start[p] + t.seg_len[p] == t.seg_start[s];", "merges[s] = false;",
+     "touching ranges not merged"),
+    ("plan.cpp", "merges[s] = p >= 0 && t.seg_start[p] + t.seg_len[p] == t.seg_start[s];",
+     "merges[s] = p >= 0 && t.seg_start[p] == t.seg_start[s] - 1;", "merge test off by the parent's length"),
     ("plan.cpp", "if (t.seg_len[s] < 1 || t.seg_start[s] != pos)", "if (t.seg_len[s] < 0 || t.seg_start[s] != pos)",
      "empty segments accepted"),
     ("plan.cpp", "if (t.seg_len[s] < 1 || t.seg_start[s] != pos)", "if (t.seg_len[s] < 1 || t.seg_start[s] < pos)",
