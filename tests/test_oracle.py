@@ -297,7 +297,7 @@ def test_gradients_match_finite_differences():
 
     dQ, dK, dV = A.tree_backward(q, k, v, do, *args, scale)
     h = 1e-6
-    for trial in range(8):
+    for trial in range(32):  # random directions
         u = [rng.standard_normal(x.shape) for x in (q, k, v)]
         fp = loss(q + h * u[0], k + h * u[1], v + h * u[2])
         fm = loss(q - h * u[0], k - h * u[1], v - h * u[2])
@@ -305,7 +305,7 @@ def test_gradients_match_finite_differences():
         an = float((dQ * u[0]).sum() + (dK * u[1]).sum() + (dV * u[2]).sum())
         assert abs(fd - an) <= 1e-6 * max(1.0, abs(an))
     # single coordinates: each (tensor, entry) in isolation
-    for trial in range(40):
+    for trial in range(200):
         which = trial % 3
         x = [q, k, v][which]
         pos = tuple(int(rng.integers(0, n)) for n in x.shape)
