@@ -284,6 +284,16 @@ def test_dense_route_matches_library_masked_attention_and_autograd():
         np.testing.assert_allclose(ours, ref.numpy(), rtol=0, atol=1e-11)
 
 
+def test_softmax_rows_sum_to_one_over_visible_keys_only():
+    t = W.tiny().tree
+    rng = np.random.default_rng(19)
+    q, k, v, _ = _rand(rng, t.total_tokens, 2, 1, 8)
+    mask = OT.visible_mask_bruteforce(*_tree_args(t))
+    _, _, P = A.dense_forward(q, k, v, mask, 0.4)
+    np.testing.assert_allclose(P.sum(axis=2), 1.0, rtol=0, atol=1e-13)
+    assert (P[:, ~mask] == 0).all() and (P[:, mask] > 0).all()
+
+
 def test_gradients_match_finite_differences():
     t = W.tiny().tree
     rng = np.random.default_rng(12)
