@@ -194,7 +194,9 @@ typedef struct {
  * each (host only).  *out receives a library-owned handle (NULL on error),
  * freed with sp_fragment_destroy; the tree's arrays are only read during the
  * call.  Errors: SP_ERR_INVALID_ARG (null, max_tokens < 1),
- * SP_ERR_INVALID_TREE, SP_ERR_CAP (a root path longer than max_tokens). */
+ * SP_ERR_INVALID_TREE, SP_ERR_CAP (a root path longer than max_tokens),
+ * SP_ERR_UNSUPPORTED (the sum over segments of depth + 1 passes 2^30: the
+ * tables, indexed in int32, could overflow). */
 SP_API int sp_fragment_plan(const sp_tree_desc *tree, int64_t max_tokens, sp_fragments **out);
 /* Fills *info.  Errors: SP_ERR_INVALID_ARG. */
 SP_API int sp_fragment_view(const sp_fragments *frag, sp_fragment_info *info);

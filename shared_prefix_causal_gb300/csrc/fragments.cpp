@@ -93,6 +93,11 @@ int sp_fragment_plan(const sp_tree_desc *tree, int64_t max_tokens, sp_fragments 
     return SP_ERR_INVALID_ARG;
   if ((tree->num_segments == 0) != (tree->total_tokens == 0)) return SP_ERR_INVALID_TREE;
   if (int rc = spc::validate_tree(*tree)) return rc;
+  // Each visit adds at most the segment's root path, so the entries number at
+  // most the sum of (depth + 1); the tables are indexed in int32.
+  int64_t bound = 0;
+  for (int32_t s = 0; s < tree->num_segments; ++s) bound += int64_t(tree->depth[s]) + 1;
+  if (bound > (int64_t(1) << 30)) return SP_ERR_UNSUPPORTED;
   sp_fragments *f = new (std::nothrow) sp_fragments();
   if (!f) return SP_ERR_INVALID_ARG;
   int rc = SP_OK;

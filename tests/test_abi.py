@@ -132,6 +132,11 @@ def test_plan_refuses_trees_whose_tables_overflow_int32_indexing():
     for a, b in zip((got["tiles"], got["ranges"], got["bwd"]), want):
         assert np.array_equal(a, b)
     assert got["max_ranges_per_tile"] == 300
+    # the fragment planner refuses the same deep comb for the same reason, and plans the small one
+    with pytest.raises(RuntimeError, match="status -3"):
+        spc.fragment_plan(t, 10 ** 9)
+    frag = spc.fragment_plan(small, 10 ** 6)
+    assert frag["num_fragments"] == 1 and frag["fragment_tokens"] == small.total_tokens
 
 
 def test_plan_rejects_bad_arguments():
