@@ -133,11 +133,14 @@ SP_API int sp_plan_view(const sp_plan *plan, sp_plan_info *info);
  * (this call or sp_plan_upload_to), or sp_plan_device_bytes, builds the device
  * tables inside the plan, so one thread must make those calls; after that the plan is read-only and any number of
  * calls on any streams of that device may use it at once.
- * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA. */
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA, SP_ERR_UNSUPPORTED (the forward's
+ * block lists could pass 2^30 entries: the tiles' ranges hold that many 128-key
+ * blocks, as a single sequence of a few million tokens cut into small tiles
+ * does). */
 SP_API int sp_plan_upload(sp_plan *plan, void *stream);
 
 /* Bytes of device memory the plan's tables take (for sp_plan_upload_to);
- * 0 for a NULL plan. */
+ * 0 for a NULL plan or one sp_plan_upload would refuse as SP_ERR_UNSUPPORTED. */
 SP_API size_t sp_plan_device_bytes(sp_plan *plan);
 
 /* sp_plan_upload into caller-owned device memory: no allocation and no
@@ -149,7 +152,7 @@ SP_API size_t sp_plan_device_bytes(sp_plan *plan);
  * allocations.  Repeat calls, or a call after sp_plan_upload, are no-ops.
  *   device_buffer  256-byte aligned, at least sp_plan_device_bytes(plan) bytes.
  * Errors: SP_ERR_INVALID_ARG, SP_ERR_ALIGNMENT, SP_ERR_WORKSPACE (too small),
- * SP_ERR_CUDA. */
+ * SP_ERR_CUDA, SP_ERR_UNSUPPORTED (as sp_plan_upload). */
 SP_API int sp_plan_upload_to(sp_plan *plan, void *device_buffer, size_t buffer_bytes, void *stream);
 
 /* Frees the plan (host copies, and the device copy if sp_plan_upload made

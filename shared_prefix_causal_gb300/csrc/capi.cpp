@@ -92,6 +92,11 @@ namespace {
 // Derived device tables (forward pairs, backward launch order), built once.
 int prepare_device_tables(sp_plan *p) {
   if (!p->pairs.empty() || p->tiles.empty()) return SP_OK;
+  // The forward's merged lists hold at most one entry per 128-key block of each
+  // tile's ranges, indexed in int32: plans that could pass 2^30 are refused.
+  int64_t blocks = 0;
+  for (size_t r = 0; r + 1 < p->ranges.size(); r += 2) blocks += (int64_t(p->ranges[r + 1]) - p->ranges[r] + 127) / 128;
+  if (blocks > (int64_t(1) << 30)) return SP_ERR_UNSUPPORTED;
   try {
     spc::build_pairs(*p, 128);
     spc::build_bwd_schedule(*p);

@@ -139,6 +139,17 @@ def test_plan_refuses_trees_whose_tables_overflow_int32_indexing():
     assert frag["num_fragments"] == 1 and frag["fragment_tokens"] == small.total_tokens
 
 
+def test_upload_refuses_plans_whose_forward_block_lists_could_overflow():
+    """One 600K-token sequence cut into 1-token tiles: its tiles' ranges hold about 1.4e9 blocks of
+    128 keys.  The plan itself is fine; its upload is refused before any CUDA call."""
+    T = 600_000
+    p = spc.sp_tree_plan([0], [T], [-1], [0], 1, 128, 0)
+    assert spc.sp_plan_device_bytes(p) == 0
+    assert spc._c_plan_upload(p.handle, None) == -3  # refused before any CUDA call
+    t = W.tiny().tree
+    assert spc.sp_plan_device_bytes(spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 128, 128, 0)) > 0
+
+
 def test_plan_rejects_bad_arguments():
     a = _desc(W.tiny().tree)
     for tt, kb, order in ((0, 128, 0), (32, 0, 0), (32, 128, 2)):
