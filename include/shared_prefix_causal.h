@@ -335,6 +335,23 @@ SP_API int sp_tree_attn_bwd_deterministic(const sp_plan *plan, int32_t dtype, co
                                           int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
                                           int32_t *d_status, void *stream);
 
+/* sp_tree_attn_bwd (deterministic == 0) or sp_tree_attn_bwd_deterministic
+ * (deterministic == 1) with a measurement hook; the pages have no counterpart.
+ * ev_main_begin and ev_main_end are caller-created cudaEvent_t handles (either
+ * may be NULL), recorded on `stream` just before and just after the launch of
+ * the backward's main kernel (the per-key-block kernel that forms dK, dV and,
+ * in the default mode, the dQ partials), so that the caller can time that
+ * kernel alone with cudaEventElapsedTime while the preprocess and dQ kernels
+ * run outside the pair.  Results, arguments and errors are otherwise those of
+ * the two calls above; the fp32 path has no single main kernel and returns
+ * SP_ERR_UNSUPPORTED when an event is given.  The events stay owned by the
+ * caller. */
+SP_API int sp_tree_attn_bwd_timed(const sp_plan *plan, int32_t dtype, const void *q, const void *k, const void *v,
+                                  const void *o, const float *lse, const void *d_o, void *dq, void *dk, void *dv,
+                                  void *workspace, size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv,
+                                  int32_t D, float softmax_scale, int32_t deterministic, void *ev_main_begin,
+                                  void *ev_main_end, int32_t *d_status, void *stream);
+
 /* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (64u << 20)
 
@@ -343,11 +360,20 @@ SP_API int sp_tree_attn_bwd_deterministic(const sp_plan *plan, int32_t dtype, co
  * owns the whole device, or a plugin that is handed only its inputs and
  * outputs).  The pages have no counterpart: this is a packaging variant of
  * tree_attn_bwd with identical arguments and results, minus the workspace.
- *   Scratch: a fixed SP_NOALLOC_SCRATCH_BYTES array in device memory that the
- *   library holds on every GPU where it is loaded, until process exit.  The
- *   first call on a device looks up that array's address (do it before any
- *   stream capture).  All calls on a device share the array, so calls that
- *   overlap on the GPU race; serialise them.  Nothing is allocated.
+ *   Scratch: a fixed SP_NOALLOC_SCRATCH_BYTES array that belongs to the
+ *   library's device code, held on every GPU where that code is loaded until
+ *   process exit.  The call itself allocates nothing (no cudaMalloc, no
+ *   cudaFree, no allocating library routine), but the driver commits the
+ *   array's 64 MiB when it loads the library's device code on a device: with
+ *   CUDA's default lazy module loading that happens during the first call of
+ *   this function on that device; with CUDA_MODULE_LOADING=EAGER, when the
+ *   library's device code is loaded into the context.  So make a first call
+ *   (or use EAGER loading) before a memory pool takes the whole device, and
+ *   before any stream capture: that first call also looks up the array's
+ *   device address.  The address is cached per device and context; a new
+ *   context (after cudaDeviceReset) is detected and looked up again.  All
+ *   calls on a device share the array, so calls that overlap on the GPU race;
+ *   serialise them.  Each call rewrites every scratch byte it reads.
  *   Limit: sp_tree_attn_bwd_workspace_bytes(dtype, T, Hq, D) must not exceed
  *   SP_NOALLOC_SCRATCH_BYTES (bf16 needs 4 * T * Hq * (D + 1) bytes, e.g.
  *   T * Hq <= 129,000 rows at D = 128), otherwise SP_ERR_WORKSPACE.

@@ -81,6 +81,9 @@ _c_frag_destroy = _sig("sp_fragment_destroy", None, [_vp])
 _c_bwd_det = _sig("sp_tree_attn_bwd_deterministic", ctypes.c_int,
                   [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                    _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_bwd_timed = _sig("sp_tree_attn_bwd_timed", ctypes.c_int,
+                    [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                     _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _vp, _vp, _vp, _vp])
 _c_bwd_noalloc = _sig("sp_tree_attn_bwd_noalloc", ctypes.c_int,
                       [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                        _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
@@ -102,7 +105,7 @@ EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
             "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic", "sp_fragment_plan", "sp_fragment_view",
-            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to")
+            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -226,12 +229,36 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _need_status(d_status):
+    """The optional device status word: one int32 (the kernels OR their error bits into it)."""
+    import torch
+    if d_status is not None and (d_status.dtype != torch.int32 or d_status.numel() < 1):
+        raise ValueError("d_status must be an int32 CUDA tensor of at least one element")
+
+
+def _check_bwd_shapes(q, k, v, o, lse, d_o, dq, dk, dv):
+    """Shapes and dtypes the backward entry points read and write: (T, Hq, Hkv, D)."""
+    import torch
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    for t, shp in ((k, (T, Hkv, D)), (v, (T, Hkv, D)), (o, (T, Hq, D)), (d_o, (T, Hq, D)), (dq, (T, Hq, D)),
+                   (dk, (T, Hkv, D)), (dv, (T, Hkv, D))):
+        if tuple(t.shape) != shp or t.dtype != q.dtype:
+            raise ValueError("shape or dtype mismatch")
+    if tuple(lse.shape) != (Hq, T) or lse.dtype != torch.float32:
+        raise ValueError("lse must be float32 [Hq, T]")
+    return T, Hq, Hkv, D
+
+
 def sp_tree_attn_fwd(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status=None, stream=None):
+    import torch
     _need_cuda(q, k, v, o, lse, d_status)
+    _need_status(d_status)
     T, Hq, D = q.shape
     Hkv = k.shape[1]
     if tuple(k.shape) != (T, Hkv, D) or tuple(v.shape) != (T, Hkv, D) or tuple(o.shape) != (T, Hq, D) \
-            or tuple(lse.shape) != (Hq, T) or o.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype:
+            or tuple(lse.shape) != (Hq, T) or o.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype \
+            or lse.dtype != torch.float32:
         raise ValueError("shape or dtype mismatch")
     with _on(q):
         _check(_c_fwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, D,
@@ -245,12 +272,8 @@ def sp_tree_attn_bwd_workspace_bytes(dtype: int, T: int, Hq: int, D: int) -> int
 def sp_tree_attn_bwd(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale: float,
                      d_status=None, stream=None, _fn=None):
     _need_cuda(q, k, v, o, lse, d_o, dq, dk, dv, workspace, d_status)
-    T, Hq, D = q.shape
-    Hkv = k.shape[1]
-    for t, shp in ((k, (T, Hkv, D)), (v, (T, Hkv, D)), (o, (T, Hq, D)), (d_o, (T, Hq, D)), (dq, (T, Hq, D)),
-                   (dk, (T, Hkv, D)), (dv, (T, Hkv, D))):
-        if tuple(t.shape) != shp or t.dtype != q.dtype:
-            raise ValueError("shape or dtype mismatch")
+    _need_status(d_status)
+    T, Hq, Hkv, D = _check_bwd_shapes(q, k, v, o, lse, d_o, dq, dk, dv)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     fn, name = _fn or (_c_bwd, "sp_tree_attn_bwd")
     with _on(q):
@@ -266,16 +289,40 @@ def sp_tree_attn_bwd_deterministic(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv,
                      _fn=(_c_bwd_det, "sp_tree_attn_bwd_deterministic"))
 
 
+def sp_tree_attn_bwd_timed(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, softmax_scale: float,
+                           deterministic: bool, ev_main_begin, ev_main_end, d_status=None, stream=None):
+    """sp_tree_attn_bwd(_deterministic) with two caller-owned events recorded around its main kernel.
+
+    The events are ``torch.cuda.Event(enable_timing=True)`` objects or raw ``cudaEvent_t`` handles (ints).
+    torch creates an event's handle at its first record, so a torch event never recorded before is recorded
+    once on the current stream here; the library then records it again around the main kernel."""
+    _need_cuda(q, k, v, o, lse, d_o, dq, dk, dv, workspace, d_status)
+    _need_status(d_status)
+    T, Hq, Hkv, D = _check_bwd_shapes(q, k, v, o, lse, d_o, dq, dk, dv)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    with _on(q):
+        st = _stream(stream, q.device)
+        handles = []
+        for ev in (ev_main_begin, ev_main_end):
+            if ev is None or isinstance(ev, int):
+                handles.append(_vp(ev))
+            else:
+                if not ev.cuda_event:  # torch creates its event at the first record
+                    import torch
+                    ev.record(torch.cuda.current_stream(q.device))
+                handles.append(_vp(ev.cuda_event))
+        _check(_c_bwd_timed(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o),
+                            _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, T, Hq, Hkv, D,
+                            float(softmax_scale), 1 if deterministic else 0, handles[0], handles[1], _ptr(d_status),
+                            st), "sp_tree_attn_bwd_timed")
+
+
 def sp_tree_attn_bwd_noalloc(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, softmax_scale: float,
                              d_status=None, stream=None):
     """sp_tree_attn_bwd backed by the library's fixed device scratch (no workspace)."""
     _need_cuda(q, k, v, o, lse, d_o, dq, dk, dv, d_status)
-    T, Hq, D = q.shape
-    Hkv = k.shape[1]
-    for t, shp in ((k, (T, Hkv, D)), (v, (T, Hkv, D)), (o, (T, Hq, D)), (d_o, (T, Hq, D)), (dq, (T, Hq, D)),
-                   (dk, (T, Hkv, D)), (dv, (T, Hkv, D))):
-        if tuple(t.shape) != shp or t.dtype != q.dtype:
-            raise ValueError("shape or dtype mismatch")
+    _need_status(d_status)
+    T, Hq, Hkv, D = _check_bwd_shapes(q, k, v, o, lse, d_o, dq, dk, dv)
     with _on(q):
         _check(_c_bwd_noalloc(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                               _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv), T, Hq, Hkv, D, float(softmax_scale),
@@ -284,6 +331,7 @@ def sp_tree_attn_bwd_noalloc(plan: Plan, q, k, v, o, lse, d_o, dq, dk, dv, softm
 
 def sp_edge_gather(hidden, idx, out, d_status=None, stream=None):
     _need_cuda(hidden, idx, out, d_status)
+    _need_status(d_status)
     import torch
     if idx.dtype != torch.int32:
         raise ValueError("edge indices must be int32")
@@ -302,6 +350,7 @@ def sp_edge_gather_bwd_workspace_bytes(T: int, E: int) -> int:
 
 def sp_edge_gather_bwd(grad_out, idx, grad_hidden, workspace, d_status=None, stream=None):
     _need_cuda(grad_out, idx, grad_hidden, workspace, d_status)
+    _need_status(d_status)
     import torch
     if idx.dtype != torch.int32:
         raise ValueError("edge indices must be int32")
@@ -322,6 +371,7 @@ def sp_edge_logprob_workspace_bytes(E: int, V: int) -> int:
 
 def sp_edge_logprob(hidden_sel, weight, labels, logprob, lse, workspace, d_status=None, stream=None):
     _need_cuda(hidden_sel, weight, labels, logprob, lse, workspace, d_status)
+    _need_status(d_status)
     import torch
     if labels.dtype != torch.int32 or logprob.dtype != torch.float32 or lse.dtype != torch.float32:
         raise ValueError("labels must be int32, logprob and lse float32")
@@ -343,6 +393,7 @@ def sp_edge_logprob_bwd_workspace_bytes(E: int, V: int) -> int:
 def sp_edge_logprob_bwd(hidden_sel, weight, labels, lse, grad_logprob, d_hidden_sel, d_weight, workspace,
                         d_status=None, stream=None):
     _need_cuda(hidden_sel, weight, labels, lse, grad_logprob, d_hidden_sel, d_weight, workspace, d_status)
+    _need_status(d_status)
     import torch
     E, Hd = hidden_sel.shape
     V = weight.shape[0]
@@ -360,6 +411,7 @@ def sp_edge_logprob_bwd(hidden_sel, weight, labels, lse, grad_logprob, d_hidden_
 
 def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
     _need_cuda(d_status)
+    _need_status(d_status)
     with _on(d_status):
         _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream, d_status.device)),
                "sp_debug_wait_timeout")

@@ -508,7 +508,7 @@ int bwd_head_chunk(const PlanDev &p, const AttnShape &s, int sms) {
 template <int D, int G>
 int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
-           bool deterministic, int32_t *d_status, cudaStream_t st) {
+           bool deterministic, int32_t *d_status, cudaStream_t st, cudaEvent_t ev_begin, cudaEvent_t ev_end) {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -531,9 +531,11 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
     return SP_ERR_CUDA;
   const unsigned grid = unsigned(p.n_bwd) * unsigned(s.Hkv);
   const int head_chunk = bwd_head_chunk(p, s, sms);
+  if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return SP_ERR_CUDA;
   kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, dqacc, static_cast<__nv_bfloat16 *>(dk),
                                      static_cast<__nv_bfloat16 *>(dv), d_status, head_chunk);
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
+  if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return SP_ERR_CUDA;
   // dQ without atomics: every query tile walks its own key blocks
   if (deterministic) return tc_dq(p, s, q, k, v, lse, d_o, dq, delta, d_status, st);
 
@@ -547,11 +549,12 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
 
 int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
-           bool deterministic, int32_t *d_status, void *stream) {
+           bool deterministic, int32_t *d_status, void *stream, void *ev_begin, void *ev_end) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaEvent_t e0 = static_cast<cudaEvent_t>(ev_begin), e1 = static_cast<cudaEvent_t>(ev_end);
 #define SPC_BWD_CASE(DD, GG)                                                                          \
   if (s.D == DD && s.G == GG)                                                                         \
-    return launch<DD, GG>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, deterministic, d_status, st);
+    return launch<DD, GG>(p, s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, deterministic, d_status, st, e0, e1);
   SPC_BWD_CASE(64, 1) SPC_BWD_CASE(64, 2) SPC_BWD_CASE(64, 4) SPC_BWD_CASE(64, 8)
   SPC_BWD_CASE(128, 1) SPC_BWD_CASE(128, 2) SPC_BWD_CASE(128, 4) SPC_BWD_CASE(128, 8)
 #undef SPC_BWD_CASE

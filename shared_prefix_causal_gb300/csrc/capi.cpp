@@ -222,7 +222,7 @@ namespace {
 int attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, const void *o,
              const float *lse, const void *d_o, void *dq, void *dk, void *dv, void *workspace, size_t workspace_bytes,
              int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale, bool deterministic,
-             int32_t *d_status, void *stream) {
+             int32_t *d_status, void *stream, void *ev_begin = nullptr, void *ev_end = nullptr) {
   if (!p) return SP_ERR_INVALID_ARG;
   if (int rc = check_heads(dtype, T, Hq, Hkv, D)) return rc;
   if (T != p->total_tokens) return SP_ERR_INVALID_ARG;
@@ -245,8 +245,9 @@ int attn_bwd(const sp_plan *p, int32_t dtype, const void *q, const void *k, cons
     float *dqacc = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                              align_up(size_t(T) * size_t(Hq) * sizeof(float)));
     return spc::tc_bwd(plan_dev(*p), s, q, k, v, o, lse, d_o, dq, dk, dv, delta, dqacc, deterministic, d_status,
-                       stream);
+                       stream, ev_begin, ev_end);
   }
+  if (ev_begin || ev_end) return SP_ERR_UNSUPPORTED;  // the fp32 path has no single main kernel
   // the fp32 path computes dQ per query tile already (no atomics)
   return spc::simt_bwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_o, dq, dk, dv, delta, d_status, stream);
 }
@@ -269,6 +270,16 @@ int sp_tree_attn_bwd_deterministic(const sp_plan *p, int32_t dtype, const void *
                                    int32_t D, float softmax_scale, int32_t *d_status, void *stream) {
   return attn_bwd(p, dtype, q, k, v, o, lse, d_o, dq, dk, dv, workspace, workspace_bytes, T, Hq, Hkv, D,
                   softmax_scale, true, d_status, stream);
+}
+
+int sp_tree_attn_bwd_timed(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v,
+                           const void *o, const float *lse, const void *d_o, void *dq, void *dk, void *dv,
+                           void *workspace, size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                           float softmax_scale, int32_t deterministic, void *ev_main_begin, void *ev_main_end,
+                           int32_t *d_status, void *stream) {
+  if (deterministic != 0 && deterministic != 1) return SP_ERR_INVALID_ARG;
+  return attn_bwd(p, dtype, q, k, v, o, lse, d_o, dq, dk, dv, workspace, workspace_bytes, T, Hq, Hkv, D,
+                  softmax_scale, deterministic != 0, d_status, stream, ev_main_begin, ev_main_end);
 }
 
 int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t hidden_dim, const int32_t *idx, int32_t E,

@@ -77,9 +77,11 @@ int tc_fwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
            int32_t *d_status, void *stream);
 // delta: [Hq][T] fp32 scratch; dqacc: [T][Hq][D] fp32 scratch (zeroed inside;
 // unused when deterministic, which computes dQ per query tile with tc_dq).
+// ev_begin / ev_end (cudaEvent_t, optional): recorded on the stream just before
+// and just after the main kernel's launch, so a caller can time it alone.
 int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
-           bool deterministic, int32_t *d_status, void *stream);
+           bool deterministic, int32_t *d_status, void *stream, void *ev_begin = nullptr, void *ev_end = nullptr);
 // dQ of every query tile over its own key blocks, no atomics (attn_dq_sm103a.cu);
 // delta from the backward's preprocess.
 int tc_dq(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,

@@ -175,3 +175,33 @@ def test_shape_and_dtype_mismatches_raise_before_the_call(monkeypatch, fake_cuda
     with pytest.raises(ValueError):
         spc.sp_tree_attn_fwd(FakePlan(), torch.zeros(4, 8, 64), k, v, o, lse, 0.1)  # a CPU tensor
     assert calls == [] and fake_cuda == []
+
+
+@pytest.mark.parametrize("entry", ["sp_tree_attn_bwd", "sp_tree_attn_bwd_deterministic", "sp_tree_attn_bwd_noalloc"])
+def test_backward_refuses_a_bad_lse_or_status_word(monkeypatch, fake_cuda, entry):
+    """An lse of the wrong dtype or size would be read past its end by the kernels; a status word
+    that is not int32 would be written with the wrong width.  Both are refused before the C call."""
+    recorders = [_record(monkeypatch, n) for n in ("_c_bwd", "_c_bwd_det", "_c_bwd_noalloc")]
+    q, k, v, o, lse = _attn_tensors()
+    do = FakeCuda(q.shape, q.dtype, 0x6000)
+    dq, dk, dv = FakeCuda(q.shape, q.dtype, 0x7000), FakeCuda(k.shape, k.dtype, 0x7100), FakeCuda(v.shape, v.dtype, 0x7200)
+    ws = FakeCuda((4096,), torch.uint8, 0x8000)
+    fn = getattr(spc, entry)
+
+    def call(lse_, st=None):
+        if entry == "sp_tree_attn_bwd_noalloc":
+            fn(FakePlan(), q, k, v, o, lse_, do, dq, dk, dv, 0.25, st)
+        else:
+            fn(FakePlan(), q, k, v, o, lse_, do, dq, dk, dv, ws, 0.25, st)
+
+    bad = [FakeCuda(lse.shape, torch.bfloat16, lse.ptr),                  # wrong dtype
+           FakeCuda((lse.shape[0], lse.shape[1] - 1), torch.float32, lse.ptr),  # one token short
+           FakeCuda((lse.shape[1], lse.shape[0]), torch.float32, lse.ptr)]      # transposed
+    for b in bad:
+        with pytest.raises(ValueError):
+            call(b)
+    with pytest.raises(ValueError):
+        call(lse, FakeCuda((1,), torch.int64, 0x9000))
+    assert all(r == [] for r in recorders) and fake_cuda == []
+    call(lse, FakeCuda((1,), torch.int32, 0x9000))  # the good case reaches the library
+    assert sum(len(r) for r in recorders) == 1

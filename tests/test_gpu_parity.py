@@ -92,11 +92,12 @@ def check_full(w, x, out, dtype, groups=None, qk_grads_zero=False):
     return res
 
 
-def check_sampled(w, x, out, groups, n_leaves=2, extra_rows=256, seed=0):
+def check_sampled(w, x, out, groups, n_leaves=2, extra_rows=256, seed=0, interior=()):
     """Full-size check on sampled outputs the oracle computes path by path:
     O, LSE and dQ on rows of a few root-to-leaf paths, dK/dV of the leaf
     segments' keys and of the parent segment's keys (which sum several
-    branches)."""
+    branches), and dK/dV of the ``interior`` segments' keys (each the sum over
+    every branch below it)."""
     tol = TOL["bf16"]
     t = w.tree
     rng = np.random.default_rng(seed)
@@ -139,6 +140,17 @@ def check_sampled(w, x, out, groups, n_leaves=2, extra_rows=256, seed=0):
                 ref["dk"].append(sk)
                 got["dv"].append(out["dv"][p0:p1, g])
                 ref["dv"].append(sv)
+    for seg in interior:
+        p0, p1 = int(t.seg_start[seg]), int(t.seg_start[seg] + t.seg_len[seg])
+        for g in groups:
+            sk, sv = A.subtree_key_grads(q, k, v, do, t.seg_start, t.seg_len, t.parent, w.softmax_scale, seg, g)
+            ik, iv = rel_l2(out["dk"][p0:p1, g], sk), rel_l2(out["dv"][p0:p1, g], sv)
+            print(w.name, "interior segment", seg, "group", g, {"dk": ik, "dv": iv})
+            assert ik <= tol["g_rel"] and iv <= tol["g_rel"], (seg, g)
+            got["dk"].append(out["dk"][p0:p1, g])
+            ref["dk"].append(sk)
+            got["dv"].append(out["dv"][p0:p1, g])
+            ref["dv"].append(sv)
     cat = lambda L: np.concatenate([np.ravel(a) for a in L])  # noqa: E731
     res = {n: rel_l2(cat(got[n]), cat(ref[n])) for n in ("o", "dq", "dk", "dv")}
     res["o_abs"] = float(np.abs(cat(got["o"]) - cat(ref["o"])).max())
@@ -215,11 +227,20 @@ def test_star_bf16_matches_oracle():
     check_sums(w, x, out)
 
 
+# An interior segment of the agent tree with many branches below it: segment 4
+# (depth 4, 82 tokens) has 12 leaves and a 12,211-token subtree, so its dK/dV
+# sum the contributions of every one of those branches; the segments above it
+# have subtrees of nearly the whole tree, too large for the oracle here.
+AGENT_INTERIOR = (4,)
+
+
 @pytest.mark.slow
 def test_agent_bf16_sampled():
     w = W.agent_tree()
     x, out = run_gpu(w, "bf16")
-    check_sampled(w, x, out, groups=[0, w.hkv - 1])
+    t = w.tree
+    assert int(t.depth[4]) == 4 and len([l for l in OT.leaves(t.parent) if l in set(OT.descendants(t.parent, 4))]) == 12
+    check_sampled(w, x, out, groups=[0, w.hkv - 1], interior=AGENT_INTERIOR)
     check_sums(w, x, out)
 
 
@@ -273,7 +294,7 @@ def test_deterministic_bwd_star_is_reproducible():
 def test_deterministic_bwd_agent_sampled():
     w = W.agent_tree()
     x, out = run_gpu(w, "bf16", deterministic=True)
-    check_sampled(w, x, out, groups=[0, w.hkv - 1])
+    check_sampled(w, x, out, groups=[0, w.hkv - 1], interior=AGENT_INTERIOR)
     check_sums(w, x, out)
     _, out2 = run_gpu(w, "bf16", deterministic=True, x=x)
     assert np.array_equal(out["dq"], out2["dq"])
@@ -496,3 +517,32 @@ def test_plan_uploaded_into_a_caller_buffer_gives_identical_results():
         assert torch.equal(a, b)
     p.close()  # the caller's buffer is not freed by the plan
     assert buf.is_cuda and buf.numel() > 0
+
+
+def test_timed_backward_equals_the_backward_and_times_its_main_kernel():
+    """sp_tree_attn_bwd_timed gives the backward's results (dK, dV bit-equal; deterministic mode bit-equal
+    in full) and its events bracket a positive time no longer than the whole call."""
+    w = W.grpo_star()
+    x = W.draw_tensors(w, "bf16")
+    q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "do"))
+    G = w.hq // w.hkv
+    plan = spc.tree_plan(w.tree, 128 // G)
+    o, lse = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale)
+    ws = spc.bwd_workspace(q)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for det in (False, True):
+        ref = spc.tree_attn_bwd(plan, q, k, v, o, lse, do, w.softmax_scale, deterministic=det)
+        got = tuple(torch.empty_like(a) for a in (q, k, v))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record()
+        spc.sp_tree_attn_bwd_timed(plan, q, k, v, o, lse, do, *got, ws, w.softmax_scale, det, ev[1], ev[2], st)
+        ev[3].record()
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])
+        if det:
+            assert torch.equal(got[0], ref[0])
+        else:
+            assert rel_l2(got[0].float().cpu().numpy(), ref[0].float().cpu().numpy()) < 5e-3
+        main, whole = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+        assert 0 < main <= whole
