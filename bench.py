@@ -562,20 +562,25 @@ def run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_b
     """The backward with dQ formed per query tile (no atomics), timed like the step's backward."""
     import torch
     stream = torch.cuda.current_stream(dev)
-    ms = []
+    ms, main = [], []
     for i in range(args.warmup + args.steps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        spc.sp_tree_attn_bwd_deterministic(plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status)
-        e1.record(stream)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        for x_ in e:
+            x_.record(stream)
+        e[0].record(stream)
+        spc.sp_tree_attn_bwd_timed(plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, True, e[1], e[2], status)
+        e[3].record(stream)
         torch.cuda.synchronize(dev)
         if i >= args.warmup:
-            ms.append(e0.elapsed_time(e1))
+            ms.append(e[0].elapsed_time(e[3]))
+            main.append(e[1].elapsed_time(e[2]))
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} in the deterministic backward")
     t = statistics.median(ms)
     tf = f_bwd / (t * 1e-3) / 1e12
+    tm = statistics.median(main)
     return {"ms": round(t, 4), "useful_tflops": round(tf, 2), "frac_of_peak": round(tf / p_burst, 4) if p_burst else None,
+            "key_block_kernel_ms": round(tm, 4), "query_tile_kernel_and_preprocess_ms": round(t - tm, 4),
             "launches": 3}
 
 

@@ -11,9 +11,11 @@
 // every run (the atomic path adds key blocks' partials in arrival order).
 //
 // dq_tc_kernel: one CTA per (128-row query tile, KV head), KV head outermost
-// so a head's K/V stays in L2 while its tiles run.  Warps 0-3: elementwise
-// (thread = query row = TMEM lane); warp 4: TMA producer (Q and dO once, K/V
-// blocks through a 2-stage ring); warp 5: tcgen05 MMA issuer.  Per key block
+// so a head's K/V stays in L2 while its tiles run.  Warps 0-7: elementwise,
+// thread = query row = TMEM lane, warpgroup h taking key columns
+// [64h, 64h + 64) of every row (the work needs no row reduction, so the
+// split needs no exchange); warp 8: TMA producer (Q and dO once, K/V blocks
+// through a 2-stage ring); warp 9: tcgen05 MMA issuer.  Per key block
 // n the MMA thread issues S = Q K^T and dP = dO V^T (SS), and, once the
 // elementwise warps have stored dS(n) as bf16 pairs in TMEM, dQ += dS(n) K(n)
 // (A read from TMEM, K as an MN-major B).  S(n+1) and dP(n+1) are issued as
@@ -42,7 +44,7 @@ using namespace ptx;
 constexpr int kBM = 128;           // query rows per tile (tokens x query heads of one KV head)
 constexpr int kBN = 128;           // keys per block
 constexpr int kStages = 2;         // K/V ring depth
-constexpr int kThreads = 192;      // 4 elementwise warps, producer, MMA
+constexpr int kThreads = 320;      // 8 elementwise warps, producer, MMA
 constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -51,8 +53,8 @@ enum : int {
   B_KV_FULL = 1,   // +stage
   B_KV_EMPTY = 3,  // +stage
   B_S_FULL = 5,
-  B_S_FREE = 6,    // 4 warp arrivals
-  B_DS_FULL = 7,   // +buffer, 4 warp arrivals
+  B_S_FREE = 6,    // 8 warp arrivals
+  B_DS_FULL = 7,   // +buffer, 8 warp arrivals
   B_DS_FREE = 9,   // +buffer
   B_DQ_DONE = 11,
   B_COUNT = 12
@@ -122,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status, kSpinLimit};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(ctl.bar(i), (i == B_S_FREE || i == B_DS_FULL || i == B_DS_FULL + 1) ? 4u : 1u);
+      mbar_init(ctl.bar(i), (i == B_S_FREE || i == B_DS_FULL || i == B_DS_FULL + 1) ? 8u : 1u);
     *ctl.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(sbase + L::TSLOT, 512);
     tmem_relinquish();
   }
@@ -135,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = n - kStages < 0 ? 0 : n - kStages; m < n; ++m) ctl.drain(B_KV_FULL + (m & 1), (m >> 1) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kBM, kBN, 0, 0);  // S = Q K^T, dP = dO V^T
@@ -218,8 +220,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- elementwise
-    const int r = threadIdx.x;  // query row = TMEM lane
-    const uint32_t lane_base = uint32_t(32 * warp) << 16;
+    const int h = warp >> 2;            // key columns [64h, 64h + 64)
+    const int r = threadIdx.x & 127;    // query row = TMEM lane
+    const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
     const int tok = q0 + r / G, head = g * G + r % G;
     const bool rowv = tok < q1;
     const float sl2 = s.scale * kLog2e;
@@ -238,10 +241,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // keys [kb, kb + lim) visible to this row
       const int lim = !rowv ? 0 : (causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb);
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int cc = 0; cc < kBN / 64; ++cc) {
+        const int c = 2 * h + cc;  // 32-column chunk of the block
         uint32_t us[32], ud[32];
         tmem_ld32x2(tmem + lane_base + T_S + 32 * c, tmem + lane_base + T_DP + 32 * c, us, ud);
-        if (c == kBN / 32 - 1) {
+        if (cc == kBN / 64 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(ctl.bar(B_S_FREE));
@@ -264,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fmul2(dsv[i], dsv[i + 1], pv[i], pv[i + 1], t0, t1);
         }
         // dS(n) goes to buffer st once dQ(n-2) has read it
-        if (c == 0 && !(ok = ctl.wait_warp(B_DS_FREE + st, ((n >> 1) & 1) ^ 1))) break;
+        if (cc == 0 && !(ok = ctl.wait_warp(B_DS_FREE + st, ((n >> 1) & 1) ^ 1))) break;
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(dsv[2 * i], dsv[2 * i + 1]);
@@ -280,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       __nv_bfloat16 *row = dq + (size_t(tok) * s.Hq + head) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 64; ++cc) {  // head-dim columns [D/2 h, D/2 (h + 1))
+        const int c = (D / 64) * h + cc;
         uint32_t u[32];
         tmem_ld32(tmem + lane_base + T_DQ + 32 * c, u);
         if (rowv) {
@@ -300,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);

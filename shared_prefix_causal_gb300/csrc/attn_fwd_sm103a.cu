@@ -102,10 +102,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int g = blockIdx.x / plan.n_pairs;
-  const int *pr = plan.pairs + 4 * (blockIdx.x % plan.n_pairs);
+  const int *pr = plan.pairs + 4 * size_t(blockIdx.x % plan.n_pairs);
   const int ta = pr[0], tb = pr[1], bbeg = pr[2], nblk = pr[3];
   const int G = s.G, T = s.T;
-  const int *pb = plan.pblk + 4 * bbeg;
+  const int *pb = plan.pblk + 4 * size_t(bbeg);
   const int *tla = plan.tiles + 5 * ta;
   const int *tlb = tb >= 0 ? plan.tiles + 5 * tb : nullptr;
   const int qa0 = tla[1], qa1 = tla[2];

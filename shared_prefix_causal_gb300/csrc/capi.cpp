@@ -32,7 +32,7 @@ int check_tiling(const sp_plan &p, int32_t dtype, int32_t G) {
 
 spc::PlanDev plan_dev(const sp_plan &p) {
   return {p.d_tiles, p.d_ranges, p.d_bwd, p.n_tiles(), p.n_bwd(), p.tile_tokens, p.kv_block,
-          p.d_pairs, p.d_pblk, p.n_pairs(), p.bwd_run_sum, p.bwd_run_max};
+          p.d_pairs, p.d_pblk, p.n_pairs(), p.bwd_run_sum, p.bwd_run_max, p.d_quads, p.d_qblk, p.n_quads()};
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -99,6 +99,7 @@ int prepare_device_tables(sp_plan *p) {
   if (blocks > (int64_t(1) << 30)) return SP_ERR_UNSUPPORTED;
   try {
     spc::build_pairs(*p, 128);
+    spc::build_quads(*p, 128);
     spc::build_bwd_schedule(*p);
   } catch (...) {
     return SP_ERR_INVALID_ARG;
@@ -107,13 +108,14 @@ int prepare_device_tables(sp_plan *p) {
 }
 
 struct DeviceLayout {
-  size_t bt, br, bb, bp, bk, total;
+  size_t bt, br, bb, bp, bk, bq, bqk, total;
 };
 
 DeviceLayout device_layout(const sp_plan &p) {
   DeviceLayout l{p.tiles.size() * 4, p.ranges.size() * 4, p.bwd.size() * 4, p.pairs.size() * 4,
-                 p.pblk.size() * 4, 0};
-  l.total = align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp) + align_up(l.bk) + 256;
+                 p.pblk.size() * 4, p.quads.size() * 4, p.qblk.size() * 4, 0};
+  l.total = align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp) + align_up(l.bk) + align_up(l.bq) +
+            align_up(l.bqk) + 256;
   return l;
 }
 
@@ -124,7 +126,11 @@ int copy_tables(sp_plan *p, char *base, const DeviceLayout &l, cudaStream_t st) 
   int32_t *db = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br));
   int32_t *dp = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br) + align_up(l.bb));
   int32_t *dk = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp));
+  int32_t *dq = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dk) + align_up(l.bk));
+  int32_t *dqk = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dq) + align_up(l.bq));
   if ((l.bt && cudaMemcpyAsync(dt, p->tiles.data(), l.bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.bq && cudaMemcpyAsync(dq, p->quads.data(), l.bq, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.bqk && cudaMemcpyAsync(dqk, p->qblk.data(), l.bqk, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.br && cudaMemcpyAsync(dr, p->ranges.data(), l.br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.bb && cudaMemcpyAsync(db, p->bwd_sched.data(), l.bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.bp && cudaMemcpyAsync(dp, p->pairs.data(), l.bp, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
@@ -135,6 +141,8 @@ int copy_tables(sp_plan *p, char *base, const DeviceLayout &l, cudaStream_t st) 
   p->d_bwd = db;
   p->d_pairs = dp;
   p->d_pblk = dk;
+  p->d_quads = l.bq ? dq : nullptr;
+  p->d_qblk = l.bqk ? dqk : nullptr;
   cudaGetDevice(&p->device);
   return SP_OK;
 }
@@ -152,7 +160,7 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   char *base = nullptr;
   if (cudaMalloc(&base, l.total) != cudaSuccess) return SP_ERR_CUDA;
   if (copy_tables(p, base, l, st) != SP_OK || cudaStreamSynchronize(st) != cudaSuccess) {
-    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = nullptr;
+    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = p->d_quads = p->d_qblk = nullptr;
     cudaFree(base);
     return SP_ERR_CUDA;
   }
@@ -173,7 +181,7 @@ int sp_plan_upload_to(sp_plan *p, void *device_buffer, size_t buffer_bytes, void
   const DeviceLayout l = device_layout(*p);
   if (buffer_bytes < l.total) return SP_ERR_WORKSPACE;
   if (int rc = copy_tables(p, static_cast<char *>(device_buffer), l, static_cast<cudaStream_t>(stream))) {
-    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = nullptr;
+    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = p->d_quads = p->d_qblk = nullptr;
     return rc;
   }
   p->owns_device = false;

@@ -18,19 +18,25 @@ struct sp_plan {
   // consecutive tiles and, per pair, the merged list of 128-key blocks
   std::vector<int32_t> pairs;   // [p][4] = {tile_a, tile_b or -1, blk_begin, blk_count}
   std::vector<int32_t> pblk;    // [b][4] = {kb, end_a or 0, end_b or 0, causal bits}
+  // paired-SM forward work items (built at upload): four tiles per CTA pair
+  // and their merged key-block list (see build_quads)
+  std::vector<int32_t> quads;   // [q][6] = {a0, a1, b0, b1 (or -1), blk_begin, blk_count}
+  std::vector<int32_t> qblk;    // [b][8] = {kb, end a0, a1, b0, b1 (or 0), causal bits, 0, 0}
   // backward key blocks in launch order (built at upload; same rows as bwd),
   // and the total and longest query-run length over them
   std::vector<int32_t> bwd_sched;  // [k][5]
   int64_t bwd_run_sum = 0;
   int32_t bwd_run_max = 0;
   // device copies (owned), valid after sp_plan_upload
-  int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr, *d_pairs = nullptr, *d_pblk = nullptr;
+  int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr, *d_pairs = nullptr, *d_pblk = nullptr,
+          *d_quads = nullptr, *d_qblk = nullptr;
   int device = -1;
   bool owns_device = false;  // the device tables were allocated by sp_plan_upload
   int32_t n_tiles() const { return int32_t(tiles.size() / 5); }
   int32_t n_ranges() const { return int32_t(ranges.size() / 2); }
   int32_t n_bwd() const { return int32_t(bwd.size() / 5); }
   int32_t n_pairs() const { return int32_t(pairs.size() / 4); }
+  int32_t n_quads() const { return int32_t(quads.size() / 6); }
 };
 
 namespace spc {
@@ -46,6 +52,8 @@ int build_plan(const sp_tree_desc &tree, int32_t tile_tokens, int32_t kv_block, 
 void build_bwd_schedule(sp_plan &plan);
 // Forward pairs and merged block lists from the tiles (see sp_plan::pairs).
 void build_pairs(sp_plan &plan, int32_t block_keys);
+// Paired-SM forward quads and their merged block lists (see sp_plan::quads).
+void build_quads(sp_plan &plan, int32_t block_keys);
 
 // Device-side view of a plan passed to kernels by value.
 struct PlanDev {
@@ -58,6 +66,9 @@ struct PlanDev {
   int32_t n_pairs;
   int64_t bwd_run_sum;  // sum of q1 - q0 over the bwd rows
   int32_t bwd_run_max;  // longest q1 - q0
+  const int32_t *quads;
+  const int32_t *qblk;
+  int32_t n_quads;
 };
 
 struct AttnShape {
@@ -75,6 +86,10 @@ int simt_bwd(const PlanDev &p, const AttnShape &s, int32_t dtype, const void *q,
 // Tensor-core kernels (sm_103a): bf16 input, tile_tokens * G == 128, kv_block == 128.
 int tc_fwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, void *o, float *lse,
            int32_t *d_status, void *stream);
+// The same forward on a pair of SMs (attn_fwd_pair_sm103a.cu): head_dim 128
+// only; SP_ERR_UNSUPPORTED (nothing launched) where it does not apply.
+int tc_fwd_pair(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, void *o,
+                float *lse, int32_t *d_status, void *stream);
 // delta: [Hq][T] fp32 scratch; dqacc: [T][Hq][D] fp32 scratch (zeroed inside;
 // unused when deterministic, which computes dQ per query tile with tc_dq).
 // ev_begin / ev_end (cudaEvent_t, optional): recorded on the stream just before

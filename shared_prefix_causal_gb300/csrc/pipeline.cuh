@@ -23,9 +23,12 @@ struct Ctl {
   uint32_t limit = kSpinLimit;
   __device__ uint32_t bar(int i) const { return bar0 + 8u * uint32_t(i); }
   // Bounded wait; false if it expired here or another role gave up first.
+  // kCluster: cluster-scope acquire, for barriers the peer CTA of a pair
+  // arrives on.
+  template <bool kCluster = false>
   __device__ bool wait(int i, uint32_t parity) const {
     for (uint32_t it = 0;; ++it) {
-      if (ptx::mbar_try_wait(bar(i), parity)) return true;
+      if (kCluster ? ptx::mbar_try_wait_cluster(bar(i), parity) : ptx::mbar_try_wait(bar(i), parity)) return true;
       if ((it & 255u) == 255u) {
         if (*abort) return false;
         if (it >= limit) {
@@ -36,6 +39,7 @@ struct Ctl {
       }
     }
   }
+  __device__ bool wait_cluster(int i, uint32_t parity) const { return wait<true>(i, parity); }
   // Same for a whole warp: one lane polls (32 lanes polling one barrier
   // serialise on it and starve the warps that do the work), the others wait
   // at __syncwarp, which also orders their later reads after lane 0's acquire.

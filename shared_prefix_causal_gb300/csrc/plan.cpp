@@ -11,6 +11,8 @@
 // emitted and sorted.  The canonical output (tile order, range merging,
 // backward order) is documented in the public header.
 #include <algorithm>
+#include <climits>
+#include <cstdint>
 #include <numeric>
 #include <utility>
 #include <vector>
@@ -239,6 +241,88 @@ void build_pairs(sp_plan &plan, int32_t block_keys) {
       plan.pblk.insert(plan.pblk.end(), {kb, ea, eb, flags});
     }
     plan.pairs.insert(plan.pairs.end(), {t, tb, begin, int32_t(plan.pblk.size() / 4) - begin});
+  }
+}
+
+// Work items of the paired-SM forward.  A couple is two consecutive tiles of
+// one segment (offsets 2i and 2i + 1, or a segment's last odd tile alone):
+// their key-block lists are the same up to one block, so one M = 256 product
+// over a pair of SMs (one tile per SM) wastes almost nothing.  Couples are
+// taken in the order their first tiles appear in the schedule (couple i of
+// sibling segments side by side) and grouped two by two into quads: couple
+// 2q in slot a, couple 2q + 1 in slot b.  A quad's merged key-block list feeds
+// all four tiles: qblk entry {kb, end[4], causal bits, 0, 0} with tile slots
+// a0, a1, b0, b1 (end 0: the tile does not read that block).
+void build_quads(sp_plan &plan, int32_t block_keys) {
+  plan.quads.clear();
+  plan.qblk.clear();
+  const int32_t nt = plan.n_tiles(), ns = plan.num_segments, tt = plan.tile_tokens;
+  if (nt == 0) return;
+  std::vector<int32_t> first(ns, INT32_MAX), count(ns, 0);
+  for (int32_t t = 0; t < nt; ++t) {
+    const int32_t sg = plan.tiles[5 * size_t(t)];
+    first[sg] = std::min(first[sg], plan.tiles[5 * size_t(t) + 1]);
+    ++count[sg];
+  }
+  std::vector<int64_t> base(size_t(ns) + 1, 0);
+  for (int32_t sg = 0; sg < ns; ++sg) base[sg + 1] = base[sg] + count[sg];
+  std::vector<int32_t> at(nt, -1);
+  auto offset_of = [&](int32_t t) {
+    return (plan.tiles[5 * size_t(t) + 1] - first[plan.tiles[5 * size_t(t)]]) / tt;
+  };
+  for (int32_t t = 0; t < nt; ++t) at[base[plan.tiles[5 * size_t(t)]] + offset_of(t)] = t;
+  std::vector<int32_t> couples;  // [c][2]
+  couples.reserve(size_t(nt) + 2);
+  for (int32_t t = 0; t < nt; ++t) {
+    const int32_t k = offset_of(t), sg = plan.tiles[5 * size_t(t)];
+    if (k & 1) continue;
+    couples.push_back(t);
+    couples.push_back(k + 1 < count[sg] ? at[base[sg] + k + 1] : -1);
+  }
+  const int32_t nc = int32_t(couples.size() / 2);
+  struct B {
+    int32_t kb, end;
+    bool causal;
+  };
+  std::vector<B> lists[4];
+  // a tile's 128-key blocks in key order: each range from its start, the
+  // last range (the tile's own segment) flagged causal
+  auto tile_blocks = [&](int32_t t, std::vector<B> &out) {
+    out.clear();
+    if (t < 0) return;
+    const int32_t *tl = &plan.tiles[5 * size_t(t)];
+    const int32_t last = tl[4] - 1;
+    for (int32_t r = 0; r <= last; ++r) {
+      const int32_t a = plan.ranges[2 * size_t(tl[3] + r)], e = plan.ranges[2 * size_t(tl[3] + r) + 1];
+      for (int32_t kb = a; kb < e;) {
+        out.push_back({kb, e, r == last});
+        kb += block_keys;
+      }
+    }
+  };
+  for (int32_t c = 0; c < nc; c += 2) {
+    const int32_t tiles4[4] = {couples[2 * size_t(c)], couples[2 * size_t(c) + 1],
+                               c + 1 < nc ? couples[2 * size_t(c) + 2] : -1,
+                               c + 1 < nc ? couples[2 * size_t(c) + 3] : -1};
+    for (int i = 0; i < 4; ++i) tile_blocks(tiles4[i], lists[i]);
+    const int32_t begin = int32_t(plan.qblk.size() / 8);
+    size_t pos[4] = {0, 0, 0, 0};
+    for (;;) {
+      int32_t kb = INT32_MAX;
+      for (int i = 0; i < 4; ++i)
+        if (pos[i] < lists[i].size()) kb = std::min(kb, lists[i][pos[i]].kb);
+      if (kb == INT32_MAX) break;
+      int32_t e[4] = {0, 0, 0, 0}, flags = 0;
+      for (int i = 0; i < 4; ++i)
+        if (pos[i] < lists[i].size() && lists[i][pos[i]].kb == kb) {
+          e[i] = lists[i][pos[i]].end;
+          flags |= lists[i][pos[i]].causal ? (1 << i) : 0;
+          ++pos[i];
+        }
+      plan.qblk.insert(plan.qblk.end(), {kb, e[0], e[1], e[2], e[3], flags, 0, 0});
+    }
+    plan.quads.insert(plan.quads.end(),
+                      {tiles4[0], tiles4[1], tiles4[2], tiles4[3], begin, int32_t(plan.qblk.size() / 8) - begin});
   }
 }
 

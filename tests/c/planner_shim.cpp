@@ -15,11 +15,13 @@ SP_API void *shim_plan(const sp_tree_desc *t, int32_t tile, int32_t kvb, int32_t
   return p;
 }
 
-// Builds the tables the kernels read (forward tile pairs and their merged
-// 128-key block lists; the backward launch order), as the first upload does.
+// Builds the tables the kernels read (forward tile pairs and quads with their
+// merged 128-key block lists; the backward launch order), as the first upload
+// does.
 SP_API void shim_device_tables(void *h) {
   sp_plan *p = static_cast<sp_plan *>(h);
   spc::build_pairs(*p, 128);
+  spc::build_quads(*p, 128);
   spc::build_bwd_schedule(*p);
 }
 
@@ -27,11 +29,13 @@ SP_API int64_t shim_bwd_run_sum(void *h) { return static_cast<const sp_plan *>(h
 SP_API int32_t shim_bwd_run_max(void *h) { return static_cast<const sp_plan *>(h)->bwd_run_max; }
 
 // which: 0 tiles [n][5], 1 ranges [n][2], 2 bwd [n][5], 3 pairs [n][4],
-// 4 pblk [n][4], 5 bwd_sched [n][5]; returns the row count
+// 4 pblk [n][4], 5 bwd_sched [n][5], 6 quads [n][6], 7 qblk [n][8]; returns
+// the row count
 SP_API int32_t shim_rows(void *h, int32_t which, const int32_t **data) {
   const sp_plan *p = static_cast<const sp_plan *>(h);
-  static const int width[6] = {5, 2, 5, 4, 4, 5};
-  const std::vector<int32_t> *tables[6] = {&p->tiles, &p->ranges, &p->bwd, &p->pairs, &p->pblk, &p->bwd_sched};
+  static const int width[8] = {5, 2, 5, 4, 4, 5, 6, 8};
+  const std::vector<int32_t> *tables[8] = {&p->tiles, &p->ranges, &p->bwd,       &p->pairs,
+                                           &p->pblk,  &p->bwd_sched, &p->quads, &p->qblk};
   const std::vector<int32_t> &v = *tables[which];
   *data = v.data();
   return int32_t(v.size() / width[which]);

@@ -73,15 +73,15 @@ class Host:
 
     def device_tables(self, st, ln, par, dep, tile, kvb, order):
         """The plan and the tables its first upload builds: a dict of tiles, ranges, bwd, pairs, pblk,
-        bwd_sched, run_sum and run_max, or the status of a refused call."""
+        bwd_sched, quads, qblk, run_sum and run_max, or the status of a refused call."""
         d, keep = self._desc(st, ln, par, dep)
         rc = ctypes.c_int32()
         h = self.lib.shim_plan(ctypes.byref(d), tile, kvb, order, ctypes.byref(rc))
         if rc.value:
             return rc.value
         self.lib.shim_device_tables(h)
-        names = ("tiles", "ranges", "bwd", "pairs", "pblk", "bwd_sched")
-        out = {n: self._rows(h, i, w) for i, (n, w) in enumerate(zip(names, (5, 2, 5, 4, 4, 5)))}
+        names = ("tiles", "ranges", "bwd", "pairs", "pblk", "bwd_sched", "quads", "qblk")
+        out = {n: self._rows(h, i, w) for i, (n, w) in enumerate(zip(names, (5, 2, 5, 4, 4, 5, 6, 8)))}
         out["run_sum"], out["run_max"] = int(self.lib.shim_bwd_run_sum(h)), int(self.lib.shim_bwd_run_max(h))
         self.lib.shim_free(h)
         return out

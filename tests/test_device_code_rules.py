@@ -2,11 +2,12 @@
 
 The GPU is shared with other users, so a kernel must never hang or trap it.
 These rules keep later edits from quietly breaking that:
-  * every mbarrier poll goes through the bounded waits of ``pipeline.cuh``;
+  * every mbarrier poll (CTA or cluster scope) goes through the bounded waits
+    of ``pipeline.cuh``;
   * no loop without a condition outside those waits;
   * no trap, breakpoint or device assert;
-  * every TMEM allocation is matched by a deallocation that no early return
-    skips (returns inside a lambda leave only the lambda).
+  * every TMEM allocation (one SM or a pair) is matched by a deallocation that
+    no early return skips (returns inside a lambda leave only the lambda).
 The sources are read as text with comments removed; nothing is compiled.
 """
 import glob
@@ -49,9 +50,9 @@ def test_device_sources_exist():
 
 @pytest.mark.parametrize("path", DEVICE_FILES, ids=_name)
 def test_mbarrier_polls_only_in_the_bounded_waits(path):
-    calls = re.findall(r"\bmbar_try_wait\s*\(", _code(path))
+    calls = re.findall(r"\bmbar_try_wait(?:_cluster)?\s*\(", _code(path))
     if _name(path) == "sm103_ptx.cuh":
-        assert len(calls) == 1  # the definition
+        assert len(calls) == 2  # the definitions (CTA and cluster scope)
     elif _name(path) != "pipeline.cuh":
         assert not calls, "poll an mbarrier through spc::Ctl (bounded), not directly"
 
@@ -76,8 +77,8 @@ def test_loops_without_a_condition_only_in_the_bounded_waits(path):
 @pytest.mark.parametrize("path", DEVICE_FILES, ids=_name)
 def test_tmem_is_freed_on_every_path(path):
     code = _code(path)
-    allocs = [m.start() for m in re.finditer(r"\btmem_alloc\s*\(", code)]
-    deallocs = [m.start() for m in re.finditer(r"\btmem_dealloc\s*\(", code)]
+    allocs = [m.start() for m in re.finditer(r"\btmem_alloc(?:_pair)?\s*\(", code)]
+    deallocs = [m.start() for m in re.finditer(r"\btmem_dealloc(?:_pair)?\s*\(", code)]
     if _name(path) == "sm103_ptx.cuh":
         return  # the helpers' definitions
     assert len(allocs) == len(deallocs)

@@ -10,8 +10,15 @@ list and the backward's launch order:
     i when bit t is set;
   * bwd_sched: the backward table's rows in launch order (latest run end
     first, longest run first within a run end), with the runs' sum and maximum.
-These checks hold the tables to that reading, to the forward kernel's own
-validity test, and to the canonical plan.  The tables come from the host-only
+  * quads [n][6] = {a0, a1, b0, b1 (or -1), first entry, entry count}: the
+    paired-SM forward's work items.  A couple (a0, a1) or (b0, b1) is two
+    consecutive tiles of one segment (offsets 2i and 2i + 1; a segment's last
+    odd tile alone), couples in the order of their first tiles in the
+    schedule, two per quad;
+  * qblk [m][8] = {kb, end a0, a1, b0, b1 (or 0), causal bits, 0, 0}: the
+    quad's 128-key blocks merged by start, read as the pairs' entries are.
+These checks hold the tables to that reading, to the forward kernels' own
+validity tests, and to the canonical plan.  The tables come from the host-only
 build of the planner (no CUDA).
 """
 import shutil
@@ -75,6 +82,7 @@ def check_device_tables(T, d):
             cut = np.nonzero(k1[:-1] != k0[1:])[0]  # merged runs of the covered blocks
             got = list(zip(np.r_[k0[:1], k0[cut + 1]].tolist(), np.r_[k1[cut], k1[-1:]].tolist()))
             assert got == _merge(want), "blocks do not cover the tile's ranges exactly"
+    check_quad_tables(T, d)
     bwd, sched = d["bwd"], d["bwd_sched"]
     assert sorted(map(tuple, sched.tolist())) == sorted(map(tuple, bwd.tolist()))
     runs = sched[:, 4] - sched[:, 3]
@@ -87,6 +95,85 @@ def check_device_tables(T, d):
     assert d["run_sum"] == int(runs.sum()) and d["run_max"] == (int(runs.max()) if len(runs) else 0)
 
 
+def _check_entries(tiles, ranges, ent, col, t, bit):
+    """Entries of one tile (end in column ``col``, causal flag ``bit``) cover its ranges exactly."""
+    _, _, _, rb, rc = tiles[t]
+    want = [tuple(map(int, ranges[r])) for r in range(rb, rb + rc)]
+    last = want[-1]
+    end = ent[:, col]
+    causal = ((ent[:, 5] >> bit) & 1).astype(bool)
+    assert not causal[end == 0].any()
+    sel = end > 0
+    k0 = ent[sel, 0].astype(np.int64)
+    k1 = np.minimum(k0 + BLOCK, end[sel])
+    assert (causal[sel] == ((k0 >= last[0]) & (k1 <= last[1]))).all(), "causal flag off the own range"
+    assert (k1[:-1] <= k0[1:]).all(), "a key read twice"
+    cut = np.nonzero(k1[:-1] != k0[1:])[0]
+    got = list(zip(np.r_[k0[:1], k0[cut + 1]].tolist(), np.r_[k1[cut], k1[-1:]].tolist()))
+    assert got == _merge(want), "blocks do not cover the tile's ranges exactly"
+
+
+def check_quad_tables(T, d):
+    """The paired-SM forward's quads and their merged block lists."""
+    tiles, ranges, quads, qblk = d["tiles"], d["ranges"], d["quads"], d["qblk"]
+    nt = len(tiles)
+    if nt == 0:
+        assert len(quads) == 0 and len(qblk) == 0
+        return
+    seg = tiles[:, 0]
+    first = {}
+    for t in range(nt):
+        first[int(seg[t])] = min(first.get(int(seg[t]), 1 << 40), int(tiles[t, 1]))
+    tt = d.get("tile_tokens")
+    per_seg = {}
+    for t in range(nt):
+        per_seg.setdefault(int(seg[t]), []).append(t)
+    # tile offset within its segment, from the smallest gap of the segment's tile starts
+    offs = np.zeros(nt, np.int64)
+    for sg, ts in per_seg.items():
+        starts = sorted(int(tiles[t, 1]) for t in ts)
+        step = tt or (starts[1] - starts[0] if len(starts) > 1 else 1)
+        for t in ts:
+            offs[t] = (int(tiles[t, 1]) - first[sg]) // step
+    seen = np.zeros(nt, np.int64)
+    couples = []
+    begin = 0
+    for a0, a1, b0, b1, e0, cnt in quads:
+        assert a0 >= 0 and e0 == begin and cnt >= 1
+        begin += cnt
+        for x, y in ((a0, a1), (b0, b1)):
+            if x < 0:
+                assert y < 0
+                continue
+            couples.append(x)
+            assert offs[x] % 2 == 0, "a couple starts on an odd tile"
+            seen[x] += 1
+            if y >= 0:
+                assert seg[y] == seg[x] and offs[y] == offs[x] + 1, "a couple is not two consecutive tiles"
+                seen[y] += 1
+            else:
+                assert offs[x] == len(per_seg[int(seg[x])]) - 1, "a tile left without its partner"
+    assert begin == len(qblk)
+    assert (seen == 1).all(), "a tile missing from the quads or in two of them"
+    assert couples == sorted(couples), "couples not in schedule order"
+    assert (quads[:-1, 2] >= 0).all(), "slot b empty before the last quad"
+    present = np.repeat((quads[:, :4] >= 0), quads[:, 5], axis=0)
+    kb, ends = qblk[:, 0], qblk[:, 1:5]
+    # the paired-SM kernel's own test of each entry
+    assert ((0 <= kb) & (kb < T)).all()
+    assert (((ends == 0) | (present & (ends > kb[:, None]) & (ends <= T))).all())
+    assert (ends > 0).any(axis=1).all()
+    assert (qblk[:, 6:] == 0).all()
+    for q, (a0, a1, b0, b1, e0, cnt) in enumerate(quads):
+        ent = qblk[e0:e0 + cnt]
+        assert (np.diff(ent[:, 0]) > 0).all(), "entries not merged by block start"
+        for i, t in enumerate((a0, a1, b0, b1)):
+            if t < 0:
+                assert not (ent[:, 1 + i]).any() and not ((ent[:, 5] >> i) & 1).any()
+                continue
+            _check_entries(tiles, ranges, ent, 1 + i, t, i)
+
+
 @pytest.fixture(scope="module")
 def host(tmp_path_factory):
     d = tmp_path_factory.mktemp("device_tables")
@@ -96,6 +183,7 @@ def host(tmp_path_factory):
 def _tables(host, t, tile, order=0):
     d = host.device_tables(t.seg_start, t.seg_len, t.parent, t.depth, tile, BLOCK, order)
     assert not isinstance(d, int), f"refused ({d})"
+    d["tile_tokens"] = tile
     return d
 
 
@@ -118,6 +206,7 @@ def test_single_tile_and_empty_plans(host):
     one = W.tree_from_preorder([40], [-1])
     d = _tables(host, one, 128)
     assert d["pairs"].tolist() == [[0, -1, 0, 1]] and d["pblk"].tolist() == [[0, 40, 0, 1]]
+    assert d["quads"].tolist() == [[0, -1, -1, -1, 0, 1]] and d["qblk"].tolist() == [[0, 40, 0, 0, 0, 1, 0, 0]]
     check_device_tables(40, d)
     empty = host.device_tables([], [], [], [], 128, BLOCK, 0)
     assert len(empty["pairs"]) == 0 and len(empty["bwd_sched"]) == 0 and empty["run_max"] == 0
@@ -133,6 +222,12 @@ def test_the_checks_catch_broken_tables(host):
         lambda d: d["pairs"].__setitem__((0, 3), d["pairs"][0, 3] - 1),      # an entry dropped from a pair
         lambda d: d["bwd_sched"].__setitem__(slice(None), d["bwd_sched"][::-1].copy()),  # launch order reversed
         lambda d: d.__setitem__("run_max", d["run_max"] + 1),
+    ]
+    breaks += [
+        lambda d: d["qblk"].__setitem__((0, 5), d["qblk"][0, 5] ^ 1),        # a quad's causal bit flipped
+        lambda d: d["qblk"].__setitem__((0, 1), d["qblk"][0, 1] - 1),        # a quad's block end cut short
+        lambda d: d["quads"].__setitem__((0, 5), d["quads"][0, 5] - 1),      # an entry dropped from a quad
+        lambda d: d["quads"].__setitem__((0, 1), d["quads"][0, 2]),          # a couple of two segments
     ]
     for brk in breaks:
         bad = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in good.items()}

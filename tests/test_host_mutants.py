@@ -2,7 +2,7 @@
 
 Each case plants one plausible mistake in a copy of ``plan.cpp`` (tree
 validation, tiling, range merging, ordering, the backward table, the forward
-pairs and the backward launch order built at upload) or
+pairs and quads and the backward launch order built at upload) or
 ``fragments.cpp`` (the bounded fragment planner).  The copy is built with g++
 into a small host-only library, together with ``tests/c/planner_shim.cpp``.
 The case then runs the checks the planner's parity tests make (hand-derived
@@ -81,6 +81,17 @@ MUTANTS = [
     ("plan.cpp", "plan.bwd_run_max = std::max(plan.bwd_run_max, len(i));", "plan.bwd_run_max = len(i);",
      "longest backward run mis-counted"),
     ("plan.cpp", "plan.bwd_run_sum += len(i);", "plan.bwd_run_sum = len(i);", "backward run sum mis-counted"),
+    ("plan.cpp", "couples.push_back(k + 1 < count[sg] ? at[base[sg] + k + 1] : -1);",
+     "couples.push_back(k + 2 < count[sg] ? at[base[sg] + k + 1] : -1);", "a segment's last partner tile dropped"),
+    ("plan.cpp", "    if (k & 1) continue;", "    if (!(k & 1)) continue;", "couples started on odd tiles"),
+    ("plan.cpp", "flags |= lists[i][pos[i]].causal ? (1 << i) : 0;", "flags |= lists[i][pos[i]].causal ? (1 << (i & 1)) : 0;",
+     "quad causal bits of slot b written to slot a"),
+    ("plan.cpp", "        out.push_back({kb, e, r == last});", "        out.push_back({kb, e, r == 0});",
+     "quad blocks flagged causal on the first range"),
+    ("plan.cpp", "                               c + 1 < nc ? couples[2 * size_t(c) + 2] : -1,",
+     "                               c + 1 < nc ? couples[2 * size_t(c)] : -1,", "a quad's slot b repeats slot a"),
+    ("plan.cpp", "        if (pos[i] < lists[i].size()) kb = std::min(kb, lists[i][pos[i]].kb);",
+     "        if (pos[i] < lists[i].size()) kb = lists[i][pos[i]].kb;", "quad block lists not merged by start"),
     ("fragments.cpp", "if (!cur_seg.empty() && cur_tokens + extra > cap) {",
      "if (!cur_seg.empty() && cur_tokens + extra >= cap) {", "a fragment never fills the cap exactly"),
     ("fragments.cpp", "      emit();\n      extra = path_tokens;", "      emit();",
