@@ -732,6 +732,67 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
                         "D2H of dQ,dK,dV and gathered rows"}
 
 
+def cta_tail_stats(rec):
+    """Tail of one launch from its per-CTA records [n, 4] = (start ns, end ns, SM, 0): the launch's span,
+    the share of SM-time left idle after each SM's last CTA ended (the last wave's idle time), and the
+    share of SM-time the CTAs occupied."""
+    rec = rec[rec[:, 1] > 0]
+    start, end, sm = rec[:, 0].astype(np.float64), rec[:, 1].astype(np.float64), rec[:, 2]
+    t0, t1 = start.min(), end.max()
+    span = t1 - t0
+    sms = np.unique(sm)
+    last = np.array([end[sm == x].max() for x in sms])
+    busy = float((end - start).sum() / (span * len(sms)))
+    dur = end - start
+    return {"ctas": int(len(rec)), "sms": int(len(sms)), "span_us": round(span / 1e3, 2),
+            "tail_idle_frac": round(float((t1 - last).sum() / (span * len(sms))), 4),
+            "busy_frac": round(busy, 4), "longest_cta_us": round(float(dur.max()) / 1e3, 2),
+            "median_cta_us": round(float(np.median(dur)) / 1e3, 2),
+            "last_sm_idle_us": round(float(t1 - last.min()) / 1e3, 2)}
+
+
+def run_cta_tail(args):
+    """Per-CTA start/end times of the tensor-core kernels (sp_debug_cta_clock) on one workload: how much
+    SM-time each launch leaves idle at its end, the figure split-KV work division would recover."""
+    import torch
+    dev = torch.device("cuda", 0)
+    import shared_prefix_causal_gb300 as spc
+    w = W.get(args.config)
+    G = w.hq // w.hkv
+    x = W.draw_tensors(w, "bf16")
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "do"))
+    plan = spc.tree_plan(w.tree, 128 // G, 128, 0)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, w.T), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = spc.bwd_workspace(q)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    buf = torch.zeros((1 << 20, 4), dtype=torch.int64, device=dev)
+    scale = w.softmax_scale
+    calls = {
+        "forward": (spc.CLOCK_FORWARD, lambda: spc.sp_tree_attn_fwd(plan, q, k, v, o, lse, scale, st)),
+        "backward key blocks (default)": (spc.CLOCK_KEY_BLOCKS, lambda: spc.sp_tree_attn_bwd(
+            plan, q, k, v, o, lse, do, dq, dk, dv, ws, scale, st)),
+        "backward key blocks (deterministic)": (spc.CLOCK_KEY_BLOCKS, lambda: spc.sp_tree_attn_bwd_deterministic(
+            plan, q, k, v, o, lse, do, dq, dk, dv, ws, scale, st)),
+        "backward query tiles (deterministic dQ)": (spc.CLOCK_QUERY_TILES, lambda: spc.sp_tree_attn_bwd_deterministic(
+            plan, q, k, v, o, lse, do, dq, dk, dv, ws, scale, st)),
+    }
+    out = {"workload": w.description, "tokens": w.T, "kernels": {}}
+    for name, (kid, fn) in calls.items():
+        for _ in range(2):  # warm-up
+            fn()
+        buf.zero_()
+        spc.sp_debug_cta_clock(kid, buf)
+        fn()
+        torch.cuda.synchronize(dev)
+        spc.sp_debug_cta_clock(0)
+        if st.item() != 0:
+            raise RuntimeError(f"device status {st.item()} in {name}")
+        out["kernels"][name] = cta_tail_stats(buf.cpu().numpy())
+    print(json.dumps(out), flush=True)
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -772,6 +833,8 @@ def main():
     ap.add_argument("--ref-flops", type=float, default=1.2e11, help="fp64 flop budget per reference step")
     ap.add_argument("--ref-total-flops", type=float, default=4e12,
                     help="fp64 flop budget of the whole reference run (warm-up and timed steps together)")
+    ap.add_argument("--cta-tail", action="store_true",
+                    help="instead of the bench line: per-CTA timing of the tensor-core kernels (launch tails)")
     ap.add_argument("--_oracle-child", dest="oracle_child", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_child:
@@ -779,7 +842,9 @@ def main():
         return
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.cta_tail:
+        run_cta_tail(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gpu(args)

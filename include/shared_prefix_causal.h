@@ -402,6 +402,19 @@ SP_API int sp_edge_gather(int32_t dtype, const void *hidden, int32_t T, int32_t 
  * Errors: SP_ERR_INVALID_ARG, SP_ERR_CUDA. */
 SP_API int sp_debug_wait_timeout(int32_t spin_limit, int32_t *d_status, void *stream);
 
+/* Measurement hook for the tail of a launch (the pages have no counterpart).
+ * After this call, every launch of the chosen tensor-core kernel records, per
+ * CTA b < max_ctas, four uint64 words at device_buffer[4 b]: the global timer
+ * (ns) when the CTA started and when it finished, the SM it ran on, and 0.
+ * kernel: 1 the forward's main kernel, 2 the backward's per-key-block kernel
+ * (either mode), 3 the deterministic backward's per-query-tile dQ kernel; 0 or
+ * a NULL buffer turns recording off.  The buffer (16-byte aligned, at least
+ * 32 * max_ctas bytes) stays owned by the caller and must outlive the launches;
+ * CTAs at or past max_ctas record nothing.  Process-wide setting, read when a
+ * kernel is launched; not for use while other threads launch these kernels.
+ * Errors: SP_ERR_INVALID_ARG, SP_ERR_ALIGNMENT. */
+SP_API int sp_debug_cta_clock(int32_t kernel, void *device_buffer, int64_t max_ctas);
+
 /* Static English text for a status code (never NULL). */
 SP_API const char *sp_status_string(int status);
 

@@ -99,13 +99,14 @@ _c_gather_bwd_ws = _sig("sp_edge_gather_bwd_workspace_bytes", ctypes.c_size_t, [
 _c_gather_bwd = _sig("sp_edge_gather_bwd", ctypes.c_int,
                      [_i32, _vp, _i32, _i32, _vp, _i32, _vp, _vp, ctypes.c_size_t, _vp, _vp])
 _c_wait_timeout = _sig("sp_debug_wait_timeout", ctypes.c_int, [_i32, _vp, _vp])
+_c_cta_clock = _sig("sp_debug_cta_clock", ctypes.c_int, [_i32, _vp, ctypes.c_int64])
 
 EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy", "sp_tree_attn_fwd",
             "sp_tree_attn_bwd_workspace_bytes", "sp_tree_attn_bwd", "sp_tree_attn_bwd_noalloc", "sp_edge_gather",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
             "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic", "sp_fragment_plan", "sp_fragment_view",
-            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed")
+            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed", "sp_debug_cta_clock")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -415,6 +416,22 @@ def sp_debug_wait_timeout(spin_limit: int, d_status, stream=None):
     with _on(d_status):
         _check(_c_wait_timeout(int(spin_limit), _ptr(d_status), _stream(stream, d_status.device)),
                "sp_debug_wait_timeout")
+
+
+CLOCK_FORWARD, CLOCK_KEY_BLOCKS, CLOCK_QUERY_TILES = 1, 2, 3
+
+
+def sp_debug_cta_clock(kernel: int, buffer=None):
+    """Record per-CTA start/end times of one tensor-core kernel's later launches into ``buffer`` (a CUDA
+    uint64 tensor of shape [n, 4]: start ns, end ns, SM id, 0 per CTA); ``kernel`` 0 or no buffer: off."""
+    import torch
+    if buffer is None or kernel == 0:
+        _check(_c_cta_clock(0, None, 0), "sp_debug_cta_clock")
+        return
+    _need_cuda(buffer)
+    if buffer.dtype not in (torch.int64, torch.uint64) or buffer.dim() != 2 or buffer.shape[1] != 4:
+        raise ValueError("buffer must be an int64 CUDA tensor of shape [n, 4]")
+    _check(_c_cta_clock(int(kernel), _ptr(buffer), int(buffer.shape[0])), "sp_debug_cta_clock")
 
 
 # ------------------------------------------------------------ conveniences

@@ -106,8 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
                   AttnShape s, const float *__restrict__ lse, const float *__restrict__ delta,
                   float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
-                  int32_t *d_status, int head_chunk) {
+                  int32_t *d_status, int head_chunk, CtaClock clk) {
   using L = Layout<D>;
+  const unsigned long long clk0 = clk.begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic so that accesses
   // through it stay shared-memory (not generic) accesses
@@ -472,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  clk.end(clk0);
 }
 
 // Delta = rowsum(dO * O) per (token, query head) in fp32, and zero the fp32
@@ -557,19 +559,26 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (!rc) rc = encode_bf16_3d(&tk, k, D, s.Hkv, s.T, 64, 1, kBK);
   if (!rc) rc = encode_bf16_3d(&tv, v, D, s.Hkv, s.T, 64, 1, kBK);
   if (rc) return rc;
-  auto kern = deterministic ? bwd_tc_kernel<D, G, false> : bwd_tc_kernel<D, G, true>;
+  const int head_chunk = bwd_head_chunk(p, s, sms);
+  if (deterministic) {
+    // dK, dV by the 128-row key-block kernel; dQ without atomics: every query
+    // tile walks its own key blocks
+    const int rc2 = tc_bwd_kv(p, s, q, k, v, lse, d_o, dk, dv, delta, head_chunk, d_status, st, ev_begin, ev_end);
+    if (rc2) return rc2;
+    return tc_dq(p, s, q, k, v, lse, d_o, dq, delta, d_status, st);
+  }
+  auto kern = bwd_tc_kernel<D, G, true>;
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
   const unsigned grid = unsigned(p.n_bwd) * unsigned(s.Hkv);
-  const int head_chunk = bwd_head_chunk(p, s, sms);
   if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return SP_ERR_CUDA;
+  CtaClock clk;
+  cta_clock_for(kClockKeyBlocks, &clk.buf, &clk.cap);
   kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, dqacc, static_cast<__nv_bfloat16 *>(dk),
-                                     static_cast<__nv_bfloat16 *>(dv), d_status, head_chunk);
+                                     static_cast<__nv_bfloat16 *>(dv), d_status, head_chunk, clk);
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return SP_ERR_CUDA;
-  // dQ without atomics: every query tile walks its own key blocks
-  if (deterministic) return tc_dq(p, s, q, k, v, lse, d_o, dq, delta, d_status, st);
 
   const long n8 = rows * D / 8;
   const int cgrid = int(std::min<long>((n8 + 255) / 256, long(sms) * 16));

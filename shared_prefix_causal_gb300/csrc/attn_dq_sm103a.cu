@@ -15,7 +15,9 @@
 // thread = query row = TMEM lane, warpgroup h taking key columns
 // [64h, 64h + 64) of every row (the work needs no row reduction, so the
 // split needs no exchange); warp 8: TMA producer (Q and dO once, K/V blocks
-// through a 2-stage ring); warp 9: tcgen05 MMA issuer.  Per key block
+// through rings of three and two stages: K is read last by dQ, V only by
+// dP, so a third K stage gives the next blocks' loads time to land); warp 9:
+// tcgen05 MMA issuer.  Per key block
 // n the MMA thread issues S = Q K^T and dP = dO V^T (SS), and, once the
 // elementwise warps have stored dS(n) as bf16 pairs in TMEM, dQ += dS(n) K(n)
 // (A read from TMEM, K as an MN-major B).  S(n+1) and dP(n+1) are issued as
@@ -43,21 +45,24 @@ using namespace ptx;
 
 constexpr int kBM = 128;           // query rows per tile (tokens x query heads of one KV head)
 constexpr int kBN = 128;           // keys per block
-constexpr int kStages = 2;         // K/V ring depth
+constexpr int kKStages = 3;        // K ring depth (K is read by S and, last, by dQ)
+constexpr int kVStages = 2;        // V ring depth (V is read by dP only)
 constexpr int kThreads = 320;      // 8 elementwise warps, producer, MMA
 constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int {
   B_Q_FULL = 0,
-  B_KV_FULL = 1,   // +stage
-  B_KV_EMPTY = 3,  // +stage
-  B_S_FULL = 5,
-  B_S_FREE = 6,    // 8 warp arrivals
-  B_DS_FULL = 7,   // +buffer, 8 warp arrivals
-  B_DS_FREE = 9,   // +buffer
-  B_DQ_DONE = 11,
-  B_COUNT = 12
+  B_K_FULL = 1,    // +stage (3)
+  B_K_EMPTY = 4,   // +stage
+  B_V_FULL = 7,    // +stage (2)
+  B_V_EMPTY = 9,   // +stage
+  B_S_FULL = 11,
+  B_S_FREE = 12,   // 8 warp arrivals
+  B_DS_FULL = 13,  // +buffer, 8 warp arrivals
+  B_DS_FREE = 15,  // +buffer
+  B_DQ_DONE = 17,
+  B_COUNT = 18
 };
 
 template <int D>
@@ -67,8 +72,8 @@ struct Layout {
   static constexpr int Q = 0;
   static constexpr int DO = KV;
   static constexpr int K = 2 * KV;  // + stage * KV
-  static constexpr int V = K + kStages * KV;
-  static constexpr int BAR = V + kStages * KV;
+  static constexpr int V = K + kKStages * KV;
+  static constexpr int BAR = V + kVStages * KV;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
   static constexpr int BYTES = ABORT + 4 + 1024;
@@ -96,8 +101,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
                  AttnShape s, const float *__restrict__ lse, const float *__restrict__ delta,
-                 __nv_bfloat16 *__restrict__ dq, int32_t *d_status) {
+                 __nv_bfloat16 *__restrict__ dq, int32_t *d_status, CtaClock clk) {
   using L = Layout<D>;
+  const unsigned long long clk0 = clk.begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -151,21 +157,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sbase + L::DO + c * kChunk, &tm_do, ctl.bar(B_Q_FULL), c * 64, g * G, q0);
       }
       BlockWalk w(rg, rc);
-      int n = 0;
-      for (; n < nblk; ++n, w.next()) {
-        const int st = n & 1;
-        if (!ctl.wait(B_KV_EMPTY + st, ((n >> 1) & 1) ^ 1)) break;
-        mbar_arrive_expect_tx(ctl.bar(B_KV_FULL + st), 2u * L::KV);
+      int nk = 0, nv = 0;  // K and V blocks issued
+      for (int n = 0; n < nblk; ++n, w.next()) {
+        const int ks = n % kKStages, vs = n % kVStages;
+        if (!ctl.wait(B_K_EMPTY + ks, ((n / kKStages) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(ctl.bar(B_K_FULL + ks), L::KV);
 #pragma unroll
-        for (int c = 0; c < L::kDChunks; ++c) {
-          tma_load_3d(sbase + L::K + st * L::KV + c * kChunk, &tm_k, ctl.bar(B_KV_FULL + st), c * 64, g, w.kb);
-          tma_load_3d(sbase + L::V + st * L::KV + c * kChunk, &tm_v, ctl.bar(B_KV_FULL + st), c * 64, g, w.kb);
-        }
+        for (int c = 0; c < L::kDChunks; ++c)
+          tma_load_3d(sbase + L::K + ks * L::KV + c * kChunk, &tm_k, ctl.bar(B_K_FULL + ks), c * 64, g, w.kb);
+        ++nk;
+        if (!ctl.wait(B_V_EMPTY + vs, ((n / kVStages) & 1) ^ 1)) break;
+        mbar_arrive_expect_tx(ctl.bar(B_V_FULL + vs), L::KV);
+#pragma unroll
+        for (int c = 0; c < L::kDChunks; ++c)
+          tma_load_3d(sbase + L::V + vs * L::KV + c * kChunk, &tm_v, ctl.bar(B_V_FULL + vs), c * 64, g, w.kb);
+        ++nv;
       }
       if (*ctl.abort) {
         // let the fills still in flight land before the CTA exits
         ctl.drain(B_Q_FULL, 0);
-        for (int m = n - kStages < 0 ? 0 : n - kStages; m < n; ++m) ctl.drain(B_KV_FULL + (m & 1), (m >> 1) & 1);
+        for (int m = nk - kKStages < 0 ? 0 : nk - kKStages; m < nk; ++m)
+          ctl.drain(B_K_FULL + m % kKStages, (m / kKStages) & 1);
+        for (int m = nv - kVStages < 0 ? 0 : nv - kVStages; m < nv; ++m)
+          ctl.drain(B_V_FULL + m % kVStages, (m / kVStages) & 1);
       }
     }
   } else if (warp == 9) {
@@ -177,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ddo_a = smem_desc_sw128(sbase + L::DO, 16, 1024);
       // S(n), dP(n) into TMEM; one commit for both
       auto issue_s = [&](int n) {
-        const uint32_t kst = sbase + L::K + (n & 1) * L::KV, vst = sbase + L::V + (n & 1) * L::KV;
+        const uint32_t kst = sbase + L::K + (n % kKStages) * L::KV, vst = sbase + L::V + (n % kVStages) * L::KV;
         const uint64_t dk = smem_desc_sw128(kst, 16, 1024), dv = smem_desc_sw128(vst, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -190,8 +204,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ss(tmem + T_DP, ddo_a + off, dv + off, id_s, kk > 0);
         }
         mma_commit(ctl.bar(B_S_FULL));
+        mma_commit(ctl.bar(B_V_EMPTY + n % kVStages));  // V(n) is read by dP(n) only
       };
-      bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_KV_FULL, 0);
+      bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_K_FULL, 0) && ctl.wait(B_V_FULL, 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -201,19 +216,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n + 1 < nblk) {
           // S(n) and dP(n) have been read out: S(n+1), dP(n+1) may overwrite them
           if (!(ok = ctl.wait(B_S_FREE, n & 1))) break;
-          if (!(ok = ctl.wait(B_KV_FULL + (st ^ 1), ((n + 1) >> 1) & 1))) break;
+          if (!(ok = ctl.wait(B_K_FULL + (n + 1) % kKStages, ((n + 1) / kKStages) & 1))) break;
+          if (!(ok = ctl.wait(B_V_FULL + (n + 1) % kVStages, ((n + 1) / kVStages) & 1))) break;
           tc_fence_after();
           issue_s(n + 1);
         }
         if (!(ok = ctl.wait(B_DS_FULL + st, (n >> 1) & 1))) break;
         tc_fence_after();
-        const uint64_t dk_mn = smem_desc_sw128(sbase + L::K + st * L::KV, kChunk, 1024);
+        const uint64_t dk_mn = smem_desc_sw128(sbase + L::K + (n % kKStages) * L::KV, kChunk, 1024);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_bf16_ts(tmem + T_DQ, tmem + T_DS + 64 * st + 8 * kk, dk_mn + ((kk * 2048) >> 4), id_q,
                       (n > 0 || kk > 0));
         mma_commit(ctl.bar(B_DS_FREE + st));
-        mma_commit(ctl.bar(B_KV_EMPTY + st));
+        mma_commit(ctl.bar(B_K_EMPTY + n % kKStages));
       }
       mma_commit(ctl.bar(B_DQ_DONE));
       ctl.drain(B_DQ_DONE, 0);
@@ -240,40 +256,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0);
       // keys [kb, kb + lim) visible to this row
       const int lim = !rowv ? 0 : (causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb);
+      // this group's 64 columns of S and dP, all loaded before S_FREE so the
+      // next block's S and dP products can start at once
+      uint32_t us[64], ud[64];
+      tmem_ld32x2(tmem + lane_base + T_S + 64 * h, tmem + lane_base + T_DP + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(us),
+                  *reinterpret_cast<uint32_t(*)[32]>(ud));
+      tmem_ld32x2(tmem + lane_base + T_S + 64 * h + 32, tmem + lane_base + T_DP + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(us + 32), *reinterpret_cast<uint32_t(*)[32]>(ud + 32));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctl.bar(B_S_FREE));
+      // P (in place of S), then dS (in place of dP)
+      if (full && rowv) {
 #pragma unroll
-      for (int cc = 0; cc < kBN / 64; ++cc) {
-        const int c = 2 * h + cc;  // 32-column chunk of the block
-        uint32_t us[32], ud[32];
-        tmem_ld32x2(tmem + lane_base + T_S + 32 * c, tmem + lane_base + T_DP + 32 * c, us, ud);
-        if (cc == kBN / 64 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ctl.bar(B_S_FREE));
+        for (int i = 0; i < 64; i += 2) {
+          float p0, p1;
+          ffma2(p0, p1, __uint_as_float(us[i]), __uint_as_float(us[i + 1]), sl2, sl2, nl2, nl2);
+          us[i] = __float_as_uint(p0), us[i + 1] = __float_as_uint(p1);
         }
-        float pv[32], dsv[32];
-        if (full && rowv) {
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            ffma2(pv[i], pv[i + 1], __uint_as_float(us[i]), __uint_as_float(us[i + 1]), sl2, sl2, nl2, nl2);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pv[i] = 32 * c + i < lim ? fmaf(__uint_as_float(us[i]), sl2, nl2) : -INFINITY;
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) pv[i] = ex2(pv[i]);
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float t0, t1;
-          fadd2(t0, t1, __uint_as_float(ud[i]), __uint_as_float(ud[i + 1]), ndl, ndl);
-          fmul2(dsv[i], dsv[i + 1], pv[i], pv[i + 1], t0, t1);
-        }
-        // dS(n) goes to buffer st once dQ(n-2) has read it
-        if (cc == 0 && !(ok = ctl.wait_warp(B_DS_FREE + st, ((n >> 1) & 1) ^ 1))) break;
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(dsv[2 * i], dsv[2 * i + 1]);
-        tmem_st16(tmem + lane_base + T_DS + 64 * st + 16 * c, pk);
+        for (int i = 0; i < 64; ++i)
+          us[i] = __float_as_uint(64 * h + i < lim ? fmaf(__uint_as_float(us[i]), sl2, nl2) : -INFINITY);
       }
+#pragma unroll
+      for (int i = 0; i < 64; ++i) us[i] = __float_as_uint(ex2(__uint_as_float(us[i])));
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        float t0, t1, d0, d1;
+        fadd2(t0, t1, __uint_as_float(ud[i]), __uint_as_float(ud[i + 1]), ndl, ndl);
+        fmul2(d0, d1, __uint_as_float(us[i]), __uint_as_float(us[i + 1]), t0, t1);
+        pk[i / 2] = pack_bf16(d0, d1);
+      }
+      // dS(n) goes to buffer st once dQ(n-2) has read it
+      if (!(ok = ctl.wait_warp(B_DS_FREE + st, ((n >> 1) & 1) ^ 1))) break;
+      tmem_st32(tmem + lane_base + T_DS + 64 * st + 32 * h, pk);
       if (!ok) break;
       tmem_st_wait();
       tc_fence_before();
@@ -310,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  clk.end(clk0);
 }
 
 template <int D, int G>
@@ -326,7 +345,10 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
   const unsigned grid = unsigned(p.n_tiles) * unsigned(s.Hkv);
-  kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, static_cast<__nv_bfloat16 *>(dq), d_status);
+  CtaClock clk;
+  cta_clock_for(kClockQueryTiles, &clk.buf, &clk.cap);
+  kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, static_cast<__nv_bfloat16 *>(dq), d_status,
+                                     clk);
   return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 

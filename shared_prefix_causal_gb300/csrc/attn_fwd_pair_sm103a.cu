@@ -93,8 +93,9 @@ struct Layout {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, PlanDev plan, AttnShape s,
-                    __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, int32_t *d_status) {
+                    __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, int32_t *d_status, CtaClock clk) {
   using L = Layout;
+  const unsigned long long clk0 = clk.begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
@@ -399,6 +400,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
   }
+  clk.end(clk0);
 }
 
 }  // namespace
@@ -418,7 +420,10 @@ int tc_fwd_pair(const PlanDev &p, const AttnShape &s, const void *q, const void 
   if (cudaFuncSetAttribute(fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
   const unsigned grid = 2u * unsigned(p.n_quads) * unsigned(s.Hkv);
-  fwd_pair_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, p, s, static_cast<__nv_bfloat16 *>(o), lse, d_status);
+  CtaClock clk;
+  cta_clock_for(kClockForward, &clk.buf, &clk.cap);
+  fwd_pair_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, p, s, static_cast<__nv_bfloat16 *>(o), lse, d_status,
+                                                clk);
   return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 

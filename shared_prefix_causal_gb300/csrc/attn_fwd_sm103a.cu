@@ -92,8 +92,9 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, PlanDev plan, AttnShape s,
-                  __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, int32_t *d_status) {
+                  __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, int32_t *d_status, CtaClock clk) {
   using L = Layout<D>;
+  const unsigned long long clk0 = clk.begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic so that accesses
   // through it stay shared-memory (not generic) accesses
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  clk.end(clk0);
 }
 
 template <int D>
@@ -398,7 +400,9 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
   const unsigned grid = unsigned(p.n_pairs) * unsigned(s.Hkv);
-  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, p, s, static_cast<__nv_bfloat16 *>(o), lse, d_status);
+  CtaClock clk;
+  cta_clock_for(kClockForward, &clk.buf, &clk.cap);
+  kern<<<grid, kThreads, smem, st>>>(tq, tk, tv, p, s, static_cast<__nv_bfloat16 *>(o), lse, d_status, clk);
   return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 

@@ -44,9 +44,34 @@ bool on_plan_device(const sp_plan &p) {
   return cudaGetDevice(&dev) == cudaSuccess && dev == p.device;
 }
 
+int32_t g_clock_kernel = 0;
+unsigned long long *g_clock_buf = nullptr;
+int32_t g_clock_cap = 0;
+
 }  // namespace
 
+namespace spc {
+void cta_clock_for(int32_t kernel, unsigned long long **buf, int32_t *cap) {
+  const bool on = kernel == g_clock_kernel && g_clock_buf;
+  *buf = on ? g_clock_buf : nullptr;
+  *cap = on ? g_clock_cap : 0;
+}
+}  // namespace spc
+
 extern "C" {
+
+int sp_debug_cta_clock(int32_t kernel, void *device_buffer, int64_t max_ctas) {
+  if (kernel == 0 || !device_buffer) {
+    g_clock_kernel = 0, g_clock_buf = nullptr, g_clock_cap = 0;
+    return SP_OK;
+  }
+  if (kernel < 1 || kernel > 3 || max_ctas <= 0 || max_ctas > (int64_t(1) << 30)) return SP_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(device_buffer) & 15u) return SP_ERR_ALIGNMENT;
+  g_clock_kernel = kernel;
+  g_clock_buf = static_cast<unsigned long long *>(device_buffer);
+  g_clock_cap = int32_t(max_ctas);
+  return SP_OK;
+}
 
 int sp_tree_plan(const sp_tree_desc *tree, int32_t tile_tokens, int32_t kv_block, int32_t order, sp_plan **out) {
   if (!out) return SP_ERR_INVALID_ARG;

@@ -71,6 +71,12 @@ struct PlanDev {
   int32_t n_quads;
 };
 
+// Kernels whose CTAs can record their start and end times (sp_debug_cta_clock).
+enum ClockedKernel : int32_t { kClockForward = 1, kClockKeyBlocks = 2, kClockQueryTiles = 3 };
+struct CtaClock;
+// The record buffer for launches of `kernel` (null buffer when not enabled).
+void cta_clock_for(int32_t kernel, unsigned long long **buf, int32_t *cap);
+
 struct AttnShape {
   int32_t T, Hq, Hkv, D, G;
   float scale;
@@ -97,6 +103,11 @@ int tc_fwd_pair(const PlanDev &p, const AttnShape &s, const void *q, const void 
 int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
            bool deterministic, int32_t *d_status, void *stream, void *ev_begin = nullptr, void *ev_end = nullptr);
+// dK and dV only, 128 query rows per step (attn_bwd_kv_sm103a.cu), for the
+// deterministic backward; events as tc_bwd.
+int tc_bwd_kv(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,
+              const void *d_o, void *dk, void *dv, const float *delta, int head_chunk, int32_t *d_status,
+              void *stream, void *ev_begin, void *ev_end);
 // dQ of every query tile over its own key blocks, no atomics (attn_dq_sm103a.cu);
 // delta from the backward's preprocess.
 int tc_dq(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,

@@ -56,4 +56,29 @@ struct Ctl {
   }
 };
 
+// Per-CTA timing record for measurements of a launch's tail: when enabled (a
+// non-null buffer), thread 0 of CTA b writes {start ns, end ns, SM id, 0}
+// (global timer) to buf[4 b .. 4 b + 3] for b < cap.  Off, it costs a branch.
+struct CtaClock {
+  unsigned long long *buf = nullptr;
+  int32_t cap = 0;
+  __device__ static unsigned long long now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+  }
+  __device__ unsigned long long begin() const { return buf ? now() : 0ull; }
+  __device__ void end(unsigned long long t0) const {
+    if (buf && threadIdx.x == 0 && int64_t(blockIdx.x) < cap) {
+      uint32_t sm;
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+      unsigned long long *r = buf + 4 * size_t(blockIdx.x);
+      r[0] = t0;
+      r[1] = now();
+      r[2] = sm;
+      r[3] = 0;
+    }
+  }
+};
+
 }  // namespace spc

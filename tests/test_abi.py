@@ -471,3 +471,15 @@ def test_bench_peaks_from_the_measured_file_else_the_fallback(tmp_path, content,
     if content is not None:
         path.write_text(content if isinstance(content, str) else json.dumps(content))
     assert bench.resolve_peaks(*bench.load_peaks(str(path))) == want
+
+
+def test_bench_cta_tail_stats_by_hand():
+    """Two SMs, two CTAs each: SM 0 busy [0, 100) and [100, 150), SM 1 busy [0, 80) and [80, 120); the
+    launch spans 150; SM 1 idles 30 after its last CTA: tail idle 30 / (150 x 2), busy 270 / 300."""
+    import bench
+    rec = np.array([[0, 100, 0, 0], [0, 80, 1, 0], [100, 150, 0, 0], [80, 120, 1, 0], [0, 0, 0, 0]],
+                   dtype=np.int64)  # the last row: a CTA past the buffer records nothing
+    out = bench.cta_tail_stats(rec)
+    assert out["ctas"] == 4 and out["sms"] == 2
+    assert out["tail_idle_frac"] == pytest.approx(0.1) and out["busy_frac"] == pytest.approx(0.9)
+    assert out["longest_cta_us"] == pytest.approx(0.1) and out["last_sm_idle_us"] == pytest.approx(0.03)

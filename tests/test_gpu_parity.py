@@ -284,10 +284,10 @@ def test_deterministic_bwd_star_is_reproducible():
     _, ref = run_gpu(w, "bf16", x=x)
     for n in ("dq", "dk", "dv"):
         assert np.array_equal(out[n], out2[n]), n  # bit-identical from run to run
-    for n in ("dk", "dv"):
-        assert np.array_equal(out[n], ref[n]), n  # dK, dV: the same kernel either way
-    # dQ: the two summation orders agree to within bf16 rounding
-    assert rel_l2(out["dq"], ref["dq"]) < 5e-3
+    # the two backward paths add the same terms in other orders (dQ: per query tile against atomics;
+    # dK, dV: 128- against 64-row query steps): they agree to within bf16 rounding
+    for n in ("dq", "dk", "dv"):
+        assert rel_l2(out[n], ref[n]) < 5e-3, n
 
 
 @pytest.mark.slow
@@ -494,8 +494,8 @@ def test_gqa_and_head_dim_sweep(hq, hkv, d):
     check_full(w, x, out, "bf16")
     _, out_det = run_gpu(w, "bf16", x=x, deterministic=True)
     check_full(w, x, out_det, "bf16")
-    for n in ("dk", "dv"):
-        assert np.array_equal(out[n], out_det[n]), n
+    for n in ("dq", "dk", "dv"):
+        assert rel_l2(out_det[n], out[n]) < 5e-3, n
 
 
 def test_plan_uploaded_into_a_caller_buffer_gives_identical_results():
