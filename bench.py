@@ -464,6 +464,7 @@ def run_gpu(args):
     e2e = run_e2e(args, spc, w, x, dev, f_fwd + f_bwd) if rank == 0 and not args.no_e2e else None
     det = run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_buf, scale, status, dev, f_bwd,
                                 p_burst)
+    paired = run_paired_fwd(args, spc, plan, q, k, v, o, lse, scale, status, dev, f_fwd, p_burst)
     lm_head = run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust) \
         if gathered is not None and not args.no_lm_head else None
 
@@ -530,6 +531,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": e2e,
         "bwd_deterministic": det,
+        "fwd_paired_sm": paired,
         "fragments": fragment_summary(spc, w, args.fragment_cap),
         "lm_head": lm_head,
     }
@@ -582,6 +584,30 @@ def run_deterministic_bwd(args, spc, plan, q, k, v, o, lse, do, dq, dk, dv, ws_b
     return {"ms": round(t, 4), "useful_tflops": round(tf, 2), "frac_of_peak": round(tf / p_burst, 4) if p_burst else None,
             "key_block_kernel_ms": round(tm, 4), "query_tile_kernel_and_preprocess_ms": round(t - tm, 4),
             "launches": 3}
+
+
+def run_paired_fwd(args, spc, plan, q, k, v, o, lse, scale, status, dev, f_fwd, p_burst):
+    """The forward on pairs of SMs (cta_group::2 products), timed like the step's forward; null where it
+    does not apply (head_dim other than 128)."""
+    import torch
+    if q.shape[2] != 128:
+        return None
+    stream = torch.cuda.current_stream(dev)
+    ms = []
+    for i in range(args.warmup + args.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        spc.sp_tree_attn_fwd_paired(plan, q, k, v, o, lse, scale, status)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if i >= args.warmup:
+            ms.append(e0.elapsed_time(e1))
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} in the paired-SM forward")
+    t = statistics.median(ms)
+    tf = f_fwd / (t * 1e-3) / 1e12
+    return {"ms": round(t, 4), "useful_tflops": round(tf, 2),
+            "frac_of_peak": round(tf / p_burst, 4) if p_burst else None, "launches": 1}
 
 
 def run_lm_head(args, spc, w, gathered, idx, dev, p_burst, p_sust):
@@ -671,55 +697,80 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         ev_comp[b].record(comp)
         ev_out[b].record(comp)
     plans = []
+    marks = []  # per step: events on the streams and host times (the breakdown of the end-to-end time)
+
+    def ev():
+        e = torch.cuda.Event(enable_timing=True)
+        return e
 
     def step(i):
         d = sets[i % nbuf]
         b = i % nbuf
+        m = {"host_t0": time.perf_counter()}
         plan = spc.tree_plan(w.tree, 128 // G, 128, 0, upload=False)
+        m["host_plan_ms"] = (time.perf_counter() - m["host_t0"]) * 1e3
         need = spc.sp_plan_device_bytes(plan)
         if plan_buf[b] is None or plan_buf[b].numel() < need:
             plan_buf[b] = torch.empty(2 * need, dtype=torch.uint8, device=dev)
         # the set's buffer is free once its previous step (two back) has computed; the upload goes on an
         # idle stream of its own (a copy from pageable host memory queued behind busy work would stall)
+        t_wait = time.perf_counter()
         ev_comp[b].synchronize()
+        m["host_wait_ms"] = (time.perf_counter() - t_wait) * 1e3
+        t_up = time.perf_counter()
+        m["upload0"], m["upload1"] = ev(), ev()
+        m["upload0"].record(s_plan)
         spc.sp_plan_upload_to(plan, plan_buf[b], s_plan)
-        ev_plan = torch.cuda.Event()
-        ev_plan.record(s_plan)
-        comp.wait_event(ev_plan)
+        m["upload1"].record(s_plan)
+        m["host_upload_ms"] = (time.perf_counter() - t_up) * 1e3
+        comp.wait_event(m["upload1"])
         plans.append(plan)
         s_in.wait_event(ev_comp[b])  # the set's inputs are free once its previous step has computed
+        m["h2d0"], m["h2d1"] = ev(), ev()
+        m["h2d0"].record(s_in)
         with torch.cuda.stream(s_in):
             for n in host:
                 d[n].copy_(host[n], non_blocking=True)
             if idx_h is not None:
                 d["idx"].copy_(idx_h, non_blocking=True)
-        ev_in = torch.cuda.Event()
-        ev_in.record(s_in)
-        comp.wait_event(ev_in)
+        m["h2d1"].record(s_in)
+        comp.wait_event(m["h2d1"])
         comp.wait_event(ev_out[b])  # the set's result buffers have been copied out
+        m["comp0"], m["comp1"] = ev(), ev()
+        m["comp0"].record(comp)
         spc.sp_tree_attn_fwd(plan, d["q"], d["k"], d["v"], d["o"], d["lse"], w.softmax_scale, status)
         spc.sp_tree_attn_bwd(plan, d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"], d["dv"],
                              d["ws"], w.softmax_scale, status)
         if d["g"] is not None:
             spc.sp_edge_gather(d["hidden"], d["idx"], d["g"], status)
+        m["comp1"].record(comp)
         ev_comp[b].record(comp)
         s_out.wait_event(ev_comp[b])
+        m["d2h0"], m["d2h1"] = ev(), ev()
+        m["d2h0"].record(s_out)
         with torch.cuda.stream(s_out):
             for n in ("dq", "dk", "dv"):
                 d["out_h"][n].copy_(d[n], non_blocking=True)
             if d["g"] is not None:
                 d["g_h"].copy_(d["g"], non_blocking=True)
+        m["d2h1"].record(s_out)
         ev_out[b].record(s_out)
+        m["host_ms"] = (time.perf_counter() - m["host_t0"]) * 1e3
+        marks.append(m)
 
     for i in range(max(1, args.warmup)):
         step(i)
     torch.cuda.synchronize(dev)
     n = max(2, min(args.steps, 10))
+    marks.clear()
+    t_start = ev()
+    t_start.record(comp)
     t0 = time.perf_counter()
     for i in range(n):
         step(i)
     torch.cuda.synchronize(dev)
     el = (time.perf_counter() - t0) / n
+    breakdown = e2e_breakdown(marks, t_start, el * 1e3)
     for p_ in plans:
         p_.close()
     if status.item() != 0:
@@ -729,7 +780,31 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
             "pipelined": "2 buffer sets; inputs in on one stream, results out on another, next step's copies "
                          "overlapping this step's compute; each step's plan uploaded into a reused device buffer",
             "includes": "tree_plan + plan upload + H2D of q,k,v,dO,hidden,idx + fwd + bwd + edge_gather + "
-                        "D2H of dQ,dK,dV and gathered rows"}
+                        "D2H of dQ,dK,dV and gathered rows",
+            "breakdown": breakdown}
+
+
+def e2e_breakdown(marks, t_start, step_ms):
+    """Where the end-to-end time per step goes, from the events of the timed steps (ms, medians over steps
+    unless said): compute, the copies in and out, the plan upload and host times; the compute stream's idle
+    time between steps; and the pipeline's fill (before the first compute) and drain (after the last)."""
+    med = lambda xs: round(statistics.median(xs), 4) if xs else None  # noqa: E731
+    el = lambda a, b: a.elapsed_time(b)  # noqa: E731
+    comp = [el(m["comp0"], m["comp1"]) for m in marks]
+    gaps = [el(marks[i]["comp1"], marks[i + 1]["comp0"]) for i in range(len(marks) - 1)]
+    total = el(t_start, marks[-1]["d2h1"])
+    fill = el(t_start, marks[0]["comp0"])
+    drain = el(marks[-1]["comp1"], marks[-1]["d2h1"])
+    return {"compute_ms": med(comp), "h2d_ms": med([el(m["h2d0"], m["h2d1"]) for m in marks]),
+            "d2h_ms": med([el(m["d2h0"], m["d2h1"]) for m in marks]),
+            "upload_ms": med([el(m["upload0"], m["upload1"]) for m in marks]),
+            "compute_idle_between_steps_ms": med(gaps), "compute_idle_total_ms": round(sum(gaps), 4),
+            "fill_ms": round(fill, 4), "drain_ms": round(drain, 4), "steps": len(marks),
+            "device_span_ms": round(total, 4), "step_ms_host_clock": round(step_ms, 4),
+            "host_plan_ms": med([m["host_plan_ms"] for m in marks]),
+            "host_upload_ms": med([m["host_upload_ms"] for m in marks]),
+            "host_wait_ms": med([m["host_wait_ms"] for m in marks]),
+            "host_step_ms": med([m["host_ms"] for m in marks])}
 
 
 def cta_tail_stats(rec):

@@ -321,14 +321,16 @@ SP_API int sp_edge_logprob_bwd(int32_t dtype, const void *hidden_sel, int32_t E,
                                int32_t *d_status, void *stream);
 
 /* sp_tree_attn_bwd with a deterministic dQ: same arguments, workspace and
- * errors, same dK/dV bits.  Instead of adding every key block's dQ partial
- * into an fp32 buffer with atomics (whose order, and so rounding, varies from
- * run to run), each query tile walks its own ancestor key ranges and
- * accumulates dQ in a fixed order (the per-run gradient accumulation of
- * "[ENHANCEMENT] Shared-prefix training ...", issue #7386, "Describe the
- * solution you'd like", made reproducible).  dQ, dK and dV are identical bit
- * for bit on every call with the same inputs.  Costs three more tensor-core
- * products per (query tile, key block) than the default path. */
+ * errors.  Instead of adding every key block's dQ partial into an fp32 buffer
+ * with atomics (whose order, and so rounding, varies from run to run), each
+ * query tile walks its own ancestor key ranges and accumulates dQ in a fixed
+ * order (the per-run gradient accumulation of "[ENHANCEMENT] Shared-prefix
+ * training ...", issue #7386, "Describe the solution you'd like", made
+ * reproducible); dK and dV come from a key-block kernel that takes 128 query
+ * rows per step.  dQ, dK and dV are identical bit for bit on every call with
+ * the same inputs, and agree with sp_tree_attn_bwd's to within bf16 rounding
+ * (the same terms summed in another order).  Recomputes S and dP once more per
+ * (query tile, key block) than the default path. */
 SP_API int sp_tree_attn_bwd_deterministic(const sp_plan *plan, int32_t dtype, const void *q, const void *k,
                                           const void *v, const void *o, const float *lse, const void *d_o, void *dq,
                                           void *dk, void *dv, void *workspace, size_t workspace_bytes, int32_t T,
@@ -351,6 +353,20 @@ SP_API int sp_tree_attn_bwd_timed(const sp_plan *plan, int32_t dtype, const void
                                   void *workspace, size_t workspace_bytes, int32_t T, int32_t Hq, int32_t Hkv,
                                   int32_t D, float softmax_scale, int32_t deterministic, void *ev_main_begin,
                                   void *ev_main_end, int32_t *d_status, void *stream);
+
+/* tree_attn_fwd on pairs of SMs: the same outputs as sp_tree_attn_fwd (to
+ * within bf16 rounding of P and O, summed in the same order per tile), from
+ * tcgen05 products that span the two SMs of a cluster (cta_group::2): each
+ * M = 256 product takes 128 query rows from each SM, and each SM loads half of
+ * every K and V block.  The pages name no such kernel; it is a variant of the
+ * forward's main kernel, kept beside it because on these workloads it runs
+ * slower than the one-SM kernel (the softmax of each tile waits on products
+ * and barriers that now cross two SMs).  bf16, head_dim 128 and the tiling of
+ * sp_tree_attn_fwd only; other cases return SP_ERR_UNSUPPORTED.  Arguments,
+ * layouts and errors as sp_tree_attn_fwd. */
+SP_API int sp_tree_attn_fwd_paired(const sp_plan *plan, int32_t dtype, const void *q, const void *k, const void *v,
+                                   void *o, float *lse, int32_t T, int32_t Hq, int32_t Hkv, int32_t D,
+                                   float softmax_scale, int32_t *d_status, void *stream);
 
 /* Size of the fixed device scratch behind sp_tree_attn_bwd_noalloc (64 MiB). */
 #define SP_NOALLOC_SCRATCH_BYTES (64u << 20)

@@ -68,6 +68,8 @@ _c_plan_upload = _sig("sp_plan_upload", ctypes.c_int, [_vp, _vp])
 _c_plan_destroy = _sig("sp_plan_destroy", None, [_vp])
 _c_fwd = _sig("sp_tree_attn_fwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
+_c_fwd_paired = _sig("sp_tree_attn_fwd_paired", ctypes.c_int,
+                     [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_ws = _sig("sp_tree_attn_bwd_workspace_bytes", ctypes.c_size_t, [_i32, _i32, _i32, _i32])
 _c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
@@ -106,7 +108,7 @@ EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
             "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic", "sp_fragment_plan", "sp_fragment_view",
-            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed", "sp_debug_cta_clock")
+            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed", "sp_debug_cta_clock", "sp_tree_attn_fwd_paired")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -251,7 +253,7 @@ def _check_bwd_shapes(q, k, v, o, lse, d_o, dq, dk, dv):
     return T, Hq, Hkv, D
 
 
-def sp_tree_attn_fwd(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status=None, stream=None):
+def sp_tree_attn_fwd(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status=None, stream=None, _fn=None):
     import torch
     _need_cuda(q, k, v, o, lse, d_status)
     _need_status(d_status)
@@ -261,9 +263,16 @@ def sp_tree_attn_fwd(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status
             or tuple(lse.shape) != (Hq, T) or o.dtype != q.dtype or k.dtype != q.dtype or v.dtype != q.dtype \
             or lse.dtype != torch.float32:
         raise ValueError("shape or dtype mismatch")
+    fn, name = _fn or (_c_fwd, "sp_tree_attn_fwd")
     with _on(q):
-        _check(_c_fwd(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, D,
-                      float(softmax_scale), _ptr(d_status), _stream(stream, q.device)), "sp_tree_attn_fwd")
+        _check(fn(plan.handle, _dtype_code(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), T, Hq, Hkv, D,
+                  float(softmax_scale), _ptr(d_status), _stream(stream, q.device)), name)
+
+
+def sp_tree_attn_fwd_paired(plan: Plan, q, k, v, o, lse, softmax_scale: float, d_status=None, stream=None):
+    """sp_tree_attn_fwd on pairs of SMs (cta_group::2 products); bf16, head_dim 128."""
+    sp_tree_attn_fwd(plan, q, k, v, o, lse, softmax_scale, d_status, stream,
+                     _fn=(_c_fwd_paired, "sp_tree_attn_fwd_paired"))
 
 
 def sp_tree_attn_bwd_workspace_bytes(dtype: int, T: int, Hq: int, D: int) -> int:

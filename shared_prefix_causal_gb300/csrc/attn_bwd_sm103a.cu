@@ -65,8 +65,7 @@ enum : int {
   B_DQ_FULL = 13,
   B_DQ_FREE = 14,
   B_FINAL = 15,
-  B_KT_FULL = 16,  // without the dQ product: K copied into TMEM (4 warp arrivals)
-  B_COUNT = 17
+  B_COUNT = 16
 };
 
 template <int D>
@@ -92,15 +91,11 @@ struct Layout {
 };
 
 // TMEM columns: S^T, dP^T (fp32, 64 each), dQ^T (fp32, 64), two P^T buffers
-// (bf16 pairs, 32 each), dK and dV (fp32, D each; 256 + 2D <= 512).  Without
-// the dQ product (deterministic mode) the dQ^T columns hold K instead, as
-// bf16 pairs (lane = key row), so that S^T = K Q^T reads its A operand from
-// TMEM: shared memory then feeds only Q to that product (a third of its
-// operand bytes), which is what bounds these N = 64 products.
-constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_K = 128, T_P = 192, T_DK = 256;
+// (bf16 pairs, 32 each), dK and dV (fp32, D each; 256 + 2D <= 512)
+constexpr uint32_t T_S = 0, T_DP = 64, T_DQ = 128, T_P = 192, T_DK = 256;
 
 
-template <int D, int G, bool kDQ>
+template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, PlanDev plan,
@@ -142,7 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1) cnt = 256;  // warps 0-7, every thread
       if (i == B_DQ_FREE) cnt = 128;                                       // warps 4-7
-      if (i == B_KT_FULL) cnt = 4;                                         // warps 0-3
       mbar_init(ctl.bar(i), cnt);
     }
     *ctl.abort = 0;
@@ -237,7 +231,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dst_mn0 = smem_desc_sw128(sbase + L::PS, kQChunk, 1024);
       constexpr uint32_t kPsStep = uint32_t(L::PS_BYTES) >> 4;  // descriptor units between buffers
       bool ok = ctl.wait(B_KV_FULL, 0);
-      if (!kDQ && ok) ok = ctl.wait(B_KT_FULL, 0);
       tc_fence_after();
       for (int j = 0; ok && j <= nq; ++j) {
         if (j < nq) {
@@ -252,10 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
             const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
-            if constexpr (kDQ)
-              mma_bf16_ss(tmem + T_S, dk_kmaj + ka, dq_k + qa, id_s, kk > 0);
-            else  // K from TMEM: 16 head-dim values = 8 columns per K step
-              mma_bf16_ts(tmem + T_S, tmem + T_K + 8 * kk, dq_k + qa, id_s, kk > 0);
+            mma_bf16_ss(tmem + T_S, dk_kmaj + ka, dq_k + qa, id_s, kk > 0);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -269,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = j - 1, st = m % kStages, pb = m & 1;
           const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
           if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
-          if (kDQ && !(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
+          if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
           tc_fence_after();
           const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
           const uint32_t pso = pb * kPsStep;
@@ -283,13 +273,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBQ / 16; ++kk)
             mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
-          if constexpr (kDQ) {
-            // dQ^T = K^T dS^T   (K = 128 keys)
+          // dQ^T = K^T dS^T   (K = 128 keys)
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
-            mma_commit(ctl.bar(B_DQ_FULL));
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
+          mma_commit(ctl.bar(B_DQ_FULL));
           mma_commit(ctl.bar(B_P_FREE + pb));
           mma_commit(ctl.bar(B_Q_EMPTY + st));
         }
@@ -345,28 +333,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    if constexpr (!kDQ) {
-      // K (row r = this thread's TMEM lane) from its swizzled shared-memory
-      // tile into TMEM as bf16 pairs, once per CTA
-      if (h == 0) {
-        ok = ctl.wait_warp(B_KV_FULL, 0);
-        if (ok) {
-#pragma unroll
-          for (int c = 0; c < L::kDChunks; ++c) {
-            uint32_t u[32];
-            const uint32_t row = sbase + L::K + c * kKChunk + r * 128;
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              ld_shared_v4(row + ((x ^ (r & 7)) << 4), u[4 * x], u[4 * x + 1], u[4 * x + 2], u[4 * x + 3]);
-            tmem_st32(tmem + lane_base + T_K + 32 * c, u);
-          }
-          tmem_st_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ctl.bar(B_KT_FULL));
-        }
-      }
-    }
     for (int j = 0; ok && j < nq; ++j) {
       const int st = j % kStages;
       const int qt = q_of(j);
@@ -435,13 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ctl.bar(B_P_FULL + pb));
-      if constexpr (kDQ) {
-        if (h == 1 && j >= 1 && !(ok = dq_readout(j - 1))) break;
-      }
+      if (h == 1 && j >= 1 && !(ok = dq_readout(j - 1))) break;
     }
-    if constexpr (kDQ) {
-      if (ok && h == 1 && nq >= 1) ok = dq_readout(nq - 1);
-    }
+    if (ok && h == 1 && nq >= 1) ok = dq_readout(nq - 1);
     if (ok && ctl.wait_warp(B_FINAL, 0)) {
       tc_fence_after();
       // group 0: dK (scaled); group 1: dV
@@ -567,7 +529,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
     if (rc2) return rc2;
     return tc_dq(p, s, q, k, v, lse, d_o, dq, delta, d_status, st);
   }
-  auto kern = bwd_tc_kernel<D, G, true>;
+  auto kern = bwd_tc_kernel<D, G>;
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;

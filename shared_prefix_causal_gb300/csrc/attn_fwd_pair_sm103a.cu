@@ -106,14 +106,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int cl = blockIdx.x >> 1;
   const int g = cl / plan.n_quads;
   const int *qd = plan.quads + 6 * size_t(cl % plan.n_quads);
-  const int bbeg = qd[4], nblk = qd[5];
-  const int *qb = plan.qblk + 8 * size_t(bbeg);
+  const int rbeg = qd[4], nrun = qd[5];
+  const int *runs = plan.qblk + 8 * size_t(rbeg);  // the quad's runs of key blocks (slots a0, a1, b0, b1)
   const int G = s.G, T = s.T;
   int t4[4], q0s[4], q1s[4];
 
   // Validate the work item: both CTAs read the same entries and so take the
   // same decision (neither reaches a cluster barrier the other skips).
-  bool bad = nblk < 1 || qd[0] < 0;
+  bool bad = nrun < 1 || qd[0] < 0;
   for (int i = 0; i < 4; ++i) {
     t4[i] = qd[i];
     q0s[i] = q1s[i] = 0;
@@ -124,17 +124,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!(0 <= q0s[i] && q0s[i] < q1s[i] && q1s[i] <= T)) bad = true;
     }
   }
-  for (int n = 0; !bad && n < nblk; ++n) {
-    const int *e = qb + 8 * n;
-    bool any = false;
-    if (!(0 <= e[0] && e[0] < T)) bad = true;
-    for (int i = 0; i < 4; ++i) {
-      if (e[1 + i] == 0) continue;
-      any = true;
-      if (t4[i] < 0 || e[1 + i] <= e[0] || e[1 + i] > T) bad = true;
-    }
-    if (!any) bad = true;
-  }
+  uint32_t present = 0;
+  for (int i = 0; i < 4; ++i) present |= t4[i] >= 0 ? (1u << i) : 0u;
+  const int64_t blocks = bad ? -1 : check_runs(runs, nrun, T, present);
+  const int nblk = int(blocks);
+  if (blocks < 1 || blocks > (int64_t(1) << 30)) bad = true;
   if (bad) {
     if (threadIdx.x == 0 && leader && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
     return;
@@ -176,8 +170,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                            q0s[i]);
       }
       int n = 0;
-      for (; n < nblk; ++n) {
-        const int st = n % kStages, kb = qb[8 * n];
+      RunCursor cur(runs);
+      for (; n < nblk; ++n, cur.next()) {
+        const int st = n % kStages, kb = cur.kb();
         const uint32_t ph = (n / kStages) & 1;
         if (!ctl.wait(B_K_EMPTY + st, ph ^ 1)) break;
         if (leader) mbar_arrive_expect_tx(ctl.bar(B_K_FULL + st), 2u * L::KH);
@@ -206,7 +201,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t dq0 = smem_desc_sw128(sbase + L::Q, 16, 1024);
       const uint64_t dq1 = smem_desc_sw128(sbase + L::Q + L::QT, 16, 1024);
       uint32_t pcount[2] = {0, 0};  // P V issued per slot
-      auto used = [&](int slot, int n) { return (qb[8 * n + 1 + 2 * slot] | qb[8 * n + 2 + 2 * slot]) != 0; };
+      // whether a slot reads the block under a cursor
+      auto used = [&](int slot, const RunCursor &c) { return (c.end(2 * slot) | c.end(2 * slot + 1)) != 0; };
       // S_slot(n) = Q_slot K_n^T into the slot's S columns of both CTAs
       auto issue_s = [&](int slot, int n) {
         const uint64_t dk = smem_desc_sw128(sbase + L::K + (n % kStages) * L::KH, 16, 1024);
@@ -229,18 +225,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mma_pair_ts(tsc + 128, tsc + 8 * kk, dv + ((kk * 2048) >> 4), idesc_o, (accumulate || kk > 0));
         mma_commit_pair(ctl.bar(B_O_DONE + slot));
       };
+      RunCursor cur(runs), nxt(runs);  // blocks n and n + 1
       bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_K_FULL, 0);
       if (ok) {
         tc_fence_after();
-        if (used(0, 0)) issue_s(0, 0);
-        if (used(1, 0)) issue_s(1, 0);
+        if (used(0, cur)) issue_s(0, 0);
+        if (used(1, cur)) issue_s(1, 0);
         mma_commit_pair(ctl.bar(B_K_EMPTY));
+        if (nblk > 1) nxt.next();
       }
       for (int n = 0; ok && n < nblk; ++n) {
         const int st = n % kStages, st1 = (n + 1) % kStages;
         const bool last = n + 1 == nblk;
+        const bool ua = used(0, cur), ub = used(1, cur);
+        const bool ua1 = !last && used(0, nxt), ub1 = !last && used(1, nxt);
+        if (!last) cur.next();
+        if (n + 2 < nblk) nxt.next();
         if (!(ok = ctl.wait(B_V_FULL + st, (n / kStages) & 1))) break;
-        if (used(0, n)) {
+        if (ua) {
           if (!(ok = ctl.wait_cluster(B_P_FULL, pcount[0] & 1))) break;
           tc_fence_after();
           issue_pv(0, n, pcount[0] > 0);
@@ -249,14 +251,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // block n+1's K half: needed from here on
         if (!last && !(ok = ctl.wait(B_K_FULL + st1, ((n + 1) / kStages) & 1))) break;
         tc_fence_after();
-        if (!last && used(0, n + 1)) issue_s(0, n + 1);
-        if (used(1, n)) {
+        if (ua1) issue_s(0, n + 1);
+        if (ub) {
           if (!(ok = ctl.wait_cluster(B_P_FULL + 1, pcount[1] & 1))) break;
           tc_fence_after();
           issue_pv(1, n, pcount[1] > 0);
           ++pcount[1];
         }
-        if (!last && used(1, n + 1)) issue_s(1, n + 1);
+        if (ub1) issue_s(1, n + 1);
         if (!last) mma_commit_pair(ctl.bar(B_K_EMPTY + st1));
         mma_commit_pair(ctl.bar(B_V_EMPTY + st));
       }
@@ -280,11 +282,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     uint32_t used = 0;  // blocks this slot has processed
-    for (int n = 0; n < nblk; ++n) {
-      const int *e = qb + 8 * n;
-      if ((e[1 + 2 * slot] | e[2 + 2 * slot]) == 0) continue;  // the slot does not read this block
-      const int kb = e[0], kv1 = e[1 + ti];
-      const bool causal = (e[5] >> ti) & 1;
+    RunCursor cur(runs);
+    for (int n = 0; n < nblk; ++n, cur.next()) {
+      if ((cur.end(2 * slot) | cur.end(2 * slot + 1)) == 0) continue;  // the slot does not read this block
+      const int kb = cur.kb(), kv1 = cur.end(ti);
+      const bool causal = cur.causal(ti);
       if (!(ok = ctl.wait_warp(B_S_FULL + slot, used & 1))) break;
       tc_fence_after();
       if (kv1 == 0) {

@@ -104,23 +104,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int g = blockIdx.x / plan.n_pairs;
   const int *pr = plan.pairs + 4 * size_t(blockIdx.x % plan.n_pairs);
-  const int ta = pr[0], tb = pr[1], bbeg = pr[2], nblk = pr[3];
+  const int ta = pr[0], tb = pr[1], rbeg = pr[2], nrun = pr[3];
   const int G = s.G, T = s.T;
-  const int *pb = plan.pblk + 4 * size_t(bbeg);
-  const int *tla = plan.tiles + 5 * ta;
-  const int *tlb = tb >= 0 ? plan.tiles + 5 * tb : nullptr;
-  const int qa0 = tla[1], qa1 = tla[2];
-  const int qb0 = tlb ? tlb[1] : 0, qb1 = tlb ? tlb[2] : 0;
+  const int *runs = plan.pblk + 8 * size_t(rbeg);  // the pair's runs of key blocks (slot 0: a, 1: b)
 
   // Validate the work item (uniform over the CTA).
-  bool bad = !(0 <= ta && ta < plan.n_tiles && tb < plan.n_tiles && nblk >= 1 && 0 <= qa0 && qa0 < qa1 &&
-               qa1 <= T && (!tlb || (0 <= qb0 && qb0 < qb1 && qb1 <= T)));
-  for (int i = 0; !bad && i < nblk; ++i) {
-    const int kb = pb[4 * i], ea = pb[4 * i + 1], eb = pb[4 * i + 2];
-    if (!(0 <= kb && kb < T && ea <= T && eb <= T && (ea > kb || eb > kb) && (ea == 0 || ea > kb) &&
-          (eb == 0 || eb > kb) && (tlb || eb == 0)))
-      bad = true;
-  }
+  bool bad = !(0 <= ta && ta < plan.n_tiles && -1 <= tb && tb < plan.n_tiles && nrun >= 1);
+  const int *tla = plan.tiles + 5 * size_t(bad ? 0 : ta);
+  const int *tlb = !bad && tb >= 0 ? plan.tiles + 5 * size_t(tb) : nullptr;
+  const int qa0 = tla[1], qa1 = tla[2];
+  const int qb0 = tlb ? tlb[1] : 0, qb1 = tlb ? tlb[2] : 0;
+  bad = bad || !(0 <= qa0 && qa0 < qa1 && qa1 <= T && (!tlb || (0 <= qb0 && qb0 < qb1 && qb1 <= T)));
+  const int64_t blocks = bad ? -1 : check_runs(runs, nrun, T, tlb ? 3u : 1u);
+  const int nblk = int(blocks);
+  if (blocks < 1 || blocks > (int64_t(1) << 30)) bad = true;
   if (bad) {
     if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
     return;
@@ -154,8 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tlb) tma_load_3d(sbase + L::Q + L::KV + c * kChunk, &tm_q, ctl.bar(B_Q_FULL), c * 64, g * G, qb0);
       }
       int n = 0;
-      for (; n < nblk; ++n) {
-        const int st = n & 1, kb = pb[4 * n];
+      RunCursor cur(runs);
+      for (; n < nblk; ++n, cur.next()) {
+        const int st = n & 1, kb = cur.kb();
         const uint32_t ph = (n >> 1) & 1;
         if (!ctl.wait(B_K_EMPTY + st, ph ^ 1)) break;
         mbar_arrive_expect_tx(ctl.bar(B_K_FULL + st), L::KV);
@@ -214,18 +212,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tsc + 128, tsc + 8 * kk, dv + ((kk * 2048) >> 4), idesc_o, (accumulate || kk > 0));
         mma_commit(ctl.bar(B_O_DONE + t));
       };
+      RunCursor cur(runs), nxt(runs);  // blocks n and n + 1
       bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_K_FULL, 0);
       if (ok) {
         tc_fence_after();
-        if (pb[1]) issue_s(0, 0);
-        if (pb[2]) issue_s(1, 0);
+        if (cur.end(0)) issue_s(0, 0);
+        if (cur.end(1)) issue_s(1, 0);
         mma_commit(ctl.bar(B_K_EMPTY));
+        if (nblk > 1) nxt.next();
       }
       for (int n = 0; ok && n < nblk; ++n) {
         const int st = n & 1;
         const bool last = n + 1 == nblk;
-        const bool ua = pb[4 * n + 1] != 0, ub = pb[4 * n + 2] != 0;
-        const bool ua1 = !last && pb[4 * (n + 1) + 1] != 0, ub1 = !last && pb[4 * (n + 1) + 2] != 0;
+        const bool ua = cur.end(0) != 0, ub = cur.end(1) != 0;
+        const bool ua1 = !last && nxt.end(0) != 0, ub1 = !last && nxt.end(1) != 0;
+        if (!last) cur.next();
+        if (n + 2 < nblk) nxt.next();
         if (!(ok = ctl.wait(B_V_FULL + st, (n >> 1) & 1))) break;
         if (ua) {
           if (!(ok = ctl.wait(B_P_FULL, pcount_a & 1))) break;
@@ -265,10 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     uint32_t used = 0;  // blocks this tile has processed
-    for (int n = 0; active && n < nblk; ++n) {
-      const int kb = pb[4 * n], kv1 = pb[4 * n + 1 + t];
+    RunCursor cur(runs);
+    for (int n = 0; active && n < nblk; ++n, cur.next()) {
+      const int kb = cur.kb(), kv1 = cur.end(t);
       if (kv1 == 0) continue;
-      const bool causal = (pb[4 * n + 3] >> t) & 1;
+      const bool causal = cur.causal(t);
       if (!(ok = ctl.wait_warp(B_S_FULL + t, used & 1))) break;
       tc_fence_after();
       float sv[kBN];

@@ -239,6 +239,26 @@ int sp_tree_attn_fwd(const sp_plan *p, int32_t dtype, const void *q, const void 
   return spc::simt_fwd(plan_dev(*p), s, dtype, q, k, v, o, lse, d_status, stream);
 }
 
+int sp_tree_attn_fwd_paired(const sp_plan *p, int32_t dtype, const void *q, const void *k, const void *v, void *o,
+                            float *lse, int32_t T, int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale,
+                            int32_t *d_status, void *stream) {
+  if (!p) return SP_ERR_INVALID_ARG;
+  if (int rc = check_heads(dtype, T, Hq, Hkv, D)) return rc;
+  if (dtype != SP_BF16 || D != 128) return SP_ERR_UNSUPPORTED;
+  if (T != p->total_tokens) return SP_ERR_INVALID_ARG;
+  if (T == 0) return SP_OK;
+  if (!q || !k || !v || !o || !lse) return SP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return SP_ERR_ALIGNMENT;
+  if (!(softmax_scale > 0.f)) return SP_ERR_INVALID_ARG;
+  if (!p->d_tiles) return SP_ERR_NOT_UPLOADED;
+  if (!on_plan_device(*p)) return SP_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (int rc = check_tiling(*p, dtype, G)) return rc;
+  const spc::AttnShape s{T, Hq, Hkv, D, G, softmax_scale};
+  return spc::tc_fwd_pair(plan_dev(*p), s, q, k, v, o, lse, d_status, stream);
+}
+
 // Workspace: Delta [Hq][T] fp32, then (bf16 only) the fp32 dQ accumulator
 // [T][Hq][D] that the tensor-core backward reduces into.
 size_t sp_tree_attn_bwd_workspace_bytes(int32_t dtype, int32_t T, int32_t Hq, int32_t D) {

@@ -16,12 +16,13 @@ struct sp_plan {
   std::vector<int32_t> bwd;     // [k][5]
   // forward work items derived from the tiles (built at upload): pairs of
   // consecutive tiles and, per pair, the merged list of 128-key blocks
-  std::vector<int32_t> pairs;   // [p][4] = {tile_a, tile_b or -1, blk_begin, blk_count}
-  std::vector<int32_t> pblk;    // [b][4] = {kb, end_a or 0, end_b or 0, causal bits}
+  // runs of 128-key blocks [r][8] = {kb, nb, end[4] (0: not read), causal bits, 0}
+  std::vector<int32_t> pairs;   // [p][4] = {tile_a, tile_b or -1, run_begin, run_count}
+  std::vector<int32_t> pblk;    // runs of the pairs (slots 0, 1)
   // paired-SM forward work items (built at upload): four tiles per CTA pair
-  // and their merged key-block list (see build_quads)
-  std::vector<int32_t> quads;   // [q][6] = {a0, a1, b0, b1 (or -1), blk_begin, blk_count}
-  std::vector<int32_t> qblk;    // [b][8] = {kb, end a0, a1, b0, b1 (or 0), causal bits, 0, 0}
+  // and their merged block runs (see build_quads)
+  std::vector<int32_t> quads;   // [q][6] = {a0, a1, b0, b1 (or -1), run_begin, run_count}
+  std::vector<int32_t> qblk;    // runs of the quads (slots a0, a1, b0, b1)
   // backward key blocks in launch order (built at upload; same rows as bwd),
   // and the total and longest query-run length over them
   std::vector<int32_t> bwd_sched;  // [k][5]
@@ -54,6 +55,16 @@ void build_bwd_schedule(sp_plan &plan);
 void build_pairs(sp_plan &plan, int32_t block_keys);
 // Paired-SM forward quads and their merged block lists (see sp_plan::quads).
 void build_quads(sp_plan &plan, int32_t block_keys);
+// One range of a tile as a run of blocks kb, kb + B, ... (nb of them), all
+// ending at the range end; the tile's last range (its own segment) is causal.
+struct TileRun {
+  int32_t kb, nb, end;
+  bool causal;
+};
+// Merges up to four tiles' run lists by block start into entries of 8 int32
+// {kb, nb, end[4], causal bits, 0} appended to runs (see plan.cpp); returns
+// the number of entries.
+int32_t merge_runs(std::vector<TileRun> (&lists)[4], int32_t block_keys, std::vector<int32_t> &runs);
 
 // Device-side view of a plan passed to kernels by value.
 struct PlanDev {

@@ -56,6 +56,51 @@ struct Ctl {
   }
 };
 
+// Walks a work item's runs of 128-key blocks (entries of 8 int32: kb, count,
+// end per tile slot, causal bits, 0) one block at a time.  The caller stops
+// after the item's last block; next() never reads past the current run.
+struct RunCursor {
+  const int32_t *r;  // current run
+  int32_t i = 0;     // block within it
+  __device__ explicit RunCursor(const int32_t *first) : r(first) {}
+  __device__ int32_t kb() const { return r[0] + 128 * i; }
+  __device__ int32_t end(int slot) const { return r[2 + slot]; }
+  __device__ bool causal(int slot) const { return (r[6] >> slot) & 1; }
+  __device__ void next() {
+    if (++i == r[1]) {
+      r += 8;
+      i = 0;
+    }
+  }
+};
+
+// Checks a work item's runs against the tokens [0, T) and the slots present
+// (bit s of `present`); returns the number of blocks, or -1 if any run is
+// malformed: an empty or out-of-range run, an end below a block it covers or
+// past T, a slot read by nothing or by an absent tile.
+__device__ inline int64_t check_runs(const int32_t *runs, int32_t n_runs, int32_t T, uint32_t present) {
+  int64_t blocks = 0;
+  for (int32_t r = 0; r < n_runs; ++r) {
+    const int32_t *e = runs + 8 * size_t(r);
+    const int64_t kb = e[0], nb = e[1];
+    if (nb < 1 || kb < 0 || kb + 128 * (nb - 1) >= T) return -1;
+    const int64_t last = kb + 128 * (nb - 1);
+    bool any = false;
+    for (int s = 0; s < 4; ++s) {
+      const int64_t end = e[2 + s];
+      if (end == 0) {
+        if ((e[6] >> s) & 1) return -1;
+        continue;
+      }
+      if (!((present >> s) & 1) || end <= last || end > T) return -1;
+      any = true;
+    }
+    if (!any) return -1;
+    blocks += nb;
+  }
+  return blocks;
+}
+
 // Per-CTA timing record for measurements of a launch's tail: when enabled (a
 // non-null buffer), thread 0 of CTA b writes {start ns, end ns, SM id, 0}
 // (global timer) to buf[4 b .. 4 b + 3] for b < cap.  Off, it costs a branch.

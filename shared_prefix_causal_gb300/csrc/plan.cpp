@@ -194,53 +194,83 @@ int build_plan(const sp_tree_desc &t, int32_t tile_tokens, int32_t kv_block, int
   return SP_OK;
 }
 
+namespace {
+
+void tile_runs(const sp_plan &plan, int32_t t, int32_t block_keys, std::vector<TileRun> &out) {
+  out.clear();
+  if (t < 0) return;
+  const int32_t *tl = &plan.tiles[5 * size_t(t)];
+  for (int32_t r = 0; r < tl[4]; ++r) {
+    const int32_t a = plan.ranges[2 * size_t(tl[3] + r)], e = plan.ranges[2 * size_t(tl[3] + r) + 1];
+    out.push_back({a, int32_t((int64_t(e) - a + block_keys - 1) / block_keys), e, r + 1 == tl[4]});
+  }
+}
+
+}  // namespace
+
+// Merges the block lists of up to four tiles (absent: an empty list) by block
+// start and appends the result to `runs` as entries of 8 int32
+//   {kb, nb, end[0], end[1], end[2], end[3], causal bits, 0}:
+// nb blocks starting at kb, kb + B, ..., each read by exactly the tiles i with
+// end[i] != 0 (up to end[i]; bit i set where that is tile i's causal range).
+// Expanded block by block this is the list that merges equal block starts of
+// the tiles' lists; a run stops where another tile's next block would start
+// inside it, so tiles share an entry only where their blocks start at the
+// same key.  Returns the number of entries.
+int32_t merge_runs(std::vector<TileRun> (&lists)[4], int32_t block_keys, std::vector<int32_t> &runs) {
+  constexpr int64_t kNone = INT64_MAX;
+  size_t ri[4] = {0, 0, 0, 0};
+  int64_t bi[4] = {0, 0, 0, 0};
+  auto cur = [&](int i) -> int64_t {
+    return ri[i] < lists[i].size() ? int64_t(lists[i][ri[i]].kb) + int64_t(block_keys) * bi[i] : kNone;
+  };
+  int32_t count = 0;
+  for (;;) {
+    int64_t kb = kNone;
+    for (int i = 0; i < 4; ++i) kb = std::min(kb, cur(i));
+    if (kb == kNone) break;
+    int64_t n = kNone;
+    int32_t e[4] = {0, 0, 0, 0}, flags = 0;
+    for (int i = 0; i < 4; ++i) {
+      const int64_t c = cur(i);
+      if (c == kb) {
+        const TileRun &tr = lists[i][ri[i]];
+        n = std::min(n, int64_t(tr.nb) - bi[i]);
+        e[i] = tr.end;
+        flags |= tr.causal ? (1 << i) : 0;
+      } else if (c != kNone) {
+        n = std::min(n, (c - kb + block_keys - 1) / block_keys);  // stop before tile i's next block
+      }
+    }
+    runs.insert(runs.end(), {int32_t(kb), int32_t(n), e[0], e[1], e[2], e[3], flags, 0});
+    ++count;
+    for (int i = 0; i < 4; ++i)
+      if (e[i] != 0 && (bi[i] += n) == lists[i][ri[i]].nb) {
+        ++ri[i];
+        bi[i] = 0;
+      }
+  }
+  return count;
+}
+
 // Pairs tiles (2i, 2i+1) in schedule order -- tile k of sibling segments, or
-// neighbouring tiles of one segment -- and merges their key blocks by start:
-// a block is a 128-key window starting at kb that tile a and/or tile b reads,
-// each with its own range end and causal flag.  Shared ancestor blocks then
-// appear once, so one K/V load feeds both tiles.
+// neighbouring tiles of one segment -- and merges their key blocks by start
+// (tile a in slot 0, tile b in slot 1 of each run).  Shared ancestor blocks
+// then appear once, so one K/V load feeds both tiles; a run covers a whole
+// stretch of blocks both tiles read alike, so the table grows with the
+// number of ranges, not of key blocks.
 void build_pairs(sp_plan &plan, int32_t block_keys) {
   plan.pairs.clear();
   plan.pblk.clear();
   const int32_t nt = plan.n_tiles();
-  struct B {
-    int32_t kb, end;
-    bool causal;
-  };
-  auto blocks = [&](int32_t t, std::vector<B> &out) {
-    out.clear();
-    const int32_t *tl = &plan.tiles[5 * size_t(t)];
-    for (int32_t r = 0; r < tl[4]; ++r) {
-      const int32_t a = plan.ranges[2 * size_t(tl[3] + r)], e = plan.ranges[2 * size_t(tl[3] + r) + 1];
-      for (int32_t kb = a; kb < e; kb += block_keys) out.push_back({kb, e, r == tl[4] - 1});
-    }
-  };
-  std::vector<B> ba, bb;
+  std::vector<TileRun> lists[4];
   for (int32_t t = 0; t < nt; t += 2) {
     const int32_t tb = t + 1 < nt ? t + 1 : -1;
-    blocks(t, ba);
-    if (tb >= 0)
-      blocks(tb, bb);
-    else
-      bb.clear();
-    const int32_t begin = int32_t(plan.pblk.size() / 4);
-    size_t i = 0, j = 0;
-    while (i < ba.size() || j < bb.size()) {
-      int32_t kb, ea = 0, eb = 0, flags = 0;
-      if (j >= bb.size() || (i < ba.size() && ba[i].kb < bb[j].kb)) {
-        kb = ba[i].kb, ea = ba[i].end, flags = ba[i].causal ? 1 : 0;
-        ++i;
-      } else if (i >= ba.size() || bb[j].kb < ba[i].kb) {
-        kb = bb[j].kb, eb = bb[j].end, flags = bb[j].causal ? 2 : 0;
-        ++j;
-      } else {
-        kb = ba[i].kb, ea = ba[i].end, eb = bb[j].end;
-        flags = (ba[i].causal ? 1 : 0) | (bb[j].causal ? 2 : 0);
-        ++i, ++j;
-      }
-      plan.pblk.insert(plan.pblk.end(), {kb, ea, eb, flags});
-    }
-    plan.pairs.insert(plan.pairs.end(), {t, tb, begin, int32_t(plan.pblk.size() / 4) - begin});
+    tile_runs(plan, t, block_keys, lists[0]);
+    tile_runs(plan, tb, block_keys, lists[1]);
+    const int32_t begin = int32_t(plan.pblk.size() / 8);
+    const int32_t n = merge_runs(lists, block_keys, plan.pblk);
+    plan.pairs.insert(plan.pairs.end(), {t, tb, begin, n});
   }
 }
 
@@ -250,9 +280,8 @@ void build_pairs(sp_plan &plan, int32_t block_keys) {
 // over a pair of SMs (one tile per SM) wastes almost nothing.  Couples are
 // taken in the order their first tiles appear in the schedule (couple i of
 // sibling segments side by side) and grouped two by two into quads: couple
-// 2q in slot a, couple 2q + 1 in slot b.  A quad's merged key-block list feeds
-// all four tiles: qblk entry {kb, end[4], causal bits, 0, 0} with tile slots
-// a0, a1, b0, b1 (end 0: the tile does not read that block).
+// 2q in slot a, couple 2q + 1 in slot b.  A quad's merged block runs feed all
+// four tiles (run slots a0, a1, b0, b1).
 void build_quads(sp_plan &plan, int32_t block_keys) {
   plan.quads.clear();
   plan.qblk.clear();
@@ -280,49 +309,15 @@ void build_quads(sp_plan &plan, int32_t block_keys) {
     couples.push_back(k + 1 < count[sg] ? at[base[sg] + k + 1] : -1);
   }
   const int32_t nc = int32_t(couples.size() / 2);
-  struct B {
-    int32_t kb, end;
-    bool causal;
-  };
-  std::vector<B> lists[4];
-  // a tile's 128-key blocks in key order: each range from its start, the
-  // last range (the tile's own segment) flagged causal
-  auto tile_blocks = [&](int32_t t, std::vector<B> &out) {
-    out.clear();
-    if (t < 0) return;
-    const int32_t *tl = &plan.tiles[5 * size_t(t)];
-    const int32_t last = tl[4] - 1;
-    for (int32_t r = 0; r <= last; ++r) {
-      const int32_t a = plan.ranges[2 * size_t(tl[3] + r)], e = plan.ranges[2 * size_t(tl[3] + r) + 1];
-      for (int32_t kb = a; kb < e;) {
-        out.push_back({kb, e, r == last});
-        kb += block_keys;
-      }
-    }
-  };
+  std::vector<TileRun> lists[4];
   for (int32_t c = 0; c < nc; c += 2) {
     const int32_t tiles4[4] = {couples[2 * size_t(c)], couples[2 * size_t(c) + 1],
                                c + 1 < nc ? couples[2 * size_t(c) + 2] : -1,
                                c + 1 < nc ? couples[2 * size_t(c) + 3] : -1};
-    for (int i = 0; i < 4; ++i) tile_blocks(tiles4[i], lists[i]);
+    for (int i = 0; i < 4; ++i) tile_runs(plan, tiles4[i], block_keys, lists[i]);
     const int32_t begin = int32_t(plan.qblk.size() / 8);
-    size_t pos[4] = {0, 0, 0, 0};
-    for (;;) {
-      int32_t kb = INT32_MAX;
-      for (int i = 0; i < 4; ++i)
-        if (pos[i] < lists[i].size()) kb = std::min(kb, lists[i][pos[i]].kb);
-      if (kb == INT32_MAX) break;
-      int32_t e[4] = {0, 0, 0, 0}, flags = 0;
-      for (int i = 0; i < 4; ++i)
-        if (pos[i] < lists[i].size() && lists[i][pos[i]].kb == kb) {
-          e[i] = lists[i][pos[i]].end;
-          flags |= lists[i][pos[i]].causal ? (1 << i) : 0;
-          ++pos[i];
-        }
-      plan.qblk.insert(plan.qblk.end(), {kb, e[0], e[1], e[2], e[3], flags, 0, 0});
-    }
-    plan.quads.insert(plan.quads.end(),
-                      {tiles4[0], tiles4[1], tiles4[2], tiles4[3], begin, int32_t(plan.qblk.size() / 8) - begin});
+    const int32_t n = merge_runs(lists, block_keys, plan.qblk);
+    plan.quads.insert(plan.quads.end(), {tiles4[0], tiles4[1], tiles4[2], tiles4[3], begin, n});
   }
 }
 

@@ -41,6 +41,9 @@ class Host:
         self.lib.shim_rows.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.POINTER(ctypes.c_int32))]
         self.lib.shim_free.argtypes = [ctypes.c_void_p]
         self.lib.shim_device_tables.argtypes = [ctypes.c_void_p]
+        self.lib.shim_merge_runs.restype = ctypes.c_int32
+        self.lib.shim_merge_runs.argtypes = [ctypes.POINTER(ctypes.c_int32)] * 2 + \
+            [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
         self.lib.shim_bwd_run_sum.restype = ctypes.c_int64
         self.lib.shim_bwd_run_sum.argtypes = [ctypes.c_void_p]
         self.lib.shim_bwd_run_max.restype = ctypes.c_int32
@@ -81,10 +84,22 @@ class Host:
             return rc.value
         self.lib.shim_device_tables(h)
         names = ("tiles", "ranges", "bwd", "pairs", "pblk", "bwd_sched", "quads", "qblk")
-        out = {n: self._rows(h, i, w) for i, (n, w) in enumerate(zip(names, (5, 2, 5, 4, 4, 5, 6, 8)))}
+        out = {n: self._rows(h, i, w) for i, (n, w) in enumerate(zip(names, (5, 2, 5, 4, 8, 5, 6, 8)))}
         out["run_sum"], out["run_max"] = int(self.lib.shim_bwd_run_sum(h)), int(self.lib.shim_bwd_run_max(h))
         self.lib.shim_free(h)
         return out
+
+    def merge_runs(self, lists, block_keys):
+        """The planner's run merge on arbitrary lists: lists[i] = [(kb, nb, end, causal), ...] for slots
+        0..3; returns the entries [n][8]."""
+        flat = np.array([x for l in lists for r in l for x in r] or [0], dtype=np.int32)
+        counts = np.array([len(l) for l in lists], dtype=np.int32)
+        cap = sum(r[1] for l in lists for r in l) + 1
+        out = np.zeros(8 * cap, dtype=np.int32)
+        p32 = ctypes.POINTER(ctypes.c_int32)
+        n = self.lib.shim_merge_runs(flat.ctypes.data_as(p32), counts.ctypes.data_as(p32), block_keys,
+                                     out.ctypes.data_as(p32), cap)
+        return out[:8 * n].reshape(n, 8)
 
     def fragments(self, st, ln, par, dep, cap):
         d, keep = self._desc(st, ln, par, dep)

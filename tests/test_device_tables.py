@@ -4,10 +4,10 @@ At upload the library builds, from the canonical plan, the forward's work
 list and the backward's launch order:
   * pairs [n][4] = {tile_a, tile_b or -1, first entry, entry count}: tiles
     2i and 2i+1 of the schedule share one CTA;
-  * pblk [m][4] = {kb, end_a or 0, end_b or 0, causal bits}: the pair's
-    128-key blocks merged by start.  Tile t reads keys [kb, min(kb + 128,
-    end_t)) of an entry whose end_t is non-zero, and only keys j <= its query
-    i when bit t is set;
+  * pblk [m][8] = {kb, nb, end_a or 0, end_b or 0, 0, 0, causal bits, 0}: the
+    pair's 128-key blocks merged by start, as runs of nb blocks kb, kb + 128,
+    ...  Tile t reads keys [kb, min(kb + 128, end_t)) of a block whose end_t is
+    non-zero, and only keys j <= its query i when bit t is set;
   * bwd_sched: the backward table's rows in launch order (latest run end
     first, longest run first within a run end), with the runs' sum and maximum.
   * quads [n][6] = {a0, a1, b0, b1 (or -1), first entry, entry count}: the
@@ -15,8 +15,8 @@ list and the backward's launch order:
     consecutive tiles of one segment (offsets 2i and 2i + 1; a segment's last
     odd tile alone), couples in the order of their first tiles in the
     schedule, two per quad;
-  * qblk [m][8] = {kb, end a0, a1, b0, b1 (or 0), causal bits, 0, 0}: the
-    quad's 128-key blocks merged by start, read as the pairs' entries are.
+  * qblk [m][8] = {kb, nb, end a0, a1, b0, b1 (or 0), causal bits, 0}: the
+    quad's block runs, read as the pairs' runs are.
 These checks hold the tables to that reading, to the forward kernels' own
 validity tests, and to the canonical plan.  The tables come from the host-only
 build of the planner (no CUDA).
@@ -44,9 +44,44 @@ def _merge(ivs):
     return out
 
 
+def expand_runs(runs):
+    """Runs [r][8] = {kb, nb, end[4], causal bits, 0} as one row per 128-key block: {kb, end[4], bits}."""
+    rows = []
+    for kb, nb, e0, e1, e2, e3, bits, zero in runs.tolist():
+        assert zero == 0 and nb >= 1
+        rows += [[kb + BLOCK * i, e0, e1, e2, e3, bits] for i in range(nb)]
+    return np.array(rows, dtype=np.int64).reshape(-1, 6)
+
+
+def check_runs_as_the_kernels_do(T, runs, present):
+    """The forward kernels' own test of a work item's runs (check_runs in pipeline.cuh)."""
+    kb, nb = runs[:, 0].astype(np.int64), runs[:, 1].astype(np.int64)
+    last = kb + BLOCK * (nb - 1)
+    assert ((nb >= 1) & (kb >= 0) & (last < T)).all()
+    for s_ in range(4):
+        end = runs[:, 2 + s_].astype(np.int64)
+        bit = (runs[:, 6] >> s_) & 1
+        assert not bit[end == 0].any()
+        if not present[s_]:
+            assert (end == 0).all()
+        assert ((end == 0) | ((end > last) & (end <= T))).all()
+    assert (runs[:, 2:6] > 0).any(axis=1).all()
+
+
 def check_device_tables(T, d):
     """Raises AssertionError where the tables break the kernels' reading of them."""
-    tiles, ranges, pairs, pblk = d["tiles"], d["ranges"], d["pairs"], d["pblk"]
+    tiles, ranges, pairs = d["tiles"], d["ranges"], d["pairs"]
+    runs = d["pblk"]
+    assert runs.shape[1] == 8
+    for ta, tb, b0, cnt in pairs:
+        check_runs_as_the_kernels_do(T, runs[b0:b0 + cnt], (True, tb >= 0, False, False))
+    # the per-block reading of the runs: {kb, end_a, end_b, causal bits}
+    per_pair = [expand_runs(runs[b0:b0 + cnt]) for _, _, b0, cnt in pairs]
+    pblk = np.concatenate(per_pair)[:, [0, 1, 2, 5]] if per_pair else np.zeros((0, 4), np.int64)
+    pairs = pairs.copy()
+    if len(pairs):
+        pairs[:, 3] = [len(x) for x in per_pair]
+        pairs[:, 2] = np.r_[0, np.cumsum(pairs[:-1, 3])]
     nt = len(tiles)
     assert len(pairs) == (nt + 1) // 2
     begin = 0
@@ -115,7 +150,17 @@ def _check_entries(tiles, ranges, ent, col, t, bit):
 
 def check_quad_tables(T, d):
     """The paired-SM forward's quads and their merged block lists."""
-    tiles, ranges, quads, qblk = d["tiles"], d["ranges"], d["quads"], d["qblk"]
+    tiles, ranges, quads = d["tiles"], d["ranges"], d["quads"]
+    for a0, a1, b0, b1, e0, cnt in quads:
+        check_runs_as_the_kernels_do(T, d["qblk"][e0:e0 + cnt], (a0 >= 0, a1 >= 0, b0 >= 0, b1 >= 0))
+    # the per-block reading of the runs: {kb, end a0, a1, b0, b1, causal bits, 0, 0}
+    per_quad = [expand_runs(d["qblk"][e0:e0 + cnt]) for *_, e0, cnt in quads]
+    qblk = np.concatenate([np.c_[x, np.zeros((len(x), 2), np.int64)] for x in per_quad]) if per_quad \
+        else np.zeros((0, 8), np.int64)
+    quads = quads.copy()
+    if len(quads):
+        quads[:, 5] = [len(x) for x in per_quad]
+        quads[:, 4] = np.r_[0, np.cumsum(quads[:-1, 5])]
     nt = len(tiles)
     if nt == 0:
         assert len(quads) == 0 and len(qblk) == 0
@@ -174,6 +219,42 @@ def check_quad_tables(T, d):
             _check_entries(tiles, ranges, ent, 1 + i, t, i)
 
 
+def random_run_lists(rng, block=BLOCK):
+    """Up to four slots of sorted, disjoint ranges with arbitrary starts (aligned or not with each other)."""
+    lists = []
+    for _ in range(4):
+        if rng.random() < 0.2:
+            lists.append([])
+            continue
+        pos, runs = int(rng.integers(0, 300)), []
+        for r in range(int(rng.integers(1, 5))):
+            a = pos + int(rng.integers(0, 3)) * int(rng.choice([block, 37, 64]))
+            e = a + int(rng.integers(1, 5 * block))
+            runs.append((a, -(-(e - a) // block), e, int(r == 0)))
+            pos = e
+        lists.append(runs)
+    return lists
+
+
+def check_run_merge(host, lists, block=BLOCK):
+    """The planner's run merge, expanded block by block, equals a merge of the slots' blocks by start."""
+    got = expand_runs(host.merge_runs(lists, block)) if any(lists) else np.zeros((0, 6), np.int64)
+    want = {}
+    for i, runs in enumerate(lists):
+        for a, nb, e, causal in runs:
+            for k in range(nb):
+                row = want.setdefault(a + block * k, [a + block * k, 0, 0, 0, 0, 0])
+                row[1 + i] = e
+                row[5] |= causal << i
+    assert got.tolist() == [want[k] for k in sorted(want)]
+
+
+def test_run_merge_equals_a_block_by_block_merge(host):
+    rng = np.random.default_rng(23)
+    for _ in range(300):
+        check_run_merge(host, random_run_lists(rng))
+
+
 @pytest.fixture(scope="module")
 def host(tmp_path_factory):
     d = tmp_path_factory.mktemp("device_tables")
@@ -205,8 +286,8 @@ def test_random_tree_tables(host):
 def test_single_tile_and_empty_plans(host):
     one = W.tree_from_preorder([40], [-1])
     d = _tables(host, one, 128)
-    assert d["pairs"].tolist() == [[0, -1, 0, 1]] and d["pblk"].tolist() == [[0, 40, 0, 1]]
-    assert d["quads"].tolist() == [[0, -1, -1, -1, 0, 1]] and d["qblk"].tolist() == [[0, 40, 0, 0, 0, 1, 0, 0]]
+    assert d["pairs"].tolist() == [[0, -1, 0, 1]] and d["pblk"].tolist() == [[0, 1, 40, 0, 0, 0, 1, 0]]
+    assert d["quads"].tolist() == [[0, -1, -1, -1, 0, 1]] and d["qblk"].tolist() == [[0, 1, 40, 0, 0, 0, 1, 0]]
     check_device_tables(40, d)
     empty = host.device_tables([], [], [], [], 128, BLOCK, 0)
     assert len(empty["pairs"]) == 0 and len(empty["bwd_sched"]) == 0 and empty["run_max"] == 0
@@ -217,16 +298,17 @@ def test_the_checks_catch_broken_tables(host):
     good = _tables(host, t, 32)
     check_device_tables(t.total_tokens, good)
     breaks = [
-        lambda d: d["pblk"].__setitem__((0, 3), d["pblk"][0, 3] ^ 1),        # a causal bit flipped
-        lambda d: d["pblk"].__setitem__((0, 1), d["pblk"][0, 1] - 1),        # a block end cut short
-        lambda d: d["pairs"].__setitem__((0, 3), d["pairs"][0, 3] - 1),      # an entry dropped from a pair
+        lambda d: d["pblk"].__setitem__((0, 6), d["pblk"][0, 6] ^ 1),        # a causal bit flipped
+        lambda d: d["pblk"].__setitem__((0, 2), d["pblk"][0, 2] - 1),        # a block end cut short
+        lambda d: d["pblk"].__setitem__((0, 1), d["pblk"][0, 1] + 1),        # a run one block too long
+        lambda d: d["pairs"].__setitem__((0, 3), d["pairs"][0, 3] - 1),      # a run dropped from a pair
         lambda d: d["bwd_sched"].__setitem__(slice(None), d["bwd_sched"][::-1].copy()),  # launch order reversed
         lambda d: d.__setitem__("run_max", d["run_max"] + 1),
     ]
     breaks += [
-        lambda d: d["qblk"].__setitem__((0, 5), d["qblk"][0, 5] ^ 1),        # a quad's causal bit flipped
-        lambda d: d["qblk"].__setitem__((0, 1), d["qblk"][0, 1] - 1),        # a quad's block end cut short
-        lambda d: d["quads"].__setitem__((0, 5), d["quads"][0, 5] - 1),      # an entry dropped from a quad
+        lambda d: d["qblk"].__setitem__((0, 6), d["qblk"][0, 6] ^ 1),        # a quad's causal bit flipped
+        lambda d: d["qblk"].__setitem__((0, 2), d["qblk"][0, 2] - 1),        # a quad's block end cut short
+        lambda d: d["quads"].__setitem__((0, 5), d["quads"][0, 5] - 1),      # a run dropped from a quad
         lambda d: d["quads"].__setitem__((0, 1), d["quads"][0, 2]),          # a couple of two segments
     ]
     for brk in breaks:

@@ -546,3 +546,74 @@ def test_timed_backward_equals_the_backward_and_times_its_main_kernel():
             assert rel_l2(got[0].float().cpu().numpy(), ref[0].float().cpu().numpy()) < 5e-3
         main, whole = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
         assert 0 < main <= whole
+
+
+# ----------------------------------------------------------- paired-SM forward
+
+def _paired_forward(w, x):
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    G = w.hq // w.hkv
+    plan = spc.tree_plan(w.tree, 128 // G)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, w.T), dtype=torch.float32, device="cuda")
+    spc.sp_tree_attn_fwd_paired(plan, q, k, v, o, lse, w.softmax_scale, st)
+    o1, lse1 = spc.tree_attn_fwd(plan, q, k, v, w.softmax_scale, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return o.float().cpu().numpy(), lse.cpu().numpy(), o1.float().cpu().numpy(), lse1.cpu().numpy()
+
+
+def test_paired_forward_matches_the_oracle_and_the_one_sm_forward():
+    """The cta_group::2 forward on every GQA ratio, degenerate trees and random trees (head_dim 128)."""
+    rng = np.random.default_rng(41)
+    cases = [(W.tree_from_preorder([300], [-1]), 4, 1), (W.tree_from_preorder([1] * 40, [-1] + list(range(39))), 8, 2),
+             (W.tree_from_preorder([40, 70, 33], [-1, 0, 1]), 4, 1)]
+    cases += [(W.random_small_tree(rng, max_segments=20, max_len=300), hq, hkv)
+              for hq, hkv in ((2, 2), (4, 2), (8, 2), (8, 1))]
+    for tr, hq, hkv in cases:
+        w = W.Workload("paired", "", tr, hq, hkv, 128, 0.5, 7, None, None)
+        x = W.draw_tensors(w, "bf16")
+        o, lse, o1, lse1 = _paired_forward(w, x)
+        xs = np32(x)
+        O, L = A.tree_forward(xs["q"], xs["k"], xs["v"], tr.seg_start, tr.seg_len, tr.parent, w.softmax_scale)
+        assert rel_l2(o, O) <= TOL["bf16"]["o_rel"] and float(np.abs(o - O).max()) <= TOL["bf16"]["o_abs"]
+        assert float(np.abs(lse - L).max()) <= TOL["bf16"]["lse"]
+        # the one-SM kernel adds the same blocks in the same order per tile
+        assert rel_l2(o, o1) <= 1e-3 and float(np.abs(lse - lse1).max()) <= 1e-5
+
+
+def test_paired_forward_star_full_and_agent_sampled():
+    for name in ("star", "agent"):
+        w = W.get(name)
+        x = W.draw_tensors(w, "bf16")
+        o, lse, o1, lse1 = _paired_forward(w, x)
+        assert rel_l2(o, o1) <= 1e-3 and float(np.abs(lse - lse1).max()) <= 1e-5
+        t = w.tree
+        xs = np32(x)
+        if name == "star":
+            O, L = A.tree_forward(xs["q"], xs["k"], xs["v"], t.seg_start, t.seg_len, t.parent, w.softmax_scale,
+                                  [0, w.hkv - 1])
+            G = w.hq // w.hkv
+            hs = [h for g in (0, w.hkv - 1) for h in range(g * G, (g + 1) * G)]
+            assert rel_l2(o[:, hs], O[:, hs]) <= TOL["bf16"]["o_rel"]
+            assert float(np.abs(lse[hs] - L[hs]).max()) <= TOL["bf16"]["lse"]
+        else:  # rows of the shortest root-to-leaf path, KV head 0
+            leaf = min(OT.leaves(t.parent), key=lambda l: len(OT.path_tokens(t.seg_start, t.seg_len, t.parent, l)))
+            idx = OT.path_tokens(t.seg_start, t.seg_len, t.parent, leaf)
+            r = A.path_attention(xs["q"], xs["k"], xs["v"], w.softmax_scale, idx, 0)
+            G = w.hq // w.hkv
+            assert rel_l2(o[idx, :G], r["O"]) <= TOL["bf16"]["o_rel"]
+            assert float(np.abs(lse[:G][:, idx] - r["LSE"]).max()) <= TOL["bf16"]["lse"]
+
+
+def test_paired_forward_refuses_what_it_does_not_cover():
+    w = W.Workload("paired64", "", W.tree_from_preorder([100], [-1]), 4, 1, 64, 0.5, 7, None, None)
+    x = W.draw_tensors(w, "bf16")
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    plan = spc.tree_plan(w.tree, 32)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.hq, w.T), dtype=torch.float32, device="cuda")
+    with pytest.raises(spc.SPError) as e:
+        spc.sp_tree_attn_fwd_paired(plan, q, k, v, o, lse, w.softmax_scale)
+    assert e.value.code == -3  # SP_ERR_UNSUPPORTED: head_dim 64
