@@ -59,6 +59,7 @@ constexpr int kStages = 4;         // K/V ring depth
 constexpr int kThreads = 320;      // 8 softmax warps + producer + MMA
 constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk (Q)
 constexpr int kHalfChunk = 64 * 128;  // 64 rows x 128 bytes (this CTA's K half, per head-dim chunk)
+constexpr int kRunsInSmem = 128;  // block runs of a work item kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -83,7 +84,8 @@ struct Layout {
   static constexpr int Q = 0;                 // + slot * QT
   static constexpr int K = 2 * QT;            // + stage * KH
   static constexpr int V = K + kStages * KH;  // + stage * VH
-  static constexpr int BAR = V + kStages * VH;
+  static constexpr int RUNS = V + kStages * VH;  // the work item's block runs (kRunsInSmem x 32 bytes)
+  static constexpr int BAR = RUNS + kRunsInSmem * 32;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
   static constexpr int BYTES = ABORT + 4 + 1024;  // + alignment slack
@@ -144,10 +146,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(sbase + L::TSLOT, 512);
     tmem_relinquish_pair();
   }
+  // The work item's runs are read by every role at every block: from shared
+  // memory when they fit (they do unless a tile's ranges split into many runs)
+  const bool runs_in_smem = nrun <= kRunsInSmem;
+  if (runs_in_smem) {
+    int32_t *dst = reinterpret_cast<int32_t *>(smem + L::RUNS);
+    for (int i = threadIdx.x; i < 8 * nrun; i += kThreads) dst[i] = runs[i];
+  }
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated in both
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
+  if (runs_in_smem) runs = reinterpret_cast<const int32_t *>(smem + L::RUNS);
   auto lead_bar = [&](int i) { return mapa_shared(ctl.bar(i), 0); };
 
   if (warp == 8) {

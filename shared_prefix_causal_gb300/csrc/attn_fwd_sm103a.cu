@@ -54,6 +54,7 @@ constexpr int kBN = 128;           // keys per block
 constexpr int kStages = 2;         // K/V ring depth
 constexpr int kThreads = 320;      // 8 softmax warps + producer + MMA
 constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk
+constexpr int kRunsInSmem = 128;  // block runs of a work item kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -78,7 +79,8 @@ struct Layout {
   static constexpr int Q = 0;                   // + tile * KV
   static constexpr int K = 2 * KV;              // + stage * KV
   static constexpr int V = K + kStages * KV;
-  static constexpr int BAR = V + kStages * KV;
+  static constexpr int RUNS = V + kStages * KV;  // the work item's block runs (kRunsInSmem x 32 bytes)
+  static constexpr int BAR = RUNS + kRunsInSmem * 32;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
   static constexpr int BYTES = ABORT + 4 + 1024;  // + alignment slack
@@ -133,10 +135,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(sbase + L::TSLOT, 512);
     tmem_relinquish();
   }
+  // The work item's runs are read by every role at every block: from shared
+  // memory when they fit (they do unless a tile's ranges split into many runs)
+  const bool runs_in_smem = nrun <= kRunsInSmem;
+  if (runs_in_smem) {
+    int32_t *dst = reinterpret_cast<int32_t *>(smem + L::RUNS);
+    for (int i = threadIdx.x; i < 8 * nrun; i += kThreads) dst[i] = runs[i];
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
+  if (runs_in_smem) runs = reinterpret_cast<const int32_t *>(smem + L::RUNS);
 
   if (warp == 8) {
     // ------------------------------------------------------------ producer

@@ -28,6 +28,9 @@ def _stats(t):
     ("forest", 323402, 272, 256, 1, 32, 8, 128, None),
     ("agent", 65536, 106, 58, 8, 32, 8, 128, 3419),
     ("long", 131072, 63, 28, 12, 64, 8, 128, None),
+    ("forest_small", 40560, 34, 32, 1, 32, 8, 128, None),
+    ("agent_small", 16384, 27, 13, 8, 32, 8, 128, 876),
+    ("long_small", 16384, 16, 3, 12, 64, 8, 128, None),
 ])
 def test_documented_sizes(name, T, segments, leaves, max_depth, hq, hkv, D, edges):
     w = W.get(name)

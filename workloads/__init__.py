@@ -195,12 +195,55 @@ def long_fragment() -> Workload:
                     tree, 64, 8, 128, 0.5, 4, None, None)
 
 
+# Reduced cases of the three large workloads, same recipes at a quarter to an
+# eighth of the size: small enough for hardware-counter captures of a kernel,
+# larger than L2 in their Q/K/V/dO, so their DRAM figures still mean something.
+
+def grpo_forest_small() -> Workload:
+    """2 independent stars of the forest recipe (prompt U[512, 4096], 16 completions U[128, 2048])."""
+    rng = np.random.default_rng(2)
+    lens: list[int] = []
+    pars: list[int] = []
+    for _ in range(2):
+        root = len(lens)
+        lens.append(int(rng.integers(512, 4096 + 1)))
+        pars.append(-1)
+        for _ in range(16):
+            lens.append(int(rng.integers(128, 2048 + 1)))
+            pars.append(root)
+    tree = tree_from_preorder(lens, pars)
+    return Workload("forest_small", "GRPO forest, 2 stars: prompts U[512,4096], 16 completions U[128,2048]; "
+                    "32q/8kv, D=128", tree, 32, 8, 128, 0.5, 2, None, None)
+
+
+def agent_tree_small() -> Workload:
+    """The agent-tree recipe capped at 16,384 tokens."""
+    rng = np.random.default_rng(3)
+    tree = _random_tree(rng, lambda: _log_uniform(rng, 16, 4096), lambda: _log_uniform(rng, 16, 4096),
+                        1, 4, 8, 16384)
+    edge = np.nonzero(rng.random(tree.total_tokens) < 0.05)[0].astype(np.int32)
+    return Workload("agent_small", "agent-call tree: 16384 tokens, depth<=8, branching U{1..4}, segments "
+                    "logU[16,4096]; 32q/8kv, D=128", tree, 32, 8, 128, 0.5, 3, 4096, edge)
+
+
+def long_fragment_small() -> Workload:
+    """The long-fragment recipe scaled by 1/4 in its lengths (2K trunk, segments log-uniform in
+    [64, 2048]), capped at 16,384 tokens, so that the tree still branches."""
+    rng = np.random.default_rng(4)
+    tree = _random_tree(rng, lambda: 2048, lambda: _log_uniform(rng, 64, 2048), 1, 3, 12, 16384)
+    return Workload("long_small", "long bounded fragment: 16384 tokens, 2K trunk, depth<=12, branching U{1..3}, "
+                    "segments logU[64,2048]; 64q/8kv, D=128", tree, 64, 8, 128, 0.5, 4, None, None)
+
+
 CONFIGS: dict[str, Callable[[], Workload]] = {
     "tiny": tiny,
     "star": grpo_star,
     "forest": grpo_forest,
     "agent": agent_tree,
     "long": long_fragment,
+    "forest_small": grpo_forest_small,
+    "agent_small": agent_tree_small,
+    "long_small": long_fragment_small,
 }
 
 
