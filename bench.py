@@ -46,15 +46,30 @@ LAUNCHES_PER_STEP = {"fwd": 1, "bwd": 3, "gather": 1}
 # canonical plan they start from is fixed bit for bit by the planner's tests.
 CSRC = os.path.join(ROOT, "shared_prefix_causal_gb300", "csrc")
 TRAFFIC_SOURCES = {
-    "fwd_tc_kernel": ("attn_fwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_pairs"),
+    "fwd_tc_kernel": ("attn_fwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_pairs",
+                      "plan.cpp:tile_runs", "plan.cpp:merge_runs"),
     "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_bwd_schedule"),
 }
+# DRAM bytes (read + write) of one launch, from an ncu capture of one launch of the kernel on the
+# named workload (dram__bytes_read.sum + dram__bytes_write.sum), with the digest of the code that
+# decides that traffic; the units are query heads x useful pairs of that workload.
 MEASURED_TRAFFIC = {
-    "agent": {"fwd_tc_kernel": (813.75e6 + 510.94e6, "cb788fccbf1250a9"),
-              "bwd_tc_kernel": (16.64e9 + 8.42e9, "1c4afdf5b4242bb4")},
-    "star": {"fwd_tc_kernel": (94.39e6 + 27.93e6, "cb788fccbf1250a9"),
-             "bwd_tc_kernel": (333.02e6 + 131.47e6, "1c4afdf5b4242bb4")},
+    "star": {"units": 506117152,
+             "fwd_tc_kernel": (94215424 + 27723008, "177b62d43aadb1f6"),
+             "bwd_tc_kernel": (334935296 + 137194240, "03ec65811963b438")},
+    "agent_small": {"units": 2424419552,
+                    "fwd_tc_kernel": (202080768 + 100678912, "177b62d43aadb1f6"),
+                    "bwd_tc_kernel": (2089151744 + 990385408, "03ec65811963b438")},
+    "long_small": {"units": 8211399552,
+                   "fwd_tc_kernel": (336242432 + 233239808, "177b62d43aadb1f6"),
+                   "bwd_tc_kernel": (13751483392 + 7161786880, "03ec65811963b438")},
+    "forest_small": {"units": 3793239488,
+                     "fwd_tc_kernel": (500553984 + 303532800, "177b62d43aadb1f6"),
+                     "bwd_tc_kernel": (3346484736 + 1629801472, "03ec65811963b438")},
 }
+# Full-size workloads are not captured with more than the launch time: their traffic is the reduced
+# workload's of the same shape, scaled by the ratio of units (query heads x useful pairs).
+TRAFFIC_SCALED_FROM = {"agent": "agent_small", "long": "long_small", "forest": "forest_small"}
 
 
 # ------------------------------------------------------------------ helpers
@@ -104,12 +119,18 @@ def sources_digest(kernel: str) -> str:
     return m.hexdigest()[:16]
 
 
-def measured_traffic(config: str, kernel: str):
-    """DRAM bytes per launch from the committed capture, or None if absent or stale."""
-    entry = MEASURED_TRAFFIC.get(config, {}).get(kernel)
-    if entry is None or sources_digest(kernel) != entry[1]:
-        return None
-    return int(entry[0])
+def measured_traffic(config: str, kernel: str, units: int):
+    """(DRAM bytes per launch, how they were obtained), or (None, why) if absent or stale."""
+    src = config if config in MEASURED_TRAFFIC else TRAFFIC_SCALED_FROM.get(config)
+    entry = MEASURED_TRAFFIC.get(src, {}).get(kernel)
+    if entry is None:
+        return None, "no capture"
+    if sources_digest(kernel) != entry[1]:
+        return None, "capture predates the kernel's current code"
+    if src == config:
+        return int(entry[0]), "ncu capture of one launch on this workload"
+    scale = units / MEASURED_TRAFFIC[src]["units"]
+    return int(round(entry[0] * scale)), f"ncu capture of one launch on {src}, scaled by units x{scale:.3f}"
 
 
 def tile_efficiency(spc, plan, G: int, pairs: int) -> dict:
@@ -439,6 +460,8 @@ def run_gpu(args):
     pairs = useful_pairs(w.tree)
     f_fwd = 4.0 * D * w.hq * pairs
     f_bwd = 10.0 * D * w.hq * pairs
+    traffic_fwd = measured_traffic(args.config, "fwd_tc_kernel", w.hq * pairs)
+    traffic_bwd = measured_traffic(args.config, "bwd_tc_kernel", w.hq * pairs)
     ms_step = total_ms / args.steps
     value = job_throughput(f_fwd + f_bwd, ws, ms_step) / 1e12
     pk = resolve_peaks(*load_peaks())
@@ -512,7 +535,7 @@ def run_gpu(args):
             "peak": p_burst, "unit": "TFLOP/s",
             "frac": round(f_bwd / (mean_main * 1e-3) / 1e12 / p_burst, 4) if p_burst else None,
             "ms": round(mean_main, 4), "flops_per_launch": f_bwd,
-            "traffic": measured_traffic(args.config, "bwd_tc_kernel"), "traffic_kernel": "bwd_tc_kernel",
+            "traffic": traffic_bwd[0], "traffic_source": traffic_bwd[1], "traffic_kernel": "bwd_tc_kernel",
             "algorithmic_bytes": algo_bwd,
             "peak_source": f"bf16 burst, {src_burst} (the kernel runs {mean_main:.1f} ms at a time inside a "
                            f"{total_ms / 1e3:.2f} s timed region)",
@@ -524,7 +547,7 @@ def run_gpu(args):
             "kernel": "tree_attn_fwd", "bound": "tensor",
             "achieved": round(f_fwd / (mean_fwd * 1e-3) / 1e12, 2), "peak": p_burst, "unit": "TFLOP/s",
             "frac": round(f_fwd / (mean_fwd * 1e-3) / 1e12 / p_burst, 4) if p_burst else None,
-            "traffic": measured_traffic(args.config, "fwd_tc_kernel"), "traffic_kernel": "fwd_tc_kernel",
+            "traffic": traffic_fwd[0], "traffic_source": traffic_fwd[1], "traffic_kernel": "fwd_tc_kernel",
             "algorithmic_bytes": algo_fwd, "peak_source": f"bf16 burst, {src_burst}"},
         "gpu_launches": args.steps * sum(LAUNCHES_PER_STEP.values() if hidden is not None
                                          else [LAUNCHES_PER_STEP["fwd"], LAUNCHES_PER_STEP["bwd"]]),

@@ -225,15 +225,23 @@ def test_zero_sized_calls_are_no_ops_before_any_device_work():
 
 def test_bench_traffic_is_null_when_kernel_sources_change(monkeypatch):
     import bench
-    assert bench.measured_traffic("tiny", "bwd_tc_kernel") is None  # never captured
+    assert bench.measured_traffic("nowhere", "bwd_tc_kernel", 1)[0] is None  # never captured
     for cfg, ks in bench.MEASURED_TRAFFIC.items():
-        for k, (nbytes, digest) in ks.items():
+        assert ks["units"] > 0
+        for k, (nbytes, digest) in ((k, v) for k, v in ks.items() if k != "units"):
             assert len(digest) == 16 and nbytes > 0
-    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent", {"bwd_tc_kernel": (1.0, "0" * 16)})
-    assert bench.measured_traffic("agent", "bwd_tc_kernel") is None
-    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent",
-                        {"bwd_tc_kernel": (7.0, bench.sources_digest("bwd_tc_kernel"))})
-    assert bench.measured_traffic("agent", "bwd_tc_kernel") == 7
+    # every bench workload but the tiny tree has a capture of its own or of a reduced twin
+    for cfg in W.CONFIGS:
+        assert cfg == "tiny" or cfg in bench.MEASURED_TRAFFIC or bench.TRAFFIC_SCALED_FROM[cfg] in bench.MEASURED_TRAFFIC
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent_small",
+                        {"units": 10, "bwd_tc_kernel": (1.0, "0" * 16)})
+    assert bench.measured_traffic("agent_small", "bwd_tc_kernel", 10)[0] is None
+    assert bench.measured_traffic("agent", "bwd_tc_kernel", 30)[0] is None
+    monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent_small",
+                        {"units": 10, "bwd_tc_kernel": (7.0, bench.sources_digest("bwd_tc_kernel"))})
+    assert bench.measured_traffic("agent_small", "bwd_tc_kernel", 10)[0] == 7
+    nbytes, how = bench.measured_traffic("agent", "bwd_tc_kernel", 30)
+    assert nbytes == 21 and "agent_small" in how and "x3.000" in how
 
 
 # ------------------------------------------------------------ bounded fragments
