@@ -54,6 +54,9 @@ TRAFFIC_SOURCES = {
 # named workload (dram__bytes_read.sum + dram__bytes_write.sum), with the digest of the code that
 # decides that traffic; the units are query heads x useful pairs of that workload.
 MEASURED_TRAFFIC = {
+    "tiny": {"units": 26252,
+             "fwd_tc_kernel": (198400 + 0, "177b62d43aadb1f6"),
+             "bwd_tc_kernel": (352768 + 0, "03ec65811963b438")},
     "star": {"units": 506117152,
              "fwd_tc_kernel": (94215424 + 27723008, "177b62d43aadb1f6"),
              "bwd_tc_kernel": (334935296 + 137194240, "03ec65811963b438")},
@@ -684,15 +687,17 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
     """Same metric through the public API from pinned host buffers.  Every step
     plans the tree and uploads the plan, copies that step's inputs in, runs
     forward, backward and the gather, and copies dQ, dK, dV and the gathered
-    rows out.  Steps are pipelined the way a training loop would run them: two
+    rows out.  Steps are pipelined the way a training loop would run them: three
     device buffer sets, inputs copied on one stream and results on another
-    while the previous step computes (the copies of a step still precede and
-    follow its own compute)."""
+    while the previous steps compute (the copies of a step still precede and
+    follow its own compute).  A step's inputs start copying in as soon as the
+    step three back has computed, so a copy that runs late (the host-device link
+    is shared by both directions) still has two steps of compute to hide behind."""
     import torch
     G = w.hq // w.hkv
     host = {n: t.pin_memory() for n, t in x.items()}
     idx_h = torch.from_numpy(w.edge_idx).pin_memory() if w.edge_idx is not None else None
-    nbuf = 2
+    nbuf = 3
     sets = []
     for _ in range(nbuf):
         d = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
@@ -712,7 +717,23 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         (sets[0]["g_h"].numel() * 2 if sets[0]["g_h"] is not None else 0)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     comp = torch.cuda.current_stream(dev)
-    s_in, s_out, s_plan = (torch.cuda.Stream(device=dev) for _ in range(3))
+    s_plan = torch.cuda.Stream(device=dev)
+    # copies in on three streams and out on two, so several copy engines share the link: the tensors of
+    # each direction are dealt to the streams largest first, each to the stream with the fewest bytes so far
+    s_in = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    s_out = [torch.cuda.Stream(device=dev) for _ in range(2)]
+
+    def deal(names, nbytes, k):
+        lanes, load = [[] for _ in range(k)], [0] * k
+        for n in sorted(names, key=lambda n_: -nbytes[n_]):
+            i = load.index(min(load))
+            lanes[i].append(n)
+            load[i] += nbytes[n]
+        return lanes
+    in_bytes = {n: t.numel() * t.element_size() for n, t in host.items()}
+    if idx_h is not None:
+        in_bytes["idx"] = idx_h.numel() * idx_h.element_size()
+    in_lanes = deal(list(in_bytes), in_bytes, len(s_in))
     plan_buf = [None] * nbuf  # per buffer set: the device buffer its steps' plans are uploaded into
     ev_comp = [torch.cuda.Event() for _ in range(nbuf)]   # compute of the set's last step done
     ev_out = [torch.cuda.Event() for _ in range(nbuf)]    # results of the set's last step copied out
@@ -735,7 +756,7 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         need = spc.sp_plan_device_bytes(plan)
         if plan_buf[b] is None or plan_buf[b].numel() < need:
             plan_buf[b] = torch.empty(2 * need, dtype=torch.uint8, device=dev)
-        # the set's buffer is free once its previous step (two back) has computed; the upload goes on an
+        # the set's buffer is free once its previous step (three back) has computed; the upload goes on an
         # idle stream of its own (a copy from pageable host memory queued behind busy work would stall)
         t_wait = time.perf_counter()
         ev_comp[b].synchronize()
@@ -748,15 +769,20 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         m["host_upload_ms"] = (time.perf_counter() - t_up) * 1e3
         comp.wait_event(m["upload1"])
         plans.append(plan)
-        s_in.wait_event(ev_comp[b])  # the set's inputs are free once its previous step has computed
         m["h2d0"], m["h2d1"] = ev(), ev()
-        m["h2d0"].record(s_in)
-        with torch.cuda.stream(s_in):
-            for n in host:
-                d[n].copy_(host[n], non_blocking=True)
-            if idx_h is not None:
-                d["idx"].copy_(idx_h, non_blocking=True)
-        m["h2d1"].record(s_in)
+        s_in[0].wait_event(ev_comp[b])  # the set's inputs are free once its previous step has computed
+        m["h2d0"].record(s_in[0])
+        for si, lane_names in zip(s_in, in_lanes):
+            if si is not s_in[0]:
+                si.wait_event(m["h2d0"])
+            with torch.cuda.stream(si):
+                for n in lane_names:
+                    d[n].copy_(idx_h if n == "idx" else host[n], non_blocking=True)
+        for si in s_in[1:]:
+            e_ = torch.cuda.Event()
+            e_.record(si)
+            s_in[0].wait_event(e_)
+        m["h2d1"].record(s_in[0])
         comp.wait_event(m["h2d1"])
         comp.wait_event(ev_out[b])  # the set's result buffers have been copied out
         m["comp0"], m["comp1"] = ev(), ev()
@@ -768,23 +794,30 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
             spc.sp_edge_gather(d["hidden"], d["idx"], d["g"], status)
         m["comp1"].record(comp)
         ev_comp[b].record(comp)
-        s_out.wait_event(ev_comp[b])
         m["d2h0"], m["d2h1"] = ev(), ev()
-        m["d2h0"].record(s_out)
-        with torch.cuda.stream(s_out):
-            for n in ("dq", "dk", "dv"):
-                d["out_h"][n].copy_(d[n], non_blocking=True)
-            if d["g"] is not None:
-                d["g_h"].copy_(d["g"], non_blocking=True)
-        m["d2h1"].record(s_out)
-        ev_out[b].record(s_out)
+        s_out[0].wait_event(ev_comp[b])
+        m["d2h0"].record(s_out[0])
+        outs = [(d["out_h"][n], d[n]) for n in ("dq", "dk", "dv")] + \
+            ([(d["g_h"], d["g"])] if d["g"] is not None else [])
+        out_bytes = {i: src.numel() * src.element_size() for i, (_, src) in enumerate(outs)}
+        for so, lane_ids in zip(s_out, deal(list(out_bytes), out_bytes, len(s_out))):
+            so.wait_event(m["d2h0"])
+            with torch.cuda.stream(so):
+                for i in lane_ids:
+                    outs[i][0].copy_(outs[i][1], non_blocking=True)
+        for so in s_out[1:]:
+            e_ = torch.cuda.Event()
+            e_.record(so)
+            s_out[0].wait_event(e_)
+        m["d2h1"].record(s_out[0])
+        ev_out[b].record(s_out[0])
         m["host_ms"] = (time.perf_counter() - m["host_t0"]) * 1e3
         marks.append(m)
 
     for i in range(max(1, args.warmup)):
         step(i)
     torch.cuda.synchronize(dev)
-    n = max(2, min(args.steps, 10))
+    n = max(2, min(args.steps, 20))
     marks.clear()
     t_start = ev()
     t_start.record(comp)
@@ -800,7 +833,7 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         raise RuntimeError(f"device status {status.item()} in the end-to-end run")
     return {"value": round(flops_per_step / el / 1e12, 3), "unit": UNIT, "ms_per_step": round(el * 1e3, 3),
             "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipelined": "2 buffer sets; inputs in on one stream, results out on another, next step's copies "
+            "pipelined": "3 buffer sets; inputs in on three streams, results out on two, the next steps' copies "
                          "overlapping this step's compute; each step's plan uploaded into a reused device buffer",
             "includes": "tree_plan + plan upload + H2D of q,k,v,dO,hidden,idx + fwd + bwd + edge_gather + "
                         "D2H of dQ,dK,dV and gathered rows",
@@ -822,6 +855,9 @@ def e2e_breakdown(marks, t_start, step_ms):
             "d2h_ms": med([el(m["d2h0"], m["d2h1"]) for m in marks]),
             "upload_ms": med([el(m["upload0"], m["upload1"]) for m in marks]),
             "compute_idle_between_steps_ms": med(gaps), "compute_idle_total_ms": round(sum(gaps), 4),
+            "compute_idle_max_ms": round(max(gaps), 4) if gaps else None,
+            "compute_gaps_ms": [round(x, 3) for x in gaps],
+            "h2d_max_ms": round(max(el(m["h2d0"], m["h2d1"]) for m in marks), 4),
             "fill_ms": round(fill, 4), "drain_ms": round(drain, 4), "steps": len(marks),
             "device_span_ms": round(total, 4), "step_ms_host_clock": round(step_ms, 4),
             "host_plan_ms": med([m["host_plan_ms"] for m in marks]),

@@ -65,6 +65,7 @@ typedef enum {
 #define SP_DEV_INDEX_RANGE 1 /* edge_gather met an index outside [0, T); that row is zero-filled */
 #define SP_DEV_TIMEOUT 2     /* a pipeline wait in an attention kernel exceeded its spin limit */
 #define SP_DEV_BAD_PLAN 4    /* a plan entry points outside [0, T); the work item was skipped */
+#define SP_DEV_SMEM_LAYOUT 8 /* a CTA's shared memory did not start where its layout needs; it ran nothing */
 
 typedef enum { SP_BF16 = 0, SP_F32 = 1 } sp_dtype;
 
@@ -330,7 +331,10 @@ SP_API int sp_edge_logprob_bwd(int32_t dtype, const void *hidden_sel, int32_t E,
  * rows per step.  dQ, dK and dV are identical bit for bit on every call with
  * the same inputs, and agree with sp_tree_attn_bwd's to within bf16 rounding
  * (the same terms summed in another order).  Recomputes S and dP once more per
- * (query tile, key block) than the default path. */
+ * (query tile, key block) than the default path.  Besides sp_tree_attn_bwd's
+ * device codes it may set SP_DEV_SMEM_LAYOUT (the key-block kernel found its
+ * shared memory not 1024-byte aligned and ran nothing; dK and dV are then not
+ * written). */
 SP_API int sp_tree_attn_bwd_deterministic(const sp_plan *plan, int32_t dtype, const void *q, const void *k,
                                           const void *v, const void *o, const float *lse, const void *d_o, void *dq,
                                           void *dk, void *dv, void *workspace, size_t workspace_bytes, int32_t T,

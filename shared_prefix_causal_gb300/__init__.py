@@ -26,6 +26,7 @@ SP_F32 = 1
 SP_DEV_INDEX_RANGE = 1
 SP_DEV_TIMEOUT = 2
 SP_DEV_BAD_PLAN = 4
+SP_DEV_SMEM_LAYOUT = 8
 SP_ERR_CAP = -10
 
 if not os.path.exists(LIB_PATH):

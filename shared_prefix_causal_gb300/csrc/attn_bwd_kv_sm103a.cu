@@ -35,6 +35,10 @@
 // the other still has to read); warp 8: TMA producer (Q and dO tiles, and each
 // step's per-column -LSE and -Delta staged by the whole warp); warp 9: the
 // single-thread MMA issuer.  Epilogue: warpgroup 0 stores dK, 1 stores dV.
+// Q and dO travel in rings of their own (three and two stages): Q(j) is read
+// by S^T(j), the first product of a step, and last by dK(j); dO(j) by dP^T(j)
+// and dV(j).  The third Q stage lets Q(j+1) be fetched a whole step before
+// S^T(j+1) needs it, which two stages shared by both tiles could not.
 // Every mbarrier wait is bounded (Ctl); on expiry the CTA records
 // SP_DEV_TIMEOUT, stops issuing, drains, frees TMEM and returns.
 #include <cuda.h>
@@ -55,37 +59,51 @@ constexpr int kBK = 128;            // keys per CTA
 constexpr int kBQ = 128;            // query rows per step
 constexpr int kThreads = 320;       // 8 elementwise warps, producer, MMA
 constexpr int kChunk = 128 * 128;   // 128 rows x 128 bytes
-constexpr int kStages = 2;          // Q/dO ring depth
+constexpr int kQStages = 3;         // Q ring depth
+constexpr int kOStages = 2;         // dO ring depth
+constexpr int kStatSlots = 2;       // per-step -LSE / -Delta slots
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int {
   B_KV_FULL = 0,
-  B_Q_FULL = 1,    // +stage
-  B_Q_EMPTY = 3,   // +stage
-  B_S_FULL = 5,
-  B_DP_FULL = 6,
-  B_P_FULL = 7,    // +half (2), 8 warp arrivals each
-  B_DS_FULL = 9,   // 8 warp arrivals
-  B_FINAL = 10,
-  B_COUNT = 11
+  B_Q_FULL = 1,     // +stage (3)
+  B_Q_EMPTY = 4,    // +stage
+  B_O_FULL = 7,     // +stage (2)
+  B_O_EMPTY = 9,    // +stage
+  B_ST_FULL = 11,   // +slot (2)
+  B_ST_EMPTY = 13,  // +slot, 8 warp arrivals
+  B_S_FULL = 15,
+  B_DP_FULL = 16,
+  B_P_FULL = 17,    // +half (2), 8 warp arrivals each
+  B_DS_FULL = 19,   // 8 warp arrivals
+  B_FINAL = 20,
+  B_COUNT = 21
 };
 
+// Shared memory: a small region (barriers, TMEM address, abort flag, the
+// per-step statistics) first, then the 1024-byte aligned tiles.  At D = 128
+// the tiles take 224 KB, so the whole fits the 227 KB a CTA may have only
+// when the small region and its padding stay within 3 KB: the kernel checks
+// that against the address it was given and reports SP_DEV_SMEM_LAYOUT instead
+// of running if not.
 template <int D>
 struct Layout {
   static constexpr int kDChunks = D / 64;
   static constexpr int TILE = kDChunks * kChunk;  // 128 rows x D
-  static constexpr int K = 0;
-  static constexpr int V = TILE;
-  static constexpr int STAGE = 2 * TILE;
-  static constexpr int Q_OFF = 0;           // within a stage
-  static constexpr int DO_OFF = TILE;
-  static constexpr int STAT_OFF = 2 * TILE;  // -lse2[128], -delta[128]
-  static constexpr int STAGE_BYTES = STAT_OFF + 1024;
-  static constexpr int BAR = STAGE + kStages * STAGE_BYTES;
+  static constexpr int BAR = 0;
   static constexpr int TSLOT = BAR + 8 * B_COUNT;
   static constexpr int ABORT = TSLOT + 4;
-  static constexpr int BYTES = ABORT + 4 + 1024;
-  static constexpr int ALLOC = BYTES > 120 * 1024 ? BYTES : 120 * 1024;
+  static constexpr int STAT = (ABORT + 4 + 15) & ~15;  // slot x (-lse2[128], -delta[128])
+  static constexpr int MISC = STAT + kStatSlots * 2 * 128 * 4;
+  // tile offsets from the aligned tile base
+  static constexpr int K = 0;
+  static constexpr int V = TILE;
+  static constexpr int Q = 2 * TILE;               // + stage * TILE
+  static constexpr int DO = Q + kQStages * TILE;   // + stage * TILE
+  static constexpr int TILES = DO + kOStages * TILE;
+  static constexpr int WANT = ((MISC + 1023) & ~1023) + TILES;
+  static constexpr int ALLOC = WANT > 120 * 1024 ? WANT : 120 * 1024;
+  static_assert(ALLOC <= 227 * 1024, "shared memory");
 };
 
 // TMEM columns: S^T [0, 128) (then P^T), dP^T [128, 256) (then dS^T), dK, dV.
@@ -101,8 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<D>;
   const unsigned long long clk0 = clk.begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t *smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
+  // tiles at the first 1024-byte boundary after the small region
+  const uint32_t tbase = (sbase + L::MISC + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // key blocks in launch order, head_chunk KV heads at a time (as the
@@ -118,6 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_BAD_PLAN);
     return;
   }
+  if (tbase - sbase + L::TILES > uint32_t(L::ALLOC)) {
+    if (threadIdx.x == 0 && d_status) atomicOr(d_status, SP_DEV_SMEM_LAYOUT);
+    return;
+  }
   constexpr int tps = kBQ / G;  // query tokens per step
   const int nq = (qe - qb + tps - 1) / tps;
   auto q_of = [&](int jj) { return qb + (nq - 1 - jj) * tps; };  // walked from the run's end
@@ -125,7 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status, kSpinLimit};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(ctl.bar(i), (i == B_P_FULL || i == B_P_FULL + 1 || i == B_DS_FULL) ? 8u : 1u);
+      mbar_init(ctl.bar(i), (i == B_P_FULL || i == B_P_FULL + 1 || i == B_DS_FULL || i == B_ST_EMPTY ||
+                             i == B_ST_EMPTY + 1) ? 8u : 1u);
     *ctl.abort = 0;
     fence_mbar_init();
   }
@@ -148,8 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(ctl.bar(B_KV_FULL), 2u * L::TILE);
 #pragma unroll
       for (int c = 0; c < L::kDChunks; ++c) {
-        tma_load_3d(sbase + L::K + c * kChunk, &tm_k, ctl.bar(B_KV_FULL), c * 64, g, k0);
-        tma_load_3d(sbase + L::V + c * kChunk, &tm_v, ctl.bar(B_KV_FULL), c * 64, g, k0);
+        tma_load_3d(tbase + L::K + c * kChunk, &tm_k, ctl.bar(B_KV_FULL), c * 64, g, k0);
+        tma_load_3d(tbase + L::V + c * kChunk, &tm_v, ctl.bar(B_KV_FULL), c * 64, g, k0);
       }
     }
     // -LSE (log2) and -Delta of a step's 128 columns, loaded one step ahead
@@ -166,42 +191,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     load_stats(0);
-    int j = 0;
-    for (; j < nq; ++j) {
-      const int st = j % kStages;
-      if (!ctl.wait_warp(B_Q_EMPTY + st, ((j / kStages) & 1) ^ 1)) break;
+    int nqi = 0, noi = 0;  // Q and dO tiles issued
+    for (int j = 0; j < nq; ++j) {
+      const int qs = j % kQStages, os = j % kOStages, ss = j % kStatSlots;
       const int qt = q_of(j);
-      const uint32_t stage = L::STAGE + st * L::STAGE_BYTES;
+      // Q(j) once S^T(j - 3) and dK(j - 3) have read its stage
+      if (!ctl.wait_warp(B_Q_EMPTY + qs, ((j / kQStages) & 1) ^ 1)) break;
       if (lane == 0) {
-        mbar_expect_tx(ctl.bar(B_Q_FULL + st), 2u * L::TILE);
+        mbar_arrive_expect_tx(ctl.bar(B_Q_FULL + qs), L::TILE);
 #pragma unroll
-        for (int c = 0; c < L::kDChunks; ++c) {
-          tma_load_3d(sbase + stage + L::Q_OFF + c * kChunk, &tm_q, ctl.bar(B_Q_FULL + st), c * 64, g * G, qt);
-          tma_load_3d(sbase + stage + L::DO_OFF + c * kChunk, &tm_do, ctl.bar(B_Q_FULL + st), c * 64, g * G, qt);
-        }
+        for (int c = 0; c < L::kDChunks; ++c)
+          tma_load_3d(tbase + L::Q + qs * L::TILE + c * kChunk, &tm_q, ctl.bar(B_Q_FULL + qs), c * 64, g * G, qt);
       }
-      float *stat = reinterpret_cast<float *>(smem + stage + L::STAT_OFF);
+      ++nqi;
+      // dO(j) once dP^T(j - 2) and dV(j - 2) have read its stage
+      if (!ctl.wait_warp(B_O_EMPTY + os, ((j / kOStages) & 1) ^ 1)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(ctl.bar(B_O_FULL + os), L::TILE);
+#pragma unroll
+        for (int c = 0; c < L::kDChunks; ++c)
+          tma_load_3d(tbase + L::DO + os * L::TILE + c * kChunk, &tm_do, ctl.bar(B_O_FULL + os), c * 64, g * G, qt);
+      }
+      ++noi;
+      // the step's statistics once the elementwise warps are done with step j - 2
+      if (!ctl.wait_warp(B_ST_EMPTY + ss, ((j / kStatSlots) & 1) ^ 1)) break;
+      float *stat = reinterpret_cast<float *>(smem + L::STAT + ss * 2 * 128 * 4);
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
         stat[lane + 32 * x] = -nl[x];
         stat[kBQ + lane + 32 * x] = -nd[x];
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(ctl.bar(B_Q_FULL + st));
+      if (lane == 0) mbar_arrive(ctl.bar(B_ST_FULL + ss));
       load_stats(j + 1);
     }
     if (lane == 0 && *ctl.abort) {
       ctl.drain(B_KV_FULL, 0);
-      for (int m = j - kStages < 0 ? 0 : j - kStages; m < j; ++m) ctl.drain(B_Q_FULL + m % kStages, (m / kStages) & 1);
+      for (int m = nqi - kQStages < 0 ? 0 : nqi - kQStages; m < nqi; ++m)
+        ctl.drain(B_Q_FULL + m % kQStages, (m / kQStages) & 1);
+      for (int m = noi - kOStages < 0 ? 0 : noi - kOStages; m < noi; ++m)
+        ctl.drain(B_O_FULL + m % kOStages, (m / kOStages) & 1);
     }
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kBK, kBQ, 0, 0);  // S^T, dP^T
       constexpr uint32_t id_kv = idesc_bf16_f32(kBK, D, 0, 1);   // dV, dK (B MN-major)
-      const uint64_t dk_kmaj = smem_desc_sw128(sbase + L::K, 16, 1024);
-      const uint64_t dv_kmaj = smem_desc_sw128(sbase + L::V, 16, 1024);
-      auto stage_of = [&](int jj) { return sbase + L::STAGE + (jj % kStages) * L::STAGE_BYTES; };
+      const uint64_t dk_kmaj = smem_desc_sw128(tbase + L::K, 16, 1024);
+      const uint64_t dv_kmaj = smem_desc_sw128(tbase + L::V, 16, 1024);
+      auto q_tile = [&](int jj) { return tbase + L::Q + (jj % kQStages) * L::TILE; };
+      auto o_tile = [&](int jj) { return tbase + L::DO + (jj % kOStages) * L::TILE; };
       // S^T(j) = K Q^T or dP^T(j) = V dO^T, K = D
       auto issue_scores = [&](uint32_t dcol, uint64_t a, uint32_t b_addr) {
         const uint64_t b = smem_desc_sw128(b_addr, 16, 1024);
@@ -235,32 +274,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = ctl.wait(B_KV_FULL, 0) && ctl.wait(B_Q_FULL, 0);
       if (ok) {
         tc_fence_after();
-        issue_scores(T_S, dk_kmaj, stage_of(0) + L::Q_OFF);
+        issue_scores(T_S, dk_kmaj, q_tile(0));
         mma_commit(ctl.bar(B_S_FULL));
-        issue_scores(T_DP, dv_kmaj, stage_of(0) + L::DO_OFF);
+      }
+      if (ok && (ok = ctl.wait(B_O_FULL, 0))) {
+        tc_fence_after();
+        issue_scores(T_DP, dv_kmaj, o_tile(0));
         mma_commit(ctl.bar(B_DP_FULL));
       }
       for (int j = 0; ok && j < nq; ++j) {
-        const int st = j % kStages;
         // dV += P^T dO, each half of the query rows as soon as its P^T is in TMEM
         if (!(ok = ctl.wait(B_P_FULL, j & 1))) break;
         tc_fence_after();
-        issue_grad_half(T_DK + D, T_S, stage_of(j) + L::DO_OFF, 0, j > 0);
+        issue_grad_half(T_DK + D, T_S, o_tile(j), 0, j > 0);
         if (!(ok = ctl.wait(B_P_FULL + 1, j & 1))) break;
         tc_fence_after();
-        issue_grad_half(T_DK + D, T_S, stage_of(j) + L::DO_OFF, 1, true);
+        issue_grad_half(T_DK + D, T_S, o_tile(j), 1, true);
+        mma_commit(ctl.bar(B_O_EMPTY + j % kOStages));  // dO(j): dP^T(j) and dV(j) done
         if (j + 1 < nq) {
-          if (!(ok = ctl.wait(B_Q_FULL + (j + 1) % kStages, ((j + 1) / kStages) & 1))) break;
+          if (!(ok = ctl.wait(B_Q_FULL + (j + 1) % kQStages, ((j + 1) / kQStages) & 1))) break;
           tc_fence_after();
-          issue_scores(T_S, dk_kmaj, stage_of(j + 1) + L::Q_OFF);  // after dV(j) read P^T(j)
+          issue_scores(T_S, dk_kmaj, q_tile(j + 1));  // after dV(j) read P^T(j)
           mma_commit(ctl.bar(B_S_FULL));
         }
         if (!(ok = ctl.wait(B_DS_FULL, j & 1))) break;
         tc_fence_after();
-        issue_grad(T_DK, T_DP, stage_of(j) + L::Q_OFF, j > 0);  // dK += dS^T Q
-        mma_commit(ctl.bar(B_Q_EMPTY + st));
+        issue_grad(T_DK, T_DP, q_tile(j), j > 0);  // dK += dS^T Q
+        mma_commit(ctl.bar(B_Q_EMPTY + j % kQStages));
         if (j + 1 < nq) {
-          issue_scores(T_DP, dv_kmaj, stage_of(j + 1) + L::DO_OFF);  // after dK(j) read dS^T(j)
+          if (!(ok = ctl.wait(B_O_FULL + (j + 1) % kOStages, ((j + 1) / kOStages) & 1))) break;
+          tc_fence_after();
+          issue_scores(T_DP, dv_kmaj, o_tile(j + 1));  // after dK(j) read dS^T(j)
           mma_commit(ctl.bar(B_DP_FULL));
         }
       }
@@ -277,13 +321,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = s.scale * kLog2e;
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
-      const int st = j % kStages;
+      const int ss = j % kStatSlots;
       const int qt = q_of(j);
-      const float *stat = reinterpret_cast<const float *>(smem + L::STAGE + st * L::STAGE_BYTES + L::STAT_OFF);
+      const float *stat = reinterpret_cast<const float *>(smem + L::STAT + ss * 2 * 128 * 4);
       const bool nomask = qt + tps <= qe && qt >= k1 - 1;
       const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
       const int ql = qe - qt;
-      if (!(ok = ctl.wait_warp(B_Q_FULL + st, (j / kStages) & 1))) break;  // the step's statistics
+      if (!(ok = ctl.wait_warp(B_ST_FULL + ss, (j / kStatSlots) & 1))) break;  // the step's statistics
       if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
       tc_fence_after();
       // phase A: P^T of this group's 64 columns in two halves of 32, each
@@ -356,7 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ctl.bar(B_DS_FULL));
+      if (lane == 0) {
+        mbar_arrive(ctl.bar(B_DS_FULL));
+        mbar_arrive(ctl.bar(B_ST_EMPTY + ss));  // this step's statistics are read
+      }
     }
     if (ok && ctl.wait_warp(B_FINAL, 0)) {
       tc_fence_after();

@@ -20,9 +20,10 @@
 // tcgen05 MMA issuer.  Per key block
 // n the MMA thread issues S = Q K^T and dP = dO V^T (SS), and, once the
 // elementwise warps have stored dS(n) as bf16 pairs in TMEM, dQ += dS(n) K(n)
-// (A read from TMEM, K as an MN-major B).  S(n+1) and dP(n+1) are issued as
-// soon as S(n) and dP(n) have been read, so they run while dS(n) is formed;
-// dS alternates between two TMEM buffers.
+// (A read from TMEM, K as an MN-major B).  S(n+1) is issued as soon as S(n)
+// has been read and dP(n+1) as soon as dP(n) has, so both run while dS(n) is
+// formed; the elementwise warps read S, release it, take the exponentials,
+// then read and release dP.  dS alternates between two TMEM buffers.
 // TMEM: S 128 + dP 128 + dQ D + 2 x 64 (dS) <= 512 columns.
 //
 // Every wait is bounded (Ctl): on expiry the CTA sets SP_DEV_TIMEOUT, stops
@@ -58,11 +59,13 @@ enum : int {
   B_V_FULL = 7,    // +stage (2)
   B_V_EMPTY = 9,   // +stage
   B_S_FULL = 11,
-  B_S_FREE = 12,   // 8 warp arrivals
-  B_DS_FULL = 13,  // +buffer, 8 warp arrivals
-  B_DS_FREE = 15,  // +buffer
-  B_DQ_DONE = 17,
-  B_COUNT = 18
+  B_DP_FULL = 12,
+  B_S_FREE = 13,   // 8 warp arrivals
+  B_DP_FREE = 14,  // 8 warp arrivals
+  B_DS_FULL = 15,  // +buffer, 8 warp arrivals
+  B_DS_FREE = 17,  // +buffer
+  B_DQ_DONE = 19,
+  B_COUNT = 20
 };
 
 template <int D>
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctl ctl{sbase + L::BAR, reinterpret_cast<volatile int *>(smem + L::ABORT), d_status, kSpinLimit};
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i)
-      mbar_init(ctl.bar(i), (i == B_S_FREE || i == B_DS_FULL || i == B_DS_FULL + 1) ? 8u : 1u);
+      mbar_init(ctl.bar(i), (i == B_S_FREE || i == B_DP_FREE || i == B_DS_FULL || i == B_DS_FULL + 1) ? 8u : 1u);
     *ctl.abort = 0;
     fence_mbar_init();
   }
@@ -189,37 +192,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_q = idesc_bf16_f32(kBM, D, 0, 1);    // dQ += dS K (K as MN-major B)
       const uint64_t dq_a = smem_desc_sw128(sbase + L::Q, 16, 1024);
       const uint64_t ddo_a = smem_desc_sw128(sbase + L::DO, 16, 1024);
-      // S(n), dP(n) into TMEM; one commit for both
+      // S(n) = Q K(n)^T into TMEM
       auto issue_s = [&](int n) {
-        const uint32_t kst = sbase + L::K + (n % kKStages) * L::KV, vst = sbase + L::V + (n % kVStages) * L::KV;
-        const uint64_t dk = smem_desc_sw128(kst, 16, 1024), dv = smem_desc_sw128(vst, 16, 1024);
+        const uint64_t dk = smem_desc_sw128(sbase + L::K + (n % kKStages) * L::KV, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
           mma_bf16_ss(tmem + T_S, dq_a + off, dk + off, id_s, kk > 0);
         }
+        mma_commit(ctl.bar(B_S_FULL));
+      };
+      // dP(n) = dO V(n)^T into TMEM
+      auto issue_dp = [&](int n) {
+        const uint64_t dv = smem_desc_sw128(sbase + L::V + (n % kVStages) * L::KV, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * kChunk + (kk & 3) * 32) >> 4;
           mma_bf16_ss(tmem + T_DP, ddo_a + off, dv + off, id_s, kk > 0);
         }
-        mma_commit(ctl.bar(B_S_FULL));
+        mma_commit(ctl.bar(B_DP_FULL));
         mma_commit(ctl.bar(B_V_EMPTY + n % kVStages));  // V(n) is read by dP(n) only
       };
-      bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_K_FULL, 0) && ctl.wait(B_V_FULL, 0);
+      bool ok = ctl.wait(B_Q_FULL, 0) && ctl.wait(B_K_FULL, 0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
       }
+      if (ok && (ok = ctl.wait(B_V_FULL, 0))) {
+        tc_fence_after();
+        issue_dp(0);
+      }
       for (int n = 0; ok && n < nblk; ++n) {
         const int st = n & 1;
         if (n + 1 < nblk) {
-          // S(n) and dP(n) have been read out: S(n+1), dP(n+1) may overwrite them
+          // S(n) has been read out: S(n+1) may overwrite it; likewise dP
           if (!(ok = ctl.wait(B_S_FREE, n & 1))) break;
           if (!(ok = ctl.wait(B_K_FULL + (n + 1) % kKStages, ((n + 1) / kKStages) & 1))) break;
-          if (!(ok = ctl.wait(B_V_FULL + (n + 1) % kVStages, ((n + 1) / kVStages) & 1))) break;
           tc_fence_after();
           issue_s(n + 1);
+          if (!(ok = ctl.wait(B_DP_FREE, n & 1))) break;
+          if (!(ok = ctl.wait(B_V_FULL + (n + 1) % kVStages, ((n + 1) / kVStages) & 1))) break;
+          tc_fence_after();
+          issue_dp(n + 1);
         }
         if (!(ok = ctl.wait(B_DS_FULL + st, (n >> 1) & 1))) break;
         tc_fence_after();
@@ -256,13 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool full = kb + kBN <= kv1 && (!causal || kb + kBN - 1 <= q0);
       // keys [kb, kb + lim) visible to this row
       const int lim = !rowv ? 0 : (causal ? min(kv1 - kb, tok - kb + 1) : kv1 - kb);
-      // this group's 64 columns of S and dP, all loaded before S_FREE so the
-      // next block's S and dP products can start at once
+      // this group's 64 columns of S, all loaded before S_FREE so the next
+      // block's S product can start at once
       uint32_t us[64], ud[64];
-      tmem_ld32x2(tmem + lane_base + T_S + 64 * h, tmem + lane_base + T_DP + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(us),
-                  *reinterpret_cast<uint32_t(*)[32]>(ud));
-      tmem_ld32x2(tmem + lane_base + T_S + 64 * h + 32, tmem + lane_base + T_DP + 64 * h + 32,
-                  *reinterpret_cast<uint32_t(*)[32]>(us + 32), *reinterpret_cast<uint32_t(*)[32]>(ud + 32));
+      tmem_ld32x2(tmem + lane_base + T_S + 64 * h, tmem + lane_base + T_S + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(us), *reinterpret_cast<uint32_t(*)[32]>(us + 32));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ctl.bar(B_S_FREE));
@@ -281,6 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int i = 0; i < 64; ++i) us[i] = __float_as_uint(ex2(__uint_as_float(us[i])));
+      // this group's 64 columns of dP, released as soon as they are read
+      if (!(ok = ctl.wait_warp(B_DP_FULL, n & 1))) break;
+      tc_fence_after();
+      tmem_ld32x2(tmem + lane_base + T_DP + 64 * h, tmem + lane_base + T_DP + 64 * h + 32,
+                  *reinterpret_cast<uint32_t(*)[32]>(ud), *reinterpret_cast<uint32_t(*)[32]>(ud + 32));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ctl.bar(B_DP_FREE));
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 64; i += 2) {

@@ -52,7 +52,13 @@ using namespace ptx;
 constexpr int kBM = 128;           // query rows per tile
 constexpr int kBN = 128;           // keys per block
 constexpr int kStages = 2;         // K/V ring depth
-constexpr int kThreads = 320;      // 8 softmax warps + producer + MMA
+constexpr int kThreads = 384;      // 8 softmax warps + producer + MMA + 2 idle (a full third warpgroup)
+// Registers: the launch gives every thread 168; the third warpgroup (producer,
+// MMA, idle) drops to kRegsIssue and the softmax warpgroups take what it
+// frees: 2 x 128 x kRegsSoftmax + 128 x kRegsIssue = 384 x 168.
+constexpr int kRegsIssue = 136;
+constexpr int kRegsSoftmax = 184;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsIssue <= kThreads * 168, "register split");
 constexpr int kChunk = 128 * 128;  // bytes of one 128-row x 128-byte swizzled chunk
 constexpr int kRunsInSmem = 128;  // block runs of a work item kept in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
@@ -147,8 +153,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::TSLOT);
   if (runs_in_smem) runs = reinterpret_cast<const int32_t *>(smem + L::RUNS);
-
-  if (warp == 8) {
+  if (warp >= 8) {
+    // third warpgroup: producer, MMA issuer, two idle warps
+    setmaxnreg_dec<kRegsIssue>();
+    if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -262,8 +270,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(ctl.bar(B_MMA_DONE));
       ctl.drain(B_MMA_DONE, 0);
     }
+    }
   } else {
     // ------------------------------------------------------------- softmax
+    setmaxnreg_inc<kRegsSoftmax>();
     const int t = warp >> 2;  // tile handled by this warpgroup
     const int r = threadIdx.x & 127;
     const bool active = t == 0 || tlb != nullptr;

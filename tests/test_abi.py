@@ -230,9 +230,9 @@ def test_bench_traffic_is_null_when_kernel_sources_change(monkeypatch):
         assert ks["units"] > 0
         for k, (nbytes, digest) in ((k, v) for k, v in ks.items() if k != "units"):
             assert len(digest) == 16 and nbytes > 0
-    # every bench workload but the tiny tree has a capture of its own or of a reduced twin
+    # every bench workload has a capture of its own or of a reduced twin
     for cfg in W.CONFIGS:
-        assert cfg == "tiny" or cfg in bench.MEASURED_TRAFFIC or bench.TRAFFIC_SCALED_FROM[cfg] in bench.MEASURED_TRAFFIC
+        assert cfg in bench.MEASURED_TRAFFIC or bench.TRAFFIC_SCALED_FROM[cfg] in bench.MEASURED_TRAFFIC
     monkeypatch.setitem(bench.MEASURED_TRAFFIC, "agent_small",
                         {"units": 10, "bwd_tc_kernel": (1.0, "0" * 16)})
     assert bench.measured_traffic("agent_small", "bwd_tc_kernel", 10)[0] is None
