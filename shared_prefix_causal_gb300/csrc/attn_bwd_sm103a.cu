@@ -21,11 +21,18 @@
 // [32h, 32h + 32) of every key row (TMEM lane = key row); warps 4-7 also read
 // dQ^T out (TMEM lane = head-dim index); in the epilogue warps 0-3 store dK
 // and warps 4-7 dV.  Warp 8: TMA producer (Q, dO, and the per-column LSE /
-// Delta staged by the whole warp); warp 9: the single-thread MMA issuer.  The
-// MMA issue order is software pipelined: S^T and dP^T of block j are issued
-// as soon as block j-1's S^T and dP^T have been read, before dV, dK and dQ^T
-// of block j-1, so the elementwise work of block j overlaps the second half of
-// block j-1.
+// Delta staged by the whole warp); warps 9 and 10: one MMA issuer each, warp 9
+// for S^T and dP^T, warp 10 for dV, dK and dQ^T.  S^T and dP^T of block j are
+// issued as soon as block j-1's have been read, so the elementwise work of
+// block j overlaps the gradient products of block j-1.  The two issuers share
+// the tensor pipe but wait on their own barriers: an mbarrier wait costs the
+// waiting thread about a hundred cycles even when the phase is complete, and a
+// thread blocked there issues nothing, so one issuer's waits run while the
+// other's products keep the pipe busy.  Their products write disjoint TMEM
+// columns and every operand they share is handed over through barriers (P^T,
+// dS^T and dQ^T double- or single-buffered with full/free pairs, a Q/dO stage
+// released by warp 10 after the products that read it last), so no ordering
+// between the two threads' products is needed.
 //
 // Companion kernels: bwd_pre (Delta = rowsum(dO * O) and zeroing the fp32 dQ
 // workspace) and dq_convert (scale and round dQ to bf16).
@@ -47,7 +54,7 @@ using namespace ptx;
 
 constexpr int kBK = 128;            // keys per CTA
 constexpr int kBQ = 64;             // query rows per block
-constexpr int kThreads = 320;       // 10 warps
+constexpr int kThreads = 352;       // 11 warps
 constexpr int kKChunk = 128 * 128;  // 128 rows x 128 bytes
 constexpr int kQChunk = 64 * 128;   // 64 rows x 128 bytes
 constexpr float kLog2e = 1.4426950408889634f;
@@ -65,7 +72,8 @@ enum : int {
   B_DQ_FULL = 13,
   B_DQ_FREE = 14,
   B_FINAL = 15,
-  B_COUNT = 16
+  B_SDP_DONE = 16,  // the S^T / dP^T issuer's last products have completed
+  B_COUNT = 17
 };
 
 template <int D>
@@ -217,70 +225,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctl.drain(B_Q_FULL + m % kStages, (m / kStages) & 1);
     }
   } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer
+    // ----------------------------------------------- S^T and dP^T MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kBK, kBQ, 0, 0);  // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16_f32(kBK, D, 0, 1);   // dV, dK
-      constexpr uint32_t id_q = idesc_bf16_f32(128, kBQ, 1, 1);  // dQ^T
       // operand descriptors, built once; a K step only moves the start address
       const uint64_t dk_kmaj = smem_desc_sw128(sbase + L::K, 16, 1024);
       const uint64_t dv_kmaj = smem_desc_sw128(sbase + L::V, 16, 1024);
+      bool ok = ctl.wait(B_KV_FULL, 0);
+      tc_fence_after();
+      for (int j = 0; ok && j < nq; ++j) {
+        const int st = j % kStages;
+        const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
+        if (!(ok = ctl.wait(B_Q_FULL + st, (j / kStages) & 1))) break;
+        if (!(ok = ctl.wait(B_S_FREE, (j & 1) ^ 1))) break;
+        tc_fence_after();
+        const uint64_t dq_k = smem_desc_sw128(stage + L::Q_OFF, 16, 1024);
+        const uint64_t ddo_k = smem_desc_sw128(stage + L::DO_OFF, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
+          const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + T_S, dk_kmaj + ka, dq_k + qa, id_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
+          const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
+          mma_bf16_ss(tmem + T_DP, dv_kmaj + ka, ddo_k + qa, id_s, kk > 0);
+        }
+        mma_commit(ctl.bar(B_S_FULL));
+      }
+      // every product of this thread has completed before TMEM is freed
+      mma_commit(ctl.bar(B_SDP_DONE));
+      ctl.drain(B_SDP_DONE, 0);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------ dV, dK and dQ^T MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_kv = idesc_bf16_f32(kBK, D, 0, 1);   // dV, dK
+      constexpr uint32_t id_q = idesc_bf16_f32(128, kBQ, 1, 1);  // dQ^T
       const uint64_t dk_mn = smem_desc_sw128(sbase + L::K, kKChunk, 1024);
       // per dS^T buffer b: dS^T as A (K-major) and as B (MN-major)
       const uint64_t dst_kmaj0 = smem_desc_sw128(sbase + L::PS, 16, 1024);
       const uint64_t dst_mn0 = smem_desc_sw128(sbase + L::PS, kQChunk, 1024);
       constexpr uint32_t kPsStep = uint32_t(L::PS_BYTES) >> 4;  // descriptor units between buffers
+      // P^T(m) in TMEM implies S^T(m), and so K, V and the stage's Q/dO, were
+      // in shared memory; K/V and the stage are still checked
       bool ok = ctl.wait(B_KV_FULL, 0);
-      tc_fence_after();
-      for (int j = 0; ok && j <= nq; ++j) {
-        if (j < nq) {
-          const int st = j % kStages;
-          const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
-          if (!(ok = ctl.wait(B_Q_FULL + st, (j / kStages) & 1))) break;
-          if (!(ok = ctl.wait(B_S_FREE, (j & 1) ^ 1))) break;
-          tc_fence_after();
-          const uint64_t dq_k = smem_desc_sw128(stage + L::Q_OFF, 16, 1024);
-          const uint64_t ddo_k = smem_desc_sw128(stage + L::DO_OFF, 16, 1024);
+      for (int m = 0; ok && m < nq; ++m) {
+        const int st = m % kStages, pb = m & 1;
+        const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
+        if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
+        if (!(ok = ctl.wait(B_Q_FULL + st, (m / kStages) & 1))) break;
+        if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
+        tc_fence_after();
+        const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
+        const uint32_t pso = pb * kPsStep;
+        const uint64_t dst_kmaj = dst_kmaj0 + pso, dst_mn = dst_mn0 + pso;
+        const uint64_t dq_mn = smem_desc_sw128(stage + L::Q_OFF, kQChunk, 1024);
+        // dV += P^T dO (P^T read from TMEM, 8 columns per K step); dK += dS^T Q  (K = 64 query rows)
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
-            const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
-            mma_bf16_ss(tmem + T_S, dk_kmaj + ka, dq_k + qa, id_s, kk > 0);
-          }
+        for (int kk = 0; kk < kBQ / 16; ++kk)
+          mma_bf16_ts(tmem + T_DK + D, tmem + T_P + 32 * pb + 8 * kk, ddo_mn + ((kk * 2048) >> 4), id_kv,
+                      (m > 0 || kk > 0));
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ka = ((kk >> 2) * kKChunk + (kk & 3) * 32) >> 4;
-            const uint32_t qa = ((kk >> 2) * kQChunk + (kk & 3) * 32) >> 4;
-            mma_bf16_ss(tmem + T_DP, dv_kmaj + ka, ddo_k + qa, id_s, kk > 0);
-          }
-          mma_commit(ctl.bar(B_S_FULL));
-        }
-        if (j >= 1) {
-          const int m = j - 1, st = m % kStages, pb = m & 1;
-          const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
-          if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
-          if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
-          tc_fence_after();
-          const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
-          const uint32_t pso = pb * kPsStep;
-          const uint64_t dst_kmaj = dst_kmaj0 + pso, dst_mn = dst_mn0 + pso;
-          const uint64_t dq_mn = smem_desc_sw128(stage + L::Q_OFF, kQChunk, 1024);
-          // dV += P^T dO (P^T read from TMEM, 8 columns per K step); dK += dS^T Q  (K = 64 query rows)
+        for (int kk = 0; kk < kBQ / 16; ++kk)
+          mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
+        // dQ^T = K^T dS^T   (K = 128 keys)
 #pragma unroll
-          for (int kk = 0; kk < kBQ / 16; ++kk)
-            mma_bf16_ts(tmem + T_DK + D, tmem + T_P + 32 * pb + 8 * kk, ddo_mn + ((kk * 2048) >> 4), id_kv,
-                        (m > 0 || kk > 0));
-#pragma unroll
-          for (int kk = 0; kk < kBQ / 16; ++kk)
-            mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
-          // dQ^T = K^T dS^T   (K = 128 keys)
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
-          mma_commit(ctl.bar(B_DQ_FULL));
-          mma_commit(ctl.bar(B_P_FREE + pb));
-          mma_commit(ctl.bar(B_Q_EMPTY + st));
-        }
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
+        mma_commit(ctl.bar(B_DQ_FULL));
+        mma_commit(ctl.bar(B_P_FREE + pb));
+        mma_commit(ctl.bar(B_Q_EMPTY + st));  // S^T(m) and dP^T(m) completed before P^T(m) existed
       }
       mma_commit(ctl.bar(B_FINAL));
       ctl.drain(B_FINAL, 0);

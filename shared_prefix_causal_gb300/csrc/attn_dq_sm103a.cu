@@ -16,11 +16,17 @@
 // [64h, 64h + 64) of every row (the work needs no row reduction, so the
 // split needs no exchange); warp 8: TMA producer (Q and dO once, K/V blocks
 // through rings of three and two stages: K is read last by dQ, V only by
-// dP, so a third K stage gives the next blocks' loads time to land); warp 9:
-// tcgen05 MMA issuer.  Per key block
-// n the MMA thread issues S = Q K^T and dP = dO V^T (SS), and, once the
-// elementwise warps have stored dS(n) as bf16 pairs in TMEM, dQ += dS(n) K(n)
-// (A read from TMEM, K as an MN-major B).  S(n+1) is issued as soon as S(n)
+// dP, so a third K stage gives the next blocks' loads time to land); warps 9
+// and 10: one tcgen05 MMA issuer each.  Per key block n warp 9 issues
+// S = Q K^T and dP = dO V^T (SS), and warp 10, once the elementwise warps
+// have stored dS(n) as bf16 pairs in TMEM, dQ += dS(n) K(n) (A read from
+// TMEM, K as an MN-major B).  The two issuers share the tensor pipe but wait
+// on their own barriers: an mbarrier wait costs the waiting thread about a
+// hundred cycles even when the phase is already complete, and a thread
+// blocked there issues nothing, so one issuer's waits run while the other's
+// products keep the pipe busy.  Their products touch disjoint TMEM columns
+// and every hand-over between them goes through the elementwise warps'
+// barriers, so no ordering between the two threads' products is needed.  S(n+1) is issued as soon as S(n)
 // has been read and dP(n+1) as soon as dP(n) has, so both run while dS(n) is
 // formed; the elementwise warps read S, release it, take the exponentials,
 // then read and release dP.  dS alternates between two TMEM buffers.
@@ -48,7 +54,7 @@ constexpr int kBM = 128;           // query rows per tile (tokens x query heads 
 constexpr int kBN = 128;           // keys per block
 constexpr int kKStages = 3;        // K ring depth (K is read by S and, last, by dQ)
 constexpr int kVStages = 2;        // V ring depth (V is read by dP only)
-constexpr int kThreads = 320;      // 8 elementwise warps, producer, MMA
+constexpr int kThreads = 352;      // 8 elementwise warps, producer, two MMA issuers
 constexpr int kChunk = 128 * 128;  // one 128-row x 128-byte swizzled chunk
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -65,7 +71,8 @@ enum : int {
   B_DS_FULL = 15,  // +buffer, 8 warp arrivals
   B_DS_FREE = 17,  // +buffer
   B_DQ_DONE = 19,
-  B_COUNT = 20
+  B_SDP_DONE = 20,  // the S / dP issuer's last products have completed
+  B_COUNT = 21
 };
 
 template <int D>
@@ -186,10 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp == 9) {
-    // ---------------------------------------------------------- MMA issuer
+    // ------------------------------------------------- S and dP MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(kBM, kBN, 0, 0);  // S = Q K^T, dP = dO V^T
-      constexpr uint32_t id_q = idesc_bf16_f32(kBM, D, 0, 1);    // dQ += dS K (K as MN-major B)
       const uint64_t dq_a = smem_desc_sw128(sbase + L::Q, 16, 1024);
       const uint64_t ddo_a = smem_desc_sw128(sbase + L::DO, 16, 1024);
       // S(n) = Q K(n)^T into TMEM
@@ -222,9 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_dp(0);
       }
-      for (int n = 0; ok && n < nblk; ++n) {
-        const int st = n & 1;
-        if (n + 1 < nblk) {
+      for (int n = 0; ok && n + 1 < nblk; ++n) {
+        {
           // S(n) has been read out: S(n+1) may overwrite it; likewise dP
           if (!(ok = ctl.wait(B_S_FREE, n & 1))) break;
           if (!(ok = ctl.wait(B_K_FULL + (n + 1) % kKStages, ((n + 1) / kKStages) & 1))) break;
@@ -235,7 +240,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           issue_dp(n + 1);
         }
+      }
+      // every S and dP product of this thread has completed before TMEM is freed
+      mma_commit(ctl.bar(B_SDP_DONE));
+      ctl.drain(B_SDP_DONE, 0);
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------ dQ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_q = idesc_bf16_f32(kBM, D, 0, 1);  // dQ += dS K (K as MN-major B)
+      bool ok = true;
+      for (int n = 0; ok && n < nblk; ++n) {
+        const int st = n & 1;
+        // dS(n) in TMEM (so S(n), and the K(n) it read, are complete); K(n) still checked
         if (!(ok = ctl.wait(B_DS_FULL + st, (n >> 1) & 1))) break;
+        if (!(ok = ctl.wait(B_K_FULL + n % kKStages, (n / kKStages) & 1))) break;
         tc_fence_after();
         const uint64_t dk_mn = smem_desc_sw128(sbase + L::K + (n % kKStages) * L::KV, kChunk, 1024);
 #pragma unroll
@@ -243,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + T_DQ, tmem + T_DS + 64 * st + 8 * kk, dk_mn + ((kk * 2048) >> 4), id_q,
                       (n > 0 || kk > 0));
         mma_commit(ctl.bar(B_DS_FREE + st));
-        mma_commit(ctl.bar(B_K_EMPTY + n % kKStages));
+        mma_commit(ctl.bar(B_K_EMPTY + n % kKStages));  // S(n) read K(n) before dS(n) existed
       }
       mma_commit(ctl.bar(B_DQ_DONE));
       ctl.drain(B_DQ_DONE, 0);
