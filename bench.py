@@ -55,19 +55,19 @@ TRAFFIC_SOURCES = {
 # decides that traffic; the units are query heads x useful pairs of that workload.
 MEASURED_TRAFFIC = {
     "tiny": {"units": 26252,
-             "fwd_tc_kernel": (198400 + 0, "177b62d43aadb1f6"),
+             "fwd_tc_kernel": (195840 + 0, "bef68dc65ce204f9"),
              "bwd_tc_kernel": (352768 + 0, "03ec65811963b438")},
     "star": {"units": 506117152,
-             "fwd_tc_kernel": (94215424 + 27723008, "177b62d43aadb1f6"),
+             "fwd_tc_kernel": (94210048 + 27234048, "bef68dc65ce204f9"),
              "bwd_tc_kernel": (334935296 + 137194240, "03ec65811963b438")},
     "agent_small": {"units": 2424419552,
-                    "fwd_tc_kernel": (202080768 + 100678912, "177b62d43aadb1f6"),
+                    "fwd_tc_kernel": (201810688 + 100481792, "bef68dc65ce204f9"),
                     "bwd_tc_kernel": (2089151744 + 990385408, "03ec65811963b438")},
     "long_small": {"units": 8211399552,
-                   "fwd_tc_kernel": (336242432 + 233239808, "177b62d43aadb1f6"),
+                   "fwd_tc_kernel": (336259328 + 232525568, "bef68dc65ce204f9"),
                    "bwd_tc_kernel": (13751483392 + 7161786880, "03ec65811963b438")},
     "forest_small": {"units": 3793239488,
-                     "fwd_tc_kernel": (500553984 + 303532800, "177b62d43aadb1f6"),
+                     "fwd_tc_kernel": (499720704 + 303079168, "bef68dc65ce204f9"),
                      "bwd_tc_kernel": (3346484736 + 1629801472, "03ec65811963b438")},
 }
 # Full-size workloads are not captured with more than the launch time: their traffic is the reduced

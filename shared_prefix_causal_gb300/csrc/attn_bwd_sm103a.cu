@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < B_COUNT; ++i) {
       uint32_t cnt = 1;
       if (i == B_S_FREE || i == B_P_FULL || i == B_P_FULL + 1) cnt = 256;  // warps 0-7, every thread
-      if (i == B_DQ_FREE) cnt = 128;                                       // warps 4-7
+      if (i == B_DQ_FREE) cnt = 256;                                       // warps 0-7
       mbar_init(ctl.bar(i), cnt);
     }
     *ctl.abort = 0;
@@ -308,8 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 4h..4h+3) handles query columns [32h, 32h + 32) of every key row (thread
     // = key row = TMEM lane).  Both load their S^T and dP^T columns at once, so
     // S_FREE (and the next block's S^T/dP^T products) follows right away.
-    // Group 1 also reads block j-1's dQ^T out of TMEM and adds it into the fp32
-    // workspace; in the epilogue group 0 stores dK and group 1 dV.
+    // After handing over block j's P^T and dS^T each group reads its half of
+    // block j-1's dQ^T out of TMEM and adds it into the fp32 workspace; in the
+    // epilogue group 0 stores dK and group 1 dV.
     const int h = warp >> 2;
     const int r = threadIdx.x & 127;  // key row = TMEM lane
     const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
@@ -319,33 +320,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     // dQ^T of block m: TMEM lane d = head-dim index, 64 query columns; one
     // fp32 atomic add per (column, d) into the workspace row of that query
+    // Block m's dQ^T out of TMEM and into the fp32 workspace: warpgroup h
+    // takes query columns [32h, 32h + 32) (tokens 32h / G on), so the
+    // reductions are shared by all eight warps.
     auto dq_readout = [&](int m) -> bool {
-      const int qt = q_of(m);
+      const int qt = q_of(m) + 32 * h / G;
       if (!ctl.wait_warp(B_DQ_FULL, m & 1)) return false;
       tc_fence_after();
-      uint32_t u0[32], u1[32];
-      tmem_ld32x2(tmem + lane_base + T_DQ, tmem + lane_base + T_DQ + 32, u0, u1);
+      uint32_t u[32];
+      tmem_ld32(tmem + lane_base + T_DQ + 32 * h, u);
       tc_fence_before();
       mbar_arrive(ctl.bar(B_DQ_FREE));
       const int d = r;
       if (d < D) {
-        // query row c is token qt + c / G, head g * G + c % G
+        // query column 32h + c is token qt + c / G, head g * G + c % G
         float *base = dqacc + (size_t(qt) * Hq + g * G) * D + d;
         const size_t tstride = size_t(Hq) * D;
-        if (qt + tpb <= qe) {
+        if (q_of(m) + tpb <= qe) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u0[c]));
-#pragma unroll
-          for (int c = 32; c < 64; ++c)
-            atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u1[c - 32]));
+          for (int c = 0; c < 32; ++c) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u[c]));
         } else {
           const int ql = qe - qt;
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            if (c / G < ql) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u0[c]));
-#pragma unroll
-          for (int c = 32; c < 64; ++c)
-            if (c / G < ql) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u1[c - 32]));
+            if (c / G < ql) atomicAdd(base + (c / G) * tstride + (c % G) * D, __uint_as_float(u[c]));
         }
       }
       return true;
@@ -418,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(ctl.bar(B_P_FULL + pb));
-      if (h == 1 && j >= 1 && !(ok = dq_readout(j - 1))) break;
+      if (j >= 1 && !(ok = dq_readout(j - 1))) break;
     }
-    if (ok && h == 1 && nq >= 1) ok = dq_readout(nq - 1);
+    if (ok && nq >= 1) ok = dq_readout(nq - 1);
     if (ok && ctl.wait_warp(B_FINAL, 0)) {
       tc_fence_after();
       // group 0: dK (scaled); group 1: dV
