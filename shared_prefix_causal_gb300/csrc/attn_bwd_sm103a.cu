@@ -277,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = sbase + L::STAGE + st * L::STAGE_BYTES;
         if (!(ok = ctl.wait(B_P_FULL + pb, (m >> 1) & 1))) break;
         if (!(ok = ctl.wait(B_Q_FULL + st, (m / kStages) & 1))) break;
-        if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
         tc_fence_after();
         const uint64_t ddo_mn = smem_desc_sw128(stage + L::DO_OFF, kQChunk, 1024);
         const uint32_t pso = pb * kPsStep;
@@ -291,13 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
           mma_bf16_ss(tmem + T_DK, dst_kmaj + ((kk * 32) >> 4), dq_mn + ((kk * 2048) >> 4), id_kv, (m > 0 || kk > 0));
+        // dV and dK were the stage's last readers (S^T(m) and dP^T(m) completed
+        // before P^T(m) existed): release it before waiting for the dQ^T buffer
+        mma_commit(ctl.bar(B_Q_EMPTY + st));
+        if (!(ok = ctl.wait(B_DQ_FREE, (m & 1) ^ 1))) break;
+        tc_fence_after();
         // dQ^T = K^T dS^T   (K = 128 keys)
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
           mma_bf16_ss(tmem + T_DQ, dk_mn + ((kk * 2048) >> 4), dst_mn + ((kk * 2048) >> 4), id_q, kk > 0);
         mma_commit(ctl.bar(B_DQ_FULL));
         mma_commit(ctl.bar(B_P_FREE + pb));
-        mma_commit(ctl.bar(B_Q_EMPTY + st));  // S^T(m) and dP^T(m) completed before P^T(m) existed
       }
       mma_commit(ctl.bar(B_FINAL));
       ctl.drain(B_FINAL, 0);
