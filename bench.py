@@ -56,19 +56,19 @@ TRAFFIC_SOURCES = {
 MEASURED_TRAFFIC = {
     "tiny": {"units": 26252,
              "fwd_tc_kernel": (195840 + 0, "bef68dc65ce204f9"),
-             "bwd_tc_kernel": (352768 + 0, "03ec65811963b438")},
+             "bwd_tc_kernel": (345088 + 0, "d80b00f04b0affea")},
     "star": {"units": 506117152,
              "fwd_tc_kernel": (94210048 + 27234048, "bef68dc65ce204f9"),
-             "bwd_tc_kernel": (334935296 + 137194240, "03ec65811963b438")},
+             "bwd_tc_kernel": (343944192 + 140833024, "d80b00f04b0affea")},
     "agent_small": {"units": 2424419552,
                     "fwd_tc_kernel": (201810688 + 100481792, "bef68dc65ce204f9"),
-                    "bwd_tc_kernel": (2089151744 + 990385408, "03ec65811963b438")},
+                    "bwd_tc_kernel": (2277282560 + 1094525696, "d80b00f04b0affea")},
     "long_small": {"units": 8211399552,
                    "fwd_tc_kernel": (336259328 + 232525568, "bef68dc65ce204f9"),
-                   "bwd_tc_kernel": (13751483392 + 7161786880, "03ec65811963b438")},
+                   "bwd_tc_kernel": (12625401600 + 6598909184, "d80b00f04b0affea")},
     "forest_small": {"units": 3793239488,
                      "fwd_tc_kernel": (499720704 + 303079168, "bef68dc65ce204f9"),
-                     "bwd_tc_kernel": (3346484736 + 1629801472, "03ec65811963b438")},
+                     "bwd_tc_kernel": (3755256320 + 1951604992, "d80b00f04b0affea")},
 }
 # Full-size workloads are not captured with more than the launch time: their traffic is the reduced
 # workload's of the same shape, scaled by the ratio of units (query heads x useful pairs).
@@ -573,14 +573,25 @@ def run_gpu(args):
 
 
 def fragment_summary(spc, w, cap: int):
-    """Bounded fragments of the workload's tree (host planner): count and token duplication."""
+    """Bounded fragments of the workload's tree (host planner): count and token duplication.  A cap
+    below the tree's longest root path is infeasible; it is doubled until it holds that path."""
+    need = 0
+    depth_tokens = np.zeros(w.tree.num_segments, dtype=np.int64)
+    for s in range(w.tree.num_segments):
+        p = int(w.tree.parent[s])
+        depth_tokens[s] = (depth_tokens[p] if p >= 0 else 0) + int(w.tree.seg_len[s])
+        need = max(need, int(depth_tokens[s]))
+    asked = cap
+    while cap < need:
+        cap *= 2
     t0 = time.perf_counter()
     try:
         f = spc.fragment_plan(w.tree, cap)
     except RuntimeError as e:
         return {"cap": cap, "error": str(e)}
     ms = (time.perf_counter() - t0) * 1e3
-    return {"cap": cap, "fragments": f["num_fragments"], "physical_tokens": f["physical_tokens"],
+    return {"cap": cap, **({"cap_asked": asked, "longest_root_path": need} if cap != asked else {}),
+            "fragments": f["num_fragments"], "physical_tokens": f["physical_tokens"],
             "fragment_tokens": f["fragment_tokens"],
             "duplication": round(f["fragment_tokens"] / max(1, f["physical_tokens"]), 4), "plan_ms": round(ms, 3)}
 
