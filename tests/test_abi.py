@@ -421,7 +421,11 @@ def test_bench_fragment_summary():
     out = bench.fragment_summary(spc, W.get("tiny"), 130)
     assert out["fragments"] == 4 and out["fragment_tokens"] == 426 and out["physical_tokens"] == 186
     assert out["duplication"] == round(426 / 186, 4)
-    assert "error" in bench.fragment_summary(spc, W.get("tiny"), 10)
+    # a cap below the longest root path (64 + 48 + 16 = 128 tokens) is doubled until it holds it
+    out = bench.fragment_summary(spc, W.get("tiny"), 10)
+    assert out["cap"] == 160 and out["cap_asked"] == 10 and out["longest_root_path"] == 128
+    assert out == {**bench.fragment_summary(spc, W.get("tiny"), 160), "cap_asked": 10, "longest_root_path": 128,
+                   "plan_ms": out["plan_ms"]}
 
 
 def test_bench_clock_sampler_keeps_only_the_timed_window(tmp_path):
