@@ -744,7 +744,9 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
     in_bytes = {n: t.numel() * t.element_size() for n, t in host.items()}
     if idx_h is not None:
         in_bytes["idx"] = idx_h.numel() * idx_h.element_size()
-    in_lanes = deal(list(in_bytes), in_bytes, len(s_in))
+    # the forward's inputs first, so a step's forward starts while the rest is still coming in
+    first = [n for n in ("q", "k", "v") if n in in_bytes]
+    in_lanes = [deal(first, in_bytes, len(s_in)), deal([n for n in in_bytes if n not in first], in_bytes, len(s_in))]
     plan_buf = [None] * nbuf  # per buffer set: the device buffer its steps' plans are uploaded into
     ev_comp = [torch.cuda.Event() for _ in range(nbuf)]   # compute of the set's last step done
     ev_out = [torch.cuda.Event() for _ in range(nbuf)]    # results of the set's last step copied out
@@ -780,25 +782,29 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         m["host_upload_ms"] = (time.perf_counter() - t_up) * 1e3
         comp.wait_event(m["upload1"])
         plans.append(plan)
-        m["h2d0"], m["h2d1"] = ev(), ev()
+        m["h2d0"], m["h2d_fwd"], m["h2d1"] = ev(), ev(), ev()
         s_in[0].wait_event(ev_comp[b])  # the set's inputs are free once its previous step has computed
         m["h2d0"].record(s_in[0])
-        for si, lane_names in zip(s_in, in_lanes):
-            if si is not s_in[0]:
-                si.wait_event(m["h2d0"])
-            with torch.cuda.stream(si):
-                for n in lane_names:
-                    d[n].copy_(idx_h if n == "idx" else host[n], non_blocking=True)
         for si in s_in[1:]:
-            e_ = torch.cuda.Event()
-            e_.record(si)
-            s_in[0].wait_event(e_)
-        m["h2d1"].record(s_in[0])
-        comp.wait_event(m["h2d1"])
-        comp.wait_event(ev_out[b])  # the set's result buffers have been copied out
+            si.wait_event(m["h2d0"])
+        for phase, lanes in enumerate(in_lanes):
+            for si, lane_names in zip(s_in, lanes):
+                if phase == 1:
+                    si.wait_event(m["h2d_fwd"])  # the forward's inputs get the whole link first
+                with torch.cuda.stream(si):
+                    for n in lane_names:
+                        d[n].copy_(idx_h if n == "idx" else host[n], non_blocking=True)
+            for si in s_in[1:]:
+                e_ = torch.cuda.Event()
+                e_.record(si)
+                s_in[0].wait_event(e_)
+            m["h2d_fwd" if phase == 0 else "h2d1"].record(s_in[0])
+        comp.wait_event(m["h2d_fwd"])  # Q, K, V in: the forward may start
         m["comp0"], m["comp1"] = ev(), ev()
         m["comp0"].record(comp)
         spc.sp_tree_attn_fwd(plan, d["q"], d["k"], d["v"], d["o"], d["lse"], w.softmax_scale, status)
+        comp.wait_event(m["h2d1"])  # dO, the hidden rows and the edge indices in
+        comp.wait_event(ev_out[b])  # the set's result buffers have been copied out
         spc.sp_tree_attn_bwd(plan, d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], d["dq"], d["dk"], d["dv"],
                              d["ws"], w.softmax_scale, status)
         if d["g"] is not None:
@@ -844,8 +850,9 @@ def run_e2e(args, spc, w, x, dev, flops_per_step):
         raise RuntimeError(f"device status {status.item()} in the end-to-end run")
     return {"value": round(flops_per_step / el / 1e12, 3), "unit": UNIT, "ms_per_step": round(el * 1e3, 3),
             "steps": n, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "pipelined": "3 buffer sets; inputs in on three streams, results out on two, the next steps' copies "
-                         "overlapping this step's compute; each step's plan uploaded into a reused device buffer",
+            "pipelined": "3 buffer sets; inputs in on three streams (Q, K, V first: a step's forward starts before "
+                         "dO and the hidden rows are in), results out on two, the next steps' copies overlapping "
+                         "this step's compute; each step's plan uploaded into a reused device buffer",
             "includes": "tree_plan + plan upload + H2D of q,k,v,dO,hidden,idx + fwd + bwd + edge_gather + "
                         "D2H of dQ,dK,dV and gathered rows",
             "breakdown": breakdown}
@@ -863,6 +870,7 @@ def e2e_breakdown(marks, t_start, step_ms):
     fill = el(t_start, marks[0]["comp0"])
     drain = el(marks[-1]["comp1"], marks[-1]["d2h1"])
     return {"compute_ms": med(comp), "h2d_ms": med([el(m["h2d0"], m["h2d1"]) for m in marks]),
+            "h2d_forward_inputs_ms": med([el(m["h2d0"], m["h2d_fwd"]) for m in marks if "h2d_fwd" in m]),
             "d2h_ms": med([el(m["d2h0"], m["d2h1"]) for m in marks]),
             "upload_ms": med([el(m["upload0"], m["upload1"]) for m in marks]),
             "compute_idle_between_steps_ms": med(gaps), "compute_idle_total_ms": round(sum(gaps), 4),
