@@ -881,6 +881,9 @@ def e2e_breakdown(marks, t_start, step_ms):
             "device_span_ms": round(total, 4), "step_ms_host_clock": round(step_ms, 4),
             "host_plan_ms": med([m["host_plan_ms"] for m in marks]),
             "host_upload_ms": med([m["host_upload_ms"] for m in marks]),
+            "host_upload_max_ms": round(max(m["host_upload_ms"] for m in marks), 4),
+            "host_wait_max_ms": round(max(m["host_wait_ms"] for m in marks), 4),
+            "h2d_ms_by_step": [round(el(m["h2d0"], m["h2d1"]), 2) for m in marks],
             "host_wait_ms": med([m["host_wait_ms"] for m in marks]),
             "host_step_ms": med([m["host_ms"] for m in marks])}
 
