@@ -55,19 +55,19 @@ TRAFFIC_SOURCES = {
 # decides that traffic; the units are query heads x useful pairs of that workload.
 MEASURED_TRAFFIC = {
     "tiny": {"units": 26252,
-             "fwd_tc_kernel": (195840 + 0, "bef68dc65ce204f9"),
+             "fwd_tc_kernel": (195840 + 0, "6551394c778f6917"),
              "bwd_tc_kernel": (345088 + 0, "d80b00f04b0affea")},
     "star": {"units": 506117152,
-             "fwd_tc_kernel": (94210048 + 27234048, "bef68dc65ce204f9"),
+             "fwd_tc_kernel": (94208000 + 27344384, "6551394c778f6917"),
              "bwd_tc_kernel": (343944192 + 140833024, "d80b00f04b0affea")},
     "agent_small": {"units": 2424419552,
-                    "fwd_tc_kernel": (201810688 + 100481792, "bef68dc65ce204f9"),
+                    "fwd_tc_kernel": (202022144 + 100264960, "6551394c778f6917"),
                     "bwd_tc_kernel": (2277282560 + 1094525696, "d80b00f04b0affea")},
     "long_small": {"units": 8211399552,
-                   "fwd_tc_kernel": (336259328 + 232525568, "bef68dc65ce204f9"),
+                   "fwd_tc_kernel": (336584704 + 232509952, "6551394c778f6917"),
                    "bwd_tc_kernel": (12625401600 + 6598909184, "d80b00f04b0affea")},
     "forest_small": {"units": 3793239488,
-                     "fwd_tc_kernel": (499720704 + 303079168, "bef68dc65ce204f9"),
+                     "fwd_tc_kernel": (499851008 + 303153920, "6551394c778f6917"),
                      "bwd_tc_kernel": (3755256320 + 1951604992, "d80b00f04b0affea")},
 }
 # Full-size workloads are not captured with more than the launch time: their traffic is the reduced

@@ -422,6 +422,15 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
+  // setmaxnreg.inc waits until the registers it asks for are free: launch only
+  // if the block's registers at launch cover the split, or it would never return
+  static int regs = 0;
+  if (!regs) {
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return SP_ERR_CUDA;
+    regs = fa.numRegs;
+  }
+  if (regs * kThreads < 2 * 128 * kRegsSoftmax + 128 * kRegsIssue) return SP_ERR_UNSUPPORTED;
   const unsigned grid = unsigned(p.n_pairs) * unsigned(s.Hkv);
   CtaClock clk;
   cta_clock_for(kClockForward, &clk.buf, &clk.cap);
