@@ -48,7 +48,8 @@ CSRC = os.path.join(ROOT, "shared_prefix_causal_gb300", "csrc")
 TRAFFIC_SOURCES = {
     "fwd_tc_kernel": ("attn_fwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_pairs",
                       "plan.cpp:tile_runs", "plan.cpp:merge_runs"),
-    "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_bwd_schedule"),
+    "bwd_tc_kernel": ("attn_bwd_sm103a.cu", "sm103_ptx.cuh", "pipeline.cuh", "plan.cpp:build_bwd_schedule",
+                      "plan.cpp:build_bwd_merged"),
 }
 # DRAM bytes (read + write) of one launch, from an ncu capture of one launch of the kernel on the
 # named workload (dram__bytes_read.sum + dram__bytes_write.sum), with the digest of the code that
@@ -56,19 +57,19 @@ TRAFFIC_SOURCES = {
 MEASURED_TRAFFIC = {
     "tiny": {"units": 26252,
              "fwd_tc_kernel": (195840 + 0, "6551394c778f6917"),
-             "bwd_tc_kernel": (345088 + 0, "d80b00f04b0affea")},
+             "bwd_tc_kernel": (346112 + 0, "11aa25c931f34327")},
     "star": {"units": 506117152,
              "fwd_tc_kernel": (94208000 + 27344384, "6551394c778f6917"),
-             "bwd_tc_kernel": (343944192 + 140833024, "d80b00f04b0affea")},
+             "bwd_tc_kernel": (344187648 + 141219840, "11aa25c931f34327")},
     "agent_small": {"units": 2424419552,
                     "fwd_tc_kernel": (202022144 + 100264960, "6551394c778f6917"),
-                    "bwd_tc_kernel": (2277282560 + 1094525696, "d80b00f04b0affea")},
+                    "bwd_tc_kernel": (2029278464 + 976820992, "11aa25c931f34327")},
     "long_small": {"units": 8211399552,
                    "fwd_tc_kernel": (336584704 + 232509952, "6551394c778f6917"),
-                   "bwd_tc_kernel": (12625401600 + 6598909184, "d80b00f04b0affea")},
+                   "bwd_tc_kernel": (11110119936 + 5870484224, "11aa25c931f34327")},
     "forest_small": {"units": 3793239488,
                      "fwd_tc_kernel": (499851008 + 303153920, "6551394c778f6917"),
-                     "bwd_tc_kernel": (3755256320 + 1951604992, "d80b00f04b0affea")},
+                     "bwd_tc_kernel": (3580061440 + 1836385792, "11aa25c931f34327")},
 }
 # Full-size workloads are not captured with more than the launch time: their traffic is the reduced
 # workload's of the same shape, scaled by the ratio of units (query heads x useful pairs).
@@ -138,7 +139,7 @@ def measured_traffic(config: str, kernel: str, units: int):
 
 def tile_efficiency(spc, plan, G: int, pairs: int) -> dict:
     """Useful pairs over the pairs the kernels compute (full 128-key blocks of 128-row tiles
-    forward; 64-row query blocks against 128-key blocks backward), per query head."""
+    forward; 64-row query blocks against the backward's merged 128-key blocks), per query head."""
     v = spc.sp_plan_view(plan)
     tt = int(v["tile_tokens"])
     fwd = 0
@@ -146,7 +147,8 @@ def tile_efficiency(spc, plan, G: int, pairs: int) -> dict:
         nb = sum((e - a + 127) // 128 for a, e in v["ranges"][rb:rb + rc].tolist())
         fwd += nb * 128 * tt
     tpb = 64 // G
-    bwd = sum(((q1 - q0 + tpb - 1) // tpb) * tpb * 128 for _, _, _, q0, q1 in v["bwd"].tolist())
+    bwd = sum(((q1 - q0 + tpb - 1) // tpb) * tpb * 128
+              for _, _, _, q0, q1 in spc.sp_plan_bwd_blocks(plan)["rows"].tolist())
     return {"fwd": round(pairs / max(fwd, 1), 4), "bwd": round(pairs / max(bwd, 1), 4)}
 
 

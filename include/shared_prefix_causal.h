@@ -128,6 +128,22 @@ SP_API int sp_tree_plan(const sp_tree_desc *tree, int32_t tile_tokens, int32_t k
 /* Fills *info with the plan's host tables.  Errors: SP_ERR_INVALID_ARG. */
 SP_API int sp_plan_view(const sp_plan *plan, sp_plan_info *info);
 
+/* The key blocks the bf16 backward runs (host copies, valid until
+ * sp_plan_destroy), built with the device tables (first upload or
+ * sp_plan_device_bytes; this call builds them too if needed).  The backward
+ * sums every branch's contribution into the prefix the branches share (#7914,
+ * introduction), so a block of keys walks the query run that sees them.  A
+ * segment's last, partial kv_block of keys is filled with the leading keys of
+ * the segments of its subtree that follow it in token order:
+ *   *rows     [*n_rows][5] = {seg of the first key, kv_start, kv_end,
+ *             q_begin = kv_start, q_end}, in launch order; every key of
+ *             [kv_start, kv_end) has q_end >= its own run end
+ *   *key_end  [total_tokens]: the end of each key's query run (the subtree end
+ *             of its segment); key j is seen by query i iff j <= i < key_end[j]
+ * Ownership stays with the plan.  Errors: SP_ERR_INVALID_ARG (null pointers),
+ * SP_ERR_UNSUPPORTED (as sp_plan_device_bytes). */
+SP_API int sp_plan_bwd_blocks(sp_plan *plan, const int32_t **rows, int32_t *n_rows, const int32_t **key_end);
+
 /* Copies the plan tables to device memory owned by the plan (a cudaMalloc on
  * the current device and an async copy on `stream`).  Must precede the first
  * attention call with this plan; repeat calls are no-ops.  The first upload

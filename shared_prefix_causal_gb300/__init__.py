@@ -76,6 +76,9 @@ _c_bwd = _sig("sp_tree_attn_bwd", ctypes.c_int,
               [_vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                _i32, _i32, _i32, _i32, ctypes.c_float, _vp, _vp])
 _c_plan_bytes = _sig("sp_plan_device_bytes", ctypes.c_size_t, [_vp])
+_c_plan_bwd_blocks = _sig("sp_plan_bwd_blocks", ctypes.c_int,
+                          [_vp, ctypes.POINTER(ctypes.POINTER(ctypes.c_int32)), ctypes.POINTER(ctypes.c_int32),
+                           ctypes.POINTER(ctypes.POINTER(ctypes.c_int32))])
 _c_plan_upload_to = _sig("sp_plan_upload_to", ctypes.c_int, [_vp, _vp, ctypes.c_size_t, _vp])
 _c_frag_plan = _sig("sp_fragment_plan", ctypes.c_int,
                     [ctypes.POINTER(_TreeDesc), ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)])
@@ -109,7 +112,8 @@ EXPORTED = ("sp_tree_plan", "sp_plan_view", "sp_plan_upload", "sp_plan_destroy",
             "sp_status_string", "sp_debug_wait_timeout", "sp_edge_gather_bwd_workspace_bytes", "sp_edge_gather_bwd",
             "sp_edge_logprob_workspace_bytes", "sp_edge_logprob", "sp_edge_logprob_bwd_workspace_bytes",
             "sp_edge_logprob_bwd", "sp_tree_attn_bwd_deterministic", "sp_fragment_plan", "sp_fragment_view",
-            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed", "sp_debug_cta_clock", "sp_tree_attn_fwd_paired")
+            "sp_fragment_destroy", "sp_plan_device_bytes", "sp_plan_upload_to", "sp_tree_attn_bwd_timed",
+            "sp_debug_cta_clock", "sp_tree_attn_fwd_paired", "sp_plan_bwd_blocks")
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -179,6 +183,20 @@ def sp_plan_view(plan: Plan) -> dict:
         "max_ranges_per_tile": info.max_ranges_per_tile,
         "tiles": arr(info.tiles, info.n_tiles, 5), "ranges": arr(info.ranges, info.n_ranges, 2),
         "bwd": arr(info.bwd, info.n_bwd, 5),
+    }
+
+
+def sp_plan_bwd_blocks(plan: Plan) -> dict:
+    """The key blocks the bf16 backward runs ([n][5], launch order) and every key's query-run end."""
+    rows, keys = ctypes.POINTER(ctypes.c_int32)(), ctypes.POINTER(ctypes.c_int32)()
+    n = ctypes.c_int32()
+    _check(_c_plan_bwd_blocks(plan.handle, ctypes.byref(rows), ctypes.byref(n), ctypes.byref(keys)),
+           "sp_plan_bwd_blocks")
+    T = int(sp_plan_view(plan)["total_tokens"])
+    return {
+        "rows": np.ctypeslib.as_array(rows, shape=(n.value * 5,)).reshape(n.value, 5).copy()
+        if n.value else np.zeros((0, 5), dtype=np.int32),
+        "key_end": np.ctypeslib.as_array(keys, shape=(T,)).copy() if T else np.zeros(0, dtype=np.int32),
     }
 
 

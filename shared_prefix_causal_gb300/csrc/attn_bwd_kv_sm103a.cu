@@ -128,10 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // key blocks in launch order, head_chunk KV heads at a time (as the
   // 64-row kernel): CTA b runs block (b mod span) / head_chunk of head chunk
   // b / span
-  const int span = head_chunk * plan.n_bwd;
+  const int span = head_chunk * plan.n_bwdm;
   const int item = (blockIdx.x % span) / head_chunk;
   const int g = (blockIdx.x / span) * head_chunk + blockIdx.x % head_chunk;
-  const int *blk = plan.bwd + 5 * size_t(item);
+  const int *blk = plan.bwdm + 5 * size_t(item);
   const int k0 = blk[1], k1 = blk[2], qb = blk[3], qe = blk[4];
   const int T = s.T;
   if (!(0 <= k0 && k0 < k1 && k1 - k0 <= kBK && qb == k0 && k1 <= qe && qe <= T)) {
@@ -318,15 +318,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
     const int key = k0 + r;
     const bool kvalid = key < k1;
+    // this key's own run end: a block may hold keys of segments of its first
+    // key's subtree, seen by fewer of the run's queries
+    const int key_qe = kvalid ? min(plan.key_end[key], qe) : qb;
     const float sl2 = s.scale * kLog2e;
     bool ok = true;
     for (int j = 0; j < nq; ++j) {
       const int ss = j % kStatSlots;
       const int qt = q_of(j);
       const float *stat = reinterpret_cast<const float *>(smem + L::STAT + ss * 2 * 128 * 4);
-      const bool nomask = qt + tps <= qe && qt >= k1 - 1;
-      const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
-      const int ql = qe - qt;
+      const bool nomask = qt + tps <= key_qe && qt >= k1 - 1;
+      const int kq = key - qt;  // column c is visible iff kq <= c / G and its token < key_qe
+      const int ql = key_qe - qt;  // tokens of this step inside this key's query run
       if (!(ok = ctl.wait_warp(B_ST_FULL + ss, (j / kStatSlots) & 1))) break;  // the step's statistics
       if (!(ok = ctl.wait_warp(B_S_FULL, j & 1))) break;
       tc_fence_after();
@@ -455,7 +458,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
     return SP_ERR_CUDA;
   CtaClock clk;
   cta_clock_for(kClockKeyBlocks, &clk.buf, &clk.cap);
-  const unsigned grid = unsigned(p.n_bwd) * unsigned(s.Hkv);
+  const unsigned grid = unsigned(p.n_bwdm) * unsigned(s.Hkv);
   if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return SP_ERR_CUDA;
   kern<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, p, s, lse, delta, static_cast<__nv_bfloat16 *>(dk),
                                      static_cast<__nv_bfloat16 *>(dv), d_status, head_chunk, clk);

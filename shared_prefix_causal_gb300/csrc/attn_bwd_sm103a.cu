@@ -122,10 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Key blocks in launch order (grouped by query-run end), head_chunk KV heads
   // at a time: CTA b runs block (b mod head_chunk*n_bwd) / head_chunk of head
   // chunk b / (head_chunk*n_bwd).
-  const int span = head_chunk * plan.n_bwd;
+  const int span = head_chunk * plan.n_bwdm;
   const int item = (blockIdx.x % span) / head_chunk;
   const int g = (blockIdx.x / span) * head_chunk + blockIdx.x % head_chunk;
-  const int *blk = plan.bwd + 5 * item;
+  const int *blk = plan.bwdm + 5 * item;
   const int k0 = blk[1], k1 = blk[2], qb = blk[3], qe = blk[4];
   const int T = s.T, Hq = s.Hq;
   if (!(0 <= k0 && k0 < k1 && k1 - k0 <= kBK && qb == k0 && k1 <= qe && qe <= T)) {
@@ -319,6 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(32 * (warp & 3)) << 16;
     const int key = k0 + r;
     const bool kvalid = key < k1;
+    // this key's own run end: a block may hold keys of segments of its first
+    // key's subtree, seen by fewer of the run's queries
+    const int key_qe = kvalid ? min(plan.key_end[key], qe) : qb;
     const float sl2 = s.scale * kLog2e;
     bool ok = true;
     // dQ^T of block m: TMEM lane d = head-dim index, 64 query columns; one
@@ -360,9 +363,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int pb = j & 1;
       const uint32_t prow = sbase + L::PS + pb * L::PS_BYTES + r * 128;
-      const bool nomask = qt + tpb <= qe && qt >= k1 - 1;
-      const int kq = key - qt;  // column c is visible iff kq <= c / G (and its token < qe)
-      const int ql = qe - qt;   // tokens of this block inside the query run
+      const bool nomask = qt + tpb <= key_qe && qt >= k1 - 1;
+      const int kq = key - qt;  // column c is visible iff kq <= c / G and its token < key_qe
+      const int ql = key_qe - qt;  // tokens of this block inside this key's query run
       uint32_t us[32], ud[32];
       tmem_ld32x2(tmem + lane_base + T_S + 32 * h, tmem + lane_base + T_DP + 32 * h, us, ud);
       tc_fence_before();
@@ -512,8 +515,8 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
 // blocks plus a fixed per-CTA cost.
 int bwd_head_chunk(const PlanDev &p, const AttnShape &s, int sms) {
   const double tpb = double(kBQ / s.G), fixed = 6.0;
-  const double total = double(p.bwd_run_sum) / tpb + fixed * p.n_bwd;
-  const double longest = double(p.bwd_run_max) / tpb + fixed;
+  const double total = double(p.bwdm_run_sum) / tpb + fixed * p.n_bwdm;
+  const double longest = double(p.bwdm_run_max) / tpb + fixed;
   for (int c = 1; c < s.Hkv; ++c)
     if (s.Hkv % c == 0 && c * total / double(sms) >= 2.0 * longest) return c;
   return s.Hkv;
@@ -551,7 +554,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   const int smem = Layout<D>::ALLOC;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return SP_ERR_CUDA;
-  const unsigned grid = unsigned(p.n_bwd) * unsigned(s.Hkv);
+  const unsigned grid = unsigned(p.n_bwdm) * unsigned(s.Hkv);
   if (ev_begin && cudaEventRecord(ev_begin, st) != cudaSuccess) return SP_ERR_CUDA;
   CtaClock clk;
   cta_clock_for(kClockKeyBlocks, &clk.buf, &clk.cap);

@@ -32,7 +32,8 @@ int check_tiling(const sp_plan &p, int32_t dtype, int32_t G) {
 
 spc::PlanDev plan_dev(const sp_plan &p) {
   return {p.d_tiles, p.d_ranges, p.d_bwd, p.n_tiles(), p.n_bwd(), p.tile_tokens, p.kv_block,
-          p.d_pairs, p.d_pblk, p.n_pairs(), p.bwd_run_sum, p.bwd_run_max, p.d_quads, p.d_qblk, p.n_quads()};
+          p.d_pairs, p.d_pblk, p.n_pairs(), p.bwd_run_sum, p.bwd_run_max, p.d_quads, p.d_qblk, p.n_quads(),
+          p.d_bwdm, p.n_bwdm(), p.bwdm_run_sum, p.bwdm_run_max, p.d_key_end};
 }
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -133,14 +134,15 @@ int prepare_device_tables(sp_plan *p) {
 }
 
 struct DeviceLayout {
-  size_t bt, br, bb, bp, bk, bq, bqk, total;
+  size_t bt, br, bb, bp, bk, bq, bqk, bm, be, total;
 };
 
 DeviceLayout device_layout(const sp_plan &p) {
-  DeviceLayout l{p.tiles.size() * 4, p.ranges.size() * 4, p.bwd.size() * 4, p.pairs.size() * 4,
-                 p.pblk.size() * 4, p.quads.size() * 4, p.qblk.size() * 4, 0};
+  DeviceLayout l{p.tiles.size() * 4, p.ranges.size() * 4, p.bwd.size() * 4,        p.pairs.size() * 4,
+                 p.pblk.size() * 4,  p.quads.size() * 4,  p.qblk.size() * 4,       p.bwd_merged.size() * 4,
+                 p.key_end.size() * 4, 0};
   l.total = align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp) + align_up(l.bk) + align_up(l.bq) +
-            align_up(l.bqk) + 256;
+            align_up(l.bqk) + align_up(l.bm) + align_up(l.be) + 256;
   return l;
 }
 
@@ -153,13 +155,17 @@ int copy_tables(sp_plan *p, char *base, const DeviceLayout &l, cudaStream_t st) 
   int32_t *dk = reinterpret_cast<int32_t *>(base + align_up(l.bt) + align_up(l.br) + align_up(l.bb) + align_up(l.bp));
   int32_t *dq = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dk) + align_up(l.bk));
   int32_t *dqk = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dq) + align_up(l.bq));
+  int32_t *dm = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dqk) + align_up(l.bqk));
+  int32_t *de = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(dm) + align_up(l.bm));
   if ((l.bt && cudaMemcpyAsync(dt, p->tiles.data(), l.bt, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.bq && cudaMemcpyAsync(dq, p->quads.data(), l.bq, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.bqk && cudaMemcpyAsync(dqk, p->qblk.data(), l.bqk, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.br && cudaMemcpyAsync(dr, p->ranges.data(), l.br, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.bb && cudaMemcpyAsync(db, p->bwd_sched.data(), l.bb, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
       (l.bp && cudaMemcpyAsync(dp, p->pairs.data(), l.bp, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
-      (l.bk && cudaMemcpyAsync(dk, p->pblk.data(), l.bk, cudaMemcpyHostToDevice, st) != cudaSuccess))
+      (l.bk && cudaMemcpyAsync(dk, p->pblk.data(), l.bk, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.bm && cudaMemcpyAsync(dm, p->bwd_merged.data(), l.bm, cudaMemcpyHostToDevice, st) != cudaSuccess) ||
+      (l.be && cudaMemcpyAsync(de, p->key_end.data(), l.be, cudaMemcpyHostToDevice, st) != cudaSuccess))
     return SP_ERR_CUDA;
   p->d_tiles = dt;
   p->d_ranges = dr;
@@ -168,6 +174,8 @@ int copy_tables(sp_plan *p, char *base, const DeviceLayout &l, cudaStream_t st) 
   p->d_pblk = dk;
   p->d_quads = l.bq ? dq : nullptr;
   p->d_qblk = l.bqk ? dqk : nullptr;
+  p->d_bwdm = l.bm ? dm : nullptr;
+  p->d_key_end = l.be ? de : nullptr;
   cudaGetDevice(&p->device);
   return SP_OK;
 }
@@ -185,7 +193,8 @@ int sp_plan_upload(sp_plan *p, void *stream) {
   char *base = nullptr;
   if (cudaMalloc(&base, l.total) != cudaSuccess) return SP_ERR_CUDA;
   if (copy_tables(p, base, l, st) != SP_OK || cudaStreamSynchronize(st) != cudaSuccess) {
-    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = p->d_quads = p->d_qblk = nullptr;
+    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = p->d_quads = p->d_qblk = p->d_bwdm =
+        p->d_key_end = nullptr;
     cudaFree(base);
     return SP_ERR_CUDA;
   }
@@ -198,6 +207,15 @@ size_t sp_plan_device_bytes(sp_plan *p) {
   return device_layout(*p).total;
 }
 
+int sp_plan_bwd_blocks(sp_plan *p, const int32_t **rows, int32_t *n_rows, const int32_t **key_end) {
+  if (!p || !rows || !n_rows || !key_end) return SP_ERR_INVALID_ARG;
+  if (int rc = prepare_device_tables(p)) return rc;
+  *rows = p->bwd_merged.data();
+  *n_rows = p->n_bwdm();
+  *key_end = p->key_end.data();
+  return SP_OK;
+}
+
 int sp_plan_upload_to(sp_plan *p, void *device_buffer, size_t buffer_bytes, void *stream) {
   if (!p || !device_buffer) return SP_ERR_INVALID_ARG;
   if (p->d_tiles) return SP_OK;
@@ -206,7 +224,8 @@ int sp_plan_upload_to(sp_plan *p, void *device_buffer, size_t buffer_bytes, void
   const DeviceLayout l = device_layout(*p);
   if (buffer_bytes < l.total) return SP_ERR_WORKSPACE;
   if (int rc = copy_tables(p, static_cast<char *>(device_buffer), l, static_cast<cudaStream_t>(stream))) {
-    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = p->d_quads = p->d_qblk = nullptr;
+    p->d_tiles = p->d_ranges = p->d_bwd = p->d_pairs = p->d_pblk = p->d_quads = p->d_qblk = p->d_bwdm =
+        p->d_key_end = nullptr;
     return rc;
   }
   p->owns_device = false;

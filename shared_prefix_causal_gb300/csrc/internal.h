@@ -28,9 +28,16 @@ struct sp_plan {
   std::vector<int32_t> bwd_sched;  // [k][5]
   int64_t bwd_run_sum = 0;
   int32_t bwd_run_max = 0;
+  // key blocks of the tensor-core backward (built at upload; see
+  // build_bwd_merged), in the same launch order, their runs' sum and maximum,
+  // and every key's own query-run end [total_tokens]
+  std::vector<int32_t> bwd_merged;  // [m][5]
+  int64_t bwdm_run_sum = 0;
+  int32_t bwdm_run_max = 0;
+  std::vector<int32_t> key_end;
   // device copies (owned), valid after sp_plan_upload
   int32_t *d_tiles = nullptr, *d_ranges = nullptr, *d_bwd = nullptr, *d_pairs = nullptr, *d_pblk = nullptr,
-          *d_quads = nullptr, *d_qblk = nullptr;
+          *d_quads = nullptr, *d_qblk = nullptr, *d_bwdm = nullptr, *d_key_end = nullptr;
   int device = -1;
   bool owns_device = false;  // the device tables were allocated by sp_plan_upload
   int32_t n_tiles() const { return int32_t(tiles.size() / 5); }
@@ -38,6 +45,7 @@ struct sp_plan {
   int32_t n_bwd() const { return int32_t(bwd.size() / 5); }
   int32_t n_pairs() const { return int32_t(pairs.size() / 4); }
   int32_t n_quads() const { return int32_t(quads.size() / 6); }
+  int32_t n_bwdm() const { return int32_t(bwd_merged.size() / 5); }
 };
 
 namespace spc {
@@ -49,8 +57,13 @@ int validate_tree(const sp_tree_desc &tree);
 int build_plan(const sp_tree_desc &tree, int32_t tile_tokens, int32_t kv_block, int32_t order,
                sp_plan &plan);
 // Backward launch order (see sp_plan::bwd_sched): rows grouped by the end of
-// their query run, latest first, longest run first within a group.
+// their query run, latest first, longest run first within a group; also
+// builds the merged key blocks (build_bwd_merged).
 void build_bwd_schedule(sp_plan &plan);
+// The tensor-core backward's key blocks (sp_plan::bwd_merged, key_end): a
+// segment's partial last block filled with the leading keys of the segments
+// of its subtree that follow it.
+void build_bwd_merged(sp_plan &plan);
 // Forward pairs and merged block lists from the tiles (see sp_plan::pairs).
 void build_pairs(sp_plan &plan, int32_t block_keys);
 // Paired-SM forward quads and their merged block lists (see sp_plan::quads).
@@ -80,6 +93,13 @@ struct PlanDev {
   const int32_t *quads;
   const int32_t *qblk;
   int32_t n_quads;
+  // the tensor-core backward's merged key blocks [n_bwdm][5] (launch order),
+  // their runs' sum and maximum, and every key's query-run end [T]
+  const int32_t *bwdm;
+  int32_t n_bwdm;
+  int64_t bwdm_run_sum;
+  int32_t bwdm_run_max;
+  const int32_t *key_end;
 };
 
 // Kernels whose CTAs can record their start and end times (sp_debug_cta_clock).

@@ -344,6 +344,64 @@ void build_bwd_schedule(sp_plan &plan) {
     plan.bwd_run_sum += len(i);
     plan.bwd_run_max = std::max(plan.bwd_run_max, len(i));
   }
+  build_bwd_merged(plan);
+}
+
+// Key blocks of the tensor-core backward.  A segment's last block is usually
+// partial, yet it walks the segment's whole query run with all kv_block rows.
+// Walking the keys in token order, such a block takes in the leading keys of
+// the segments that follow it while they lie in its segment's subtree (their
+// run end is at most the block's), so rows that would compute nothing work on
+// the same query run; a segment whose leading keys were taken has its
+// remaining keys blocked from there on.  The block's run is still
+// [first key, subtree end of its first key's segment), and every key keeps
+// its own run end in key_end, which the kernels mask with.  Rows {seg of the
+// first key, first key, end key, first key, run end}, in the launch order of
+// bwd_sched.
+void build_bwd_merged(sp_plan &plan) {
+  const int32_t n = plan.n_bwd(), B = plan.kv_block, T = plan.total_tokens;
+  const int32_t *b = plan.bwd.data();
+  plan.key_end.assign(size_t(std::max(T, 0)), 0);
+  for (int32_t i = 0; i < n; ++i)
+    for (int32_t k = b[5 * i + 1]; k < b[5 * i + 2]; ++k) plan.key_end[size_t(k)] = b[5 * i + 4];
+  std::vector<int32_t> order(n);  // canonical rows by first key
+  std::iota(order.begin(), order.end(), 0);
+  std::sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return b[5 * x + 1] < b[5 * y + 1]; });
+  std::vector<int32_t> from(n);  // first key of each row not yet placed
+  for (int32_t i = 0; i < n; ++i) from[i] = b[5 * i + 1];
+  std::vector<int32_t> rows;
+  for (int32_t oi = 0; oi < n; ++oi) {
+    const int32_t i = order[oi];
+    const int32_t k0 = from[i], qe = b[5 * i + 4];
+    int32_t k1 = b[5 * i + 2];
+    if (k0 >= k1) continue;  // taken in whole by an earlier block
+    for (int32_t oj = oi + 1; oj < n && k1 - k0 < B; ++oj) {
+      const int32_t j = order[oj];
+      if (from[j] != k1 || b[5 * j + 4] > qe) break;  // not contiguous, or outside the subtree
+      const int32_t take = std::min(B - (k1 - k0), b[5 * j + 2] - from[j]);
+      from[j] += take;
+      k1 += take;
+      if (from[j] < b[5 * j + 2]) break;
+    }
+    rows.insert(rows.end(), {b[5 * i], k0, k1, k0, qe});
+  }
+  const int32_t m = int32_t(rows.size() / 5);
+  std::vector<int32_t> idx(m);
+  std::iota(idx.begin(), idx.end(), 0);
+  auto len = [&](int32_t i) { return rows[5 * size_t(i) + 4] - rows[5 * size_t(i) + 3]; };
+  std::sort(idx.begin(), idx.end(), [&](int32_t x, int32_t y) {
+    if (rows[5 * size_t(x) + 4] != rows[5 * size_t(y) + 4]) return rows[5 * size_t(x) + 4] > rows[5 * size_t(y) + 4];
+    if (len(x) != len(y)) return len(x) > len(y);
+    return rows[5 * size_t(x) + 1] < rows[5 * size_t(y) + 1];
+  });
+  plan.bwd_merged.clear();
+  plan.bwdm_run_sum = 0;
+  plan.bwdm_run_max = 0;
+  for (int32_t i : idx) {
+    plan.bwd_merged.insert(plan.bwd_merged.end(), rows.begin() + 5 * size_t(i), rows.begin() + 5 * size_t(i) + 5);
+    plan.bwdm_run_sum += len(i);
+    plan.bwdm_run_max = std::max(plan.bwdm_run_max, len(i));
+  }
 }
 
 }  // namespace spc

@@ -27,15 +27,17 @@ SP_API void shim_device_tables(void *h) {
 
 SP_API int64_t shim_bwd_run_sum(void *h) { return static_cast<const sp_plan *>(h)->bwd_run_sum; }
 SP_API int32_t shim_bwd_run_max(void *h) { return static_cast<const sp_plan *>(h)->bwd_run_max; }
+SP_API int64_t shim_bwdm_run_sum(void *h) { return static_cast<const sp_plan *>(h)->bwdm_run_sum; }
+SP_API int32_t shim_bwdm_run_max(void *h) { return static_cast<const sp_plan *>(h)->bwdm_run_max; }
 
 // which: 0 tiles [n][5], 1 ranges [n][2], 2 bwd [n][5], 3 pairs [n][4],
-// 4 pblk [n][8], 5 bwd_sched [n][5], 6 quads [n][6], 7 qblk [n][8]; returns
-// the row count
+// 4 pblk [n][8], 5 bwd_sched [n][5], 6 quads [n][6], 7 qblk [n][8],
+// 8 bwd_merged [n][5], 9 key_end [n][1]; returns the row count
 SP_API int32_t shim_rows(void *h, int32_t which, const int32_t **data) {
   const sp_plan *p = static_cast<const sp_plan *>(h);
-  static const int width[8] = {5, 2, 5, 4, 8, 5, 6, 8};
-  const std::vector<int32_t> *tables[8] = {&p->tiles, &p->ranges, &p->bwd,       &p->pairs,
-                                           &p->pblk,  &p->bwd_sched, &p->quads, &p->qblk};
+  static const int width[10] = {5, 2, 5, 4, 8, 5, 6, 8, 5, 1};
+  const std::vector<int32_t> *tables[10] = {&p->tiles, &p->ranges,    &p->bwd,   &p->pairs,      &p->pblk,
+                                            &p->bwd_sched, &p->quads, &p->qblk, &p->bwd_merged, &p->key_end};
   const std::vector<int32_t> &v = *tables[which];
   *data = v.data();
   return int32_t(v.size() / width[which]);

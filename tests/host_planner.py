@@ -48,6 +48,10 @@ class Host:
         self.lib.shim_bwd_run_sum.argtypes = [ctypes.c_void_p]
         self.lib.shim_bwd_run_max.restype = ctypes.c_int32
         self.lib.shim_bwd_run_max.argtypes = [ctypes.c_void_p]
+        self.lib.shim_bwdm_run_sum.restype = ctypes.c_int64
+        self.lib.shim_bwdm_run_sum.argtypes = [ctypes.c_void_p]
+        self.lib.shim_bwdm_run_max.restype = ctypes.c_int32
+        self.lib.shim_bwdm_run_max.argtypes = [ctypes.c_void_p]
         self.lib.sp_fragment_plan.argtypes = [ctypes.POINTER(_Desc), ctypes.c_int64, ctypes.POINTER(ctypes.c_void_p)]
         self.lib.sp_fragment_view.argtypes = [ctypes.c_void_p, ctypes.POINTER(_FragInfo)]
         self.lib.sp_fragment_destroy.argtypes = [ctypes.c_void_p]
@@ -76,16 +80,19 @@ class Host:
 
     def device_tables(self, st, ln, par, dep, tile, kvb, order):
         """The plan and the tables its first upload builds: a dict of tiles, ranges, bwd, pairs, pblk,
-        bwd_sched, quads, qblk, run_sum and run_max, or the status of a refused call."""
+        bwd_sched, quads, qblk, bwd_merged, key_end, run_sum, run_max, runm_sum and runm_max, or the
+        status of a refused call."""
         d, keep = self._desc(st, ln, par, dep)
         rc = ctypes.c_int32()
         h = self.lib.shim_plan(ctypes.byref(d), tile, kvb, order, ctypes.byref(rc))
         if rc.value:
             return rc.value
         self.lib.shim_device_tables(h)
-        names = ("tiles", "ranges", "bwd", "pairs", "pblk", "bwd_sched", "quads", "qblk")
-        out = {n: self._rows(h, i, w) for i, (n, w) in enumerate(zip(names, (5, 2, 5, 4, 8, 5, 6, 8)))}
+        names = ("tiles", "ranges", "bwd", "pairs", "pblk", "bwd_sched", "quads", "qblk", "bwd_merged", "key_end")
+        out = {n: self._rows(h, i, w) for i, (n, w) in enumerate(zip(names, (5, 2, 5, 4, 8, 5, 6, 8, 5, 1)))}
+        out["key_end"] = out["key_end"].reshape(-1)
         out["run_sum"], out["run_max"] = int(self.lib.shim_bwd_run_sum(h)), int(self.lib.shim_bwd_run_max(h))
+        out["runm_sum"], out["runm_max"] = int(self.lib.shim_bwdm_run_sum(h)), int(self.lib.shim_bwdm_run_max(h))
         self.lib.shim_free(h)
         return out
 

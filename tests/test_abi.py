@@ -150,6 +150,27 @@ def test_upload_refuses_plans_whose_forward_block_lists_could_overflow():
     assert spc.sp_plan_device_bytes(spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 128, 128, 0)) > 0
 
 
+def test_merged_backward_blocks_through_the_binding():
+    """sp_plan_bwd_blocks on the CPU (no upload needed): the tiny tree's six canonical key blocks
+    become three, every key once, each block's run that of its first key; null pointers refused."""
+    t = W.tiny().tree
+    p = spc.sp_tree_plan(t.seg_start, t.seg_len, t.parent, t.depth, 32, 128, 0)
+    m, v = spc.sp_plan_bwd_blocks(p), spc.sp_plan_view(p)
+    rows, key_end = m["rows"], m["key_end"]
+    assert len(v["bwd"]) == 6 and len(rows) == 3
+    seen = np.zeros(t.total_tokens, dtype=np.int64)
+    for seg, k0, k1, q0, q1 in rows.tolist():
+        assert q0 == k0 and q1 == key_end[k0] and (key_end[k0:k1] <= q1).all()
+        seen[k0:k1] += 1
+    assert (seen == 1).all()
+    for seg, k0, k1, q0, q1 in v["bwd"].tolist():
+        assert (key_end[k0:k1] == q1).all()
+    out = ctypes.POINTER(ctypes.c_int32)()
+    n = ctypes.c_int32()
+    assert spc._c_plan_bwd_blocks(p.handle, None, ctypes.byref(n), ctypes.byref(out)) == -2
+    assert spc._c_plan_bwd_blocks(None, ctypes.byref(out), ctypes.byref(n), ctypes.byref(out)) == -2
+
+
 def test_plan_rejects_bad_arguments():
     a = _desc(W.tiny().tree)
     for tt, kb, order in ((0, 128, 0), (32, 0, 0), (32, 128, 2)):

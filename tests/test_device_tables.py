@@ -10,6 +10,12 @@ list and the backward's launch order:
     non-zero, and only keys j <= its query i when bit t is set;
   * bwd_sched: the backward table's rows in launch order (latest run end
     first, longest run first within a run end), with the runs' sum and maximum.
+  * bwd_merged, key_end: the tensor-core backward's key blocks, in the same
+    launch order.  Every key is in exactly one block; a block walks the query
+    run [first key, run end of its first key) and each of its keys is masked
+    with its own run end key_end (the subtree end of its segment), never past
+    the block's.  A block of fewer than 128 keys ends where the next key
+    belongs to no segment of its first key's subtree.
   * quads [n][6] = {a0, a1, b0, b1 (or -1), first entry, entry count}: the
     paired-SM forward's work items.  A couple (a0, a1) or (b0, b1) is two
     consecutive tiles of one segment (offsets 2i and 2i + 1; a segment's last
@@ -128,6 +134,33 @@ def check_device_tables(T, d):
             if runs[i] == runs[i + 1]:
                 assert sched[i, 1] < sched[i + 1, 1], "ties not in canonical order"
     assert d["run_sum"] == int(runs.sum()) and d["run_max"] == (int(runs.max()) if len(runs) else 0)
+    check_merged_blocks(T, d)
+
+
+def check_merged_blocks(T, d):
+    """bwd_merged and key_end against the canonical table and the reading above."""
+    bwd, rows, key_end = d["bwd"], d["bwd_merged"], d["key_end"]
+    want_end = np.zeros(T, dtype=np.int64)
+    seg_of = np.zeros(T, dtype=np.int64)
+    for seg, k0, k1, q0, q1 in bwd.tolist():
+        want_end[k0:k1] = q1
+        seg_of[k0:k1] = seg
+    assert key_end.shape == (T,) and (key_end == want_end).all(), "a key's run end is off"
+    seen = np.zeros(T, dtype=np.int64)
+    for seg, k0, k1, q0, q1 in rows.tolist():
+        assert 0 <= k0 < k1 <= T and k1 - k0 <= BLOCK and q0 == k0, "malformed block"
+        assert q1 == key_end[k0] and seg == seg_of[k0], "a block's run is not its first key's"
+        assert (key_end[k0:k1] <= q1).all(), "a key seen past its block's run"
+        if k1 - k0 < BLOCK and k1 < T:
+            assert key_end[k1] > q1, "a partial block stops before the end of its subtree's keys"
+        seen[k0:k1] += 1
+    assert (seen == 1).all(), "keys not covered exactly once"
+    runs = rows[:, 4] - rows[:, 3]
+    for i in range(len(rows) - 1):
+        a, b = rows[i], rows[i + 1]
+        assert a[4] > b[4] or (a[4] == b[4] and (runs[i] > runs[i + 1] or (runs[i] == runs[i + 1] and a[1] < b[1]))), \
+            "merged blocks not in launch order"
+    assert d["runm_sum"] == int(runs.sum()) and d["runm_max"] == (int(runs.max()) if len(runs) else 0)
 
 
 def _check_entries(tiles, ranges, ent, col, t, bit):
@@ -310,6 +343,11 @@ def test_the_checks_catch_broken_tables(host):
         lambda d: d["qblk"].__setitem__((0, 2), d["qblk"][0, 2] - 1),        # a quad's block end cut short
         lambda d: d["quads"].__setitem__((0, 5), d["quads"][0, 5] - 1),      # a run dropped from a quad
         lambda d: d["quads"].__setitem__((0, 1), d["quads"][0, 2]),          # a couple of two segments
+        lambda d: d["key_end"].__setitem__(0, d["key_end"][0] + 1),          # a key's run end off by one
+        lambda d: d["bwd_merged"].__setitem__((0, 4), d["bwd_merged"][0, 4] - 1),  # a block's run cut short
+        lambda d: d["bwd_merged"].__setitem__(slice(None), d["bwd_merged"][::-1].copy()),  # order reversed
+        lambda d: d.__setitem__("runm_sum", d["runm_sum"] + 1),
+        lambda d: d.__setitem__("bwd_merged", d["bwd_sched"].copy()),       # partial blocks left unfilled
     ]
     for brk in breaks:
         bad = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in good.items()}
