@@ -460,19 +460,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Delta = rowsum(dO * O) per (token, query head) in fp32, and zero the fp32
-// dQ workspace (when there is one).  One warp per row; 16-byte loads.
+// dQ workspace (when there is one).  A row of D values is read by D / 8 lanes
+// with 16-byte loads, so a warp takes 256 / D rows at once and every lane loads.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
                                                       const __nv_bfloat16 *__restrict__ d_o,
                                                       float *__restrict__ delta, float *__restrict__ dqacc, int T,
                                                       int Hq) {
-  const int lane = threadIdx.x & 31;
+  constexpr int kLanes = D / 8;            // lanes per row
+  constexpr int kRowsPerWarp = 32 / kLanes;
+  const int lane = threadIdx.x & 31, sub = lane / kLanes, part = lane % kLanes;
   const long rows = long(T) * Hq;
-  for (long row = (long(blockIdx.x) * 256 + threadIdx.x) / 32; row < rows; row += long(gridDim.x) * 8) {
+  const long warp0 = (long(blockIdx.x) * 256 + threadIdx.x) / 32, warps = long(gridDim.x) * 8;
+  for (long row0 = warp0 * kRowsPerWarp; row0 < rows; row0 += warps * kRowsPerWarp) {
+    const long row = row0 + sub;
+    const bool live = row < rows;
     float acc = 0.f;
-    if (lane * 8 < D) {
-      const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + lane * 8);
-      const uint4 b = *reinterpret_cast<const uint4 *>(d_o + row * D + lane * 8);
+    if (live) {
+      const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
+      const uint4 b = *reinterpret_cast<const uint4 *>(d_o + row * D + part * 8);
       const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
       const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
 #pragma unroll
@@ -481,14 +487,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__res
         acc = fmaf(x.x, y.x, acc);
         acc = fmaf(x.y, y.y, acc);
       }
+      if (dqacc) {
+        float4 *z = reinterpret_cast<float4 *>(dqacc + row * D) + 2 * part;
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
 #pragma unroll
-    for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (dqacc) {
-      float4 *z = reinterpret_cast<float4 *>(dqacc + row * D);
-      for (int c = lane; c < D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (lane == 0) delta[size_t(row % Hq) * T + row / Hq] = acc;
+    for (int off = kLanes / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && part == 0) delta[size_t(row % Hq) * T + row / Hq] = acc;
   }
 }
 
