@@ -130,7 +130,8 @@ SP_API int sp_plan_view(const sp_plan *plan, sp_plan_info *info);
 
 /* The key blocks the bf16 backward runs (host copies, valid until
  * sp_plan_destroy), built with the device tables (first upload or
- * sp_plan_device_bytes; this call builds them too if needed).  The backward
+ * sp_plan_device_bytes; this call builds them too if needed, so it falls
+ * under the same rule: one thread makes the first of these calls).  The backward
  * sums every branch's contribution into the prefix the branches share (#7914,
  * introduction), so a block of keys walks the query run that sees them.  A
  * segment's last, partial kv_block of keys is filled with the leading keys of
