@@ -34,8 +34,9 @@
 // released by warp 10 after the products that read it last), so no ordering
 // between the two threads' products is needed.
 //
-// Companion kernels: bwd_pre (Delta = rowsum(dO * O) and zeroing the fp32 dQ
-// workspace) and dq_convert (scale and round dQ to bf16).
+// Companion kernels (attn_bwd_pre_sm103a.cu): bwd_pre (Delta = rowsum(dO * O)
+// and zeroing the fp32 dQ workspace) and dq_convert (scale and round dQ to
+// bf16).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -459,61 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   clk.end(clk0);
 }
 
-// Delta = rowsum(dO * O) per (token, query head) in fp32, and zero the fp32
-// dQ workspace (when there is one).  A row of D values is read by D / 8 lanes
-// with 16-byte loads, so a warp takes 256 / D rows at once and every lane loads.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16 *__restrict__ o,
-                                                      const __nv_bfloat16 *__restrict__ d_o,
-                                                      float *__restrict__ delta, float *__restrict__ dqacc, int T,
-                                                      int Hq) {
-  constexpr int kLanes = D / 8;            // lanes per row
-  constexpr int kRowsPerWarp = 32 / kLanes;
-  const int lane = threadIdx.x & 31, sub = lane / kLanes, part = lane % kLanes;
-  const long rows = long(T) * Hq;
-  const long warp0 = (long(blockIdx.x) * 256 + threadIdx.x) / 32, warps = long(gridDim.x) * 8;
-  for (long row0 = warp0 * kRowsPerWarp; row0 < rows; row0 += warps * kRowsPerWarp) {
-    const long row = row0 + sub;
-    const bool live = row < rows;
-    float acc = 0.f;
-    if (live) {
-      const uint4 a = *reinterpret_cast<const uint4 *>(o + row * D + part * 8);
-      const uint4 b = *reinterpret_cast<const uint4 *>(d_o + row * D + part * 8);
-      const __nv_bfloat162 *pa = reinterpret_cast<const __nv_bfloat162 *>(&a);
-      const __nv_bfloat162 *pb = reinterpret_cast<const __nv_bfloat162 *>(&b);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 x = __bfloat1622float2(pa[i]), y = __bfloat1622float2(pb[i]);
-        acc = fmaf(x.x, y.x, acc);
-        acc = fmaf(x.y, y.y, acc);
-      }
-      if (dqacc) {
-        float4 *z = reinterpret_cast<float4 *>(dqacc + row * D) + 2 * part;
-        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-#pragma unroll
-    for (int off = kLanes / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && part == 0) delta[size_t(row % Hq) * T + row / Hq] = acc;
-  }
-}
-
-// dq = bf16(scale * dqacc), 8 elements per thread per step.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ dqacc,
-                                                         __nv_bfloat16 *__restrict__ dq, float scale, long n8) {
-  for (long i = long(blockIdx.x) * 256 + threadIdx.x; i < n8; i += long(gridDim.x) * 256) {
-    const float4 a = reinterpret_cast<const float4 *>(dqacc)[2 * i];
-    const float4 b = reinterpret_cast<const float4 *>(dqacc)[2 * i + 1];
-    uint4 w;
-    w.x = pack_bf16(a.x * scale, a.y * scale);
-    w.y = pack_bf16(a.z * scale, a.w * scale);
-    w.z = pack_bf16(b.x * scale, b.y * scale);
-    w.w = pack_bf16(b.z * scale, b.w * scale);
-    reinterpret_cast<uint4 *>(dq)[i] = w;
-  }
-}
-
 // How many KV heads' key blocks run together.  Fewer heads in flight means
 // fewer distinct Q/dO/dQ rows, so CTAs walking the same query run share them
 // through L2; but a chunk must hold enough work that its longest query run does
@@ -537,11 +483,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long rows = long(s.T) * s.Hq;
-  const int pre_grid = int(std::min<long>((rows + 7) / 8, long(sms) * 16));
-  bwd_pre_kernel<D><<<pre_grid, 256, 0, st>>>(static_cast<const __nv_bfloat16 *>(o),
-                                               static_cast<const __nv_bfloat16 *>(d_o), delta,
-                                               deterministic ? nullptr : dqacc, s.T, s.Hq);
-  if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
+  if (int rc0 = bwd_pre(s, o, d_o, delta, deterministic ? nullptr : dqacc, sms, st)) return rc0;
 
   CUtensorMap tq, tdo, tk, tv;
   int rc = encode_bf16_3d(&tq, q, D, s.Hq, s.T, 64, G, kBQ / G);
@@ -570,10 +512,7 @@ int launch(const PlanDev &p, const AttnShape &s, const void *q, const void *k, c
   if (cudaGetLastError() != cudaSuccess) return SP_ERR_CUDA;
   if (ev_end && cudaEventRecord(ev_end, st) != cudaSuccess) return SP_ERR_CUDA;
 
-  const long n8 = rows * D / 8;
-  const int cgrid = int(std::min<long>((n8 + 255) / 256, long(sms) * 16));
-  dq_convert_kernel<<<cgrid, 256, 0, st>>>(dqacc, static_cast<__nv_bfloat16 *>(dq), s.scale, n8);
-  return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+  return dq_convert(dqacc, dq, s.scale, rows * D, sms, st);
 }
 
 }  // namespace

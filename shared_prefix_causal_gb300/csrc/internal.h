@@ -134,6 +134,12 @@ int tc_fwd_pair(const PlanDev &p, const AttnShape &s, const void *q, const void 
 int tc_bwd(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const void *o,
            const float *lse, const void *d_o, void *dq, void *dk, void *dv, float *delta, float *dqacc,
            bool deterministic, int32_t *d_status, void *stream, void *ev_begin = nullptr, void *ev_end = nullptr);
+// The default backward's companion passes (attn_bwd_pre_sm103a.cu): Delta =
+// rowsum(dO * O) into delta [Hq][T], and zeroing dqacc [T][Hq][D] unless it
+// is null; then dq = bf16(scale * dqacc) over n = T * Hq * D values (n % 8 == 0).
+int bwd_pre(const AttnShape &s, const void *o, const void *d_o, float *delta, float *dqacc, int sms,
+            void *stream);
+int dq_convert(const float *dqacc, void *dq, float scale, long n, int sms, void *stream);
 // dK and dV only, 128 query rows per step (attn_bwd_kv_sm103a.cu), for the
 // deterministic backward; events as tc_bwd.
 int tc_bwd_kv(const PlanDev &p, const AttnShape &s, const void *q, const void *k, const void *v, const float *lse,
