@@ -57,19 +57,19 @@ TRAFFIC_SOURCES = {
 MEASURED_TRAFFIC = {
     "tiny": {"units": 26252,
              "fwd_tc_kernel": (195840 + 0, "6551394c778f6917"),
-             "bwd_tc_kernel": (346112 + 0, "11aa25c931f34327")},
+             "bwd_tc_kernel": (346624 + 0, "2a5e1bb63e8773c4")},
     "star": {"units": 506117152,
              "fwd_tc_kernel": (94208000 + 27344384, "6551394c778f6917"),
-             "bwd_tc_kernel": (344187648 + 141219840, "11aa25c931f34327")},
+             "bwd_tc_kernel": (345844224 + 142123520, "2a5e1bb63e8773c4")},
     "agent_small": {"units": 2424419552,
                     "fwd_tc_kernel": (202022144 + 100264960, "6551394c778f6917"),
-                    "bwd_tc_kernel": (2029278464 + 976820992, "11aa25c931f34327")},
+                    "bwd_tc_kernel": (2019589120 + 981808384, "2a5e1bb63e8773c4")},
     "long_small": {"units": 8211399552,
                    "fwd_tc_kernel": (336584704 + 232509952, "6551394c778f6917"),
-                   "bwd_tc_kernel": (11110119936 + 5870484224, "11aa25c931f34327")},
+                   "bwd_tc_kernel": (9595139840 + 5118466560, "2a5e1bb63e8773c4")},
     "forest_small": {"units": 3793239488,
                      "fwd_tc_kernel": (499851008 + 303153920, "6551394c778f6917"),
-                     "bwd_tc_kernel": (3580061440 + 1836385792, "11aa25c931f34327")},
+                     "bwd_tc_kernel": (3449080064 + 1793794560, "2a5e1bb63e8773c4")},
 }
 # Full-size workloads are not captured with more than the launch time: their traffic is the reduced
 # workload's of the same shape, scaled by the ratio of units (query heads x useful pairs).
