@@ -483,6 +483,27 @@ def test_sibling_permutation_gpu(name):
     assert np.abs(out2["lse"][:, perm] - out["lse"]).max() < 5e-3
 
 
+def test_merged_key_blocks_match_the_oracle():
+    """The bf16 backward's merged key blocks (a segment's partial last block filled with the leading
+    keys of its subtree's next segments, each key masked with its own run end), default and
+    deterministic, against the fp64 oracle on whole tensors: a hand-made tree whose root's last
+    block takes in four segments with three different run ends, and random trees of short segments."""
+    rng = np.random.default_rng(41)
+    trees = [W.tree_from_preorder([130, 5, 7, 50, 20, 300], [-1, 0, 1, 0, 0, -1])]
+    trees += [W.random_small_tree(rng, max_segments=30, max_len=200) for _ in range(3)]
+    for i, tr in enumerate(trees):
+        w = W.Workload("merged", "", tr, 8, 2, 128, 0.5, 23 + i, None, None)
+        plan = spc.tree_plan(tr, 32, 128, 0, upload=False)
+        merged = spc.sp_plan_bwd_blocks(plan)["rows"]
+        assert len(merged) < len(spc.sp_plan_view(plan)["bwd"])  # some block took in other segments' keys
+        if i == 0:  # the root's last block: its 2 keys, then 5 + 7 + 50 + 20 of its subtree
+            assert [128, 212] in merged[:, 1:3].tolist()
+        x = W.draw_tensors(w, "bf16")
+        for det in (False, True):
+            _, out = run_gpu(w, "bf16", x=x, deterministic=det)
+            check_full(w, x, out, "bf16")
+
+
 @pytest.mark.parametrize("hq,hkv,d", [(4, 2, 128), (4, 2, 64), (8, 1, 64), (2, 2, 128)])
 def test_gqa_and_head_dim_sweep(hq, hkv, d):
     """Every GQA ratio and head_dim the kernels instantiate, default and deterministic backward."""
