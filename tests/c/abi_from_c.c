@@ -69,6 +69,19 @@ int main(void) {
     const int32_t *b = info.bwd + 5 * i;
     printf("B %d %d %d %d %d\n", b[0], b[1], b[2], b[3], b[4]);
   }
+  if (rc == SP_OK) {
+    const int32_t *rows = NULL, *key_end = NULL;
+    int32_t n_rows = 0;
+    if (sp_plan_bwd_blocks(NULL, &rows, &n_rows, &key_end) != SP_ERR_INVALID_ARG) return fail("null bwd blocks");
+    if (sp_plan_bwd_blocks(p, &rows, &n_rows, &key_end) != SP_OK) return fail("bwd blocks");
+    for (int i = 0; i < n_rows; ++i) {
+      const int32_t *b = rows + 5 * i;
+      printf("M %d %d %d %d %d\n", b[0], b[1], b[2], b[3], b[4]);
+    }
+    printf("E");
+    for (int i = 0; i < info.total_tokens; ++i) printf(" %d", key_end[i]);
+    printf("\n");
+  }
   sp_plan_destroy(p);
 
   sp_fragments *fr = NULL;

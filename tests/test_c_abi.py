@@ -42,10 +42,10 @@ def _run(exe, tree, tile, kvb, order, cap):
     lines = [str(n)] + [f"{int(tree.seg_start[s])} {int(tree.seg_len[s])} {int(tree.parent[s])} {int(tree.depth[s])}"
                         for s in range(n)] + [f"{tile} {kvb} {order} {cap}"]
     out = subprocess.run([exe], input="\n".join(lines) + "\n", capture_output=True, text=True, check=True).stdout
-    got = {"T": [], "R": [], "B": [], "O": [], "F": []}
+    got = {"T": [], "R": [], "B": [], "O": [], "F": [], "M": [], "E": []}
     for line in out.splitlines():
         tag, *vals = line.split()
-        if tag in ("plan", "frag"):
+        if tag in ("plan", "frag", "E"):
             got[tag] = [int(x) for x in vals]
         else:
             got[tag].append([int(x) for x in vals])
@@ -62,6 +62,14 @@ def _check(got, t, tile, kvb, order, cap):
     assert np.array_equal(np.array(got["T"], dtype=np.int32).reshape(-1, 5), tiles)
     assert np.array_equal(np.array(got["R"], dtype=np.int32).reshape(-1, 2), ranges)
     assert np.array_equal(np.array(got["B"], dtype=np.int32).reshape(-1, 5), bwd)
+    # the merged backward key blocks read through sp_plan_bwd_blocks, held to their reading
+    # against the oracle's canonical table
+    from test_device_tables import check_merged_blocks
+    rows = np.array(got["M"], dtype=np.int64).reshape(-1, 5)
+    runs = rows[:, 4] - rows[:, 3]
+    check_merged_blocks(int(t.seg_len.sum()), {"bwd": bwd, "bwd_merged": rows, "key_end": np.array(got["E"]),
+                                               "runm_sum": int(runs.sum()),
+                                               "runm_max": int(runs.max()) if len(runs) else 0}, block=kvb)
     frags = OF.plan_fragments(t.seg_len, t.parent, cap)
     assert got["frag"][:3] == [0, len(frags), sum(len(f) for f in frags)]
     assert got["frag"][3:] == [int(t.seg_len.sum()), OF.fragment_tokens(frags, t.seg_len)]

@@ -137,8 +137,9 @@ def check_device_tables(T, d):
     check_merged_blocks(T, d)
 
 
-def check_merged_blocks(T, d):
-    """bwd_merged and key_end against the canonical table and the reading above."""
+def check_merged_blocks(T, d, block=BLOCK):
+    """bwd_merged and key_end against the canonical table and the reading above (blocks of
+    ``block`` keys)."""
     bwd, rows, key_end = d["bwd"], d["bwd_merged"], d["key_end"]
     want_end = np.zeros(T, dtype=np.int64)
     seg_of = np.zeros(T, dtype=np.int64)
@@ -148,10 +149,10 @@ def check_merged_blocks(T, d):
     assert key_end.shape == (T,) and (key_end == want_end).all(), "a key's run end is off"
     seen = np.zeros(T, dtype=np.int64)
     for seg, k0, k1, q0, q1 in rows.tolist():
-        assert 0 <= k0 < k1 <= T and k1 - k0 <= BLOCK and q0 == k0, "malformed block"
+        assert 0 <= k0 < k1 <= T and k1 - k0 <= block and q0 == k0, "malformed block"
         assert q1 == key_end[k0] and seg == seg_of[k0], "a block's run is not its first key's"
         assert (key_end[k0:k1] <= q1).all(), "a key seen past its block's run"
-        if k1 - k0 < BLOCK and k1 < T:
+        if k1 - k0 < block and k1 < T:
             assert key_end[k1] > q1, "a partial block stops before the end of its subtree's keys"
         seen[k0:k1] += 1
     assert (seen == 1).all(), "keys not covered exactly once"
